@@ -1,0 +1,207 @@
+"""The oracle: a plain CPU restatement of the Q8_0 block-quantized product.
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()``
+and the benchmark's CPU-baseline leg may import this package.  It shares no
+code with the CUDA library (``q8_block_quantized_gb300``) and imports nothing
+from it; the library never imports this package.
+
+The arithmetic lives in ``q8_oracle.c`` (plain C99, built with gcc at
+``-O2 -ffp-contract=off``); this module only builds that file and passes numpy
+arrays to it.  Each C function cites the page passage it follows:
+
+* "Ferro" README, "How the iGPU path is fast", item 1: Q8_0 weights, per-32
+  activation blocks, int8 dot products.
+* "Ember: packed Q8 decode", the row-contiguous source figure (a block is a
+  scale followed by 32 quants) and the packed 16-row tile figure (544 bytes
+  per 16 blocks).
+
+Every function is pinned by ``tests/test_oracle_pins.py``; none is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "q8_oracle.c")
+_LIB = os.path.join(_HERE, "libq8oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+QK = 32
+BLOCK_BYTES = 34
+EMBER_TILE_BYTES = 544
+
+_CFLAGS = ["-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-Wall", "-Wextra"]
+
+
+def build(force: bool = False) -> str:
+    """Compile q8_oracle.c into libq8oracle.so next to it (gcc, portable C)."""
+    stale = (not os.path.exists(_LIB)
+             or os.path.getmtime(_LIB) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB + ".tmp.%d" % os.getpid()
+        subprocess.run(["gcc", *_CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        f32p = ctypes.POINTER(ctypes.c_float)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        i64 = ctypes.c_int64
+        lib.q8o_f32_to_f16.argtypes = [ctypes.c_float]
+        lib.q8o_f32_to_f16.restype = ctypes.c_uint16
+        lib.q8o_f16_to_f32.argtypes = [ctypes.c_uint16]
+        lib.q8o_f16_to_f32.restype = ctypes.c_float
+        lib.q8o_quantize_block.argtypes = [f32p, u8p]
+        lib.q8o_quantize_rows.argtypes = [f32p, i64, i64, u8p]
+        lib.q8o_block_dots.argtypes = [u8p, i64, i64, u8p, i64, i32p]
+        lib.q8o_gemm.argtypes = [u8p, i64, i64, u8p, i64, f64p, f64p]
+        lib.q8o_quant_gemm.argtypes = [u8p, i64, i64, f32p, i64, u8p, f64p, f64p]
+        lib.q8o_ember_tile_pack.argtypes = [u8p, u8p]
+        lib.q8o_ember_tile_unpack.argtypes = [u8p, u8p]
+        for name in ("q8o_qk", "q8o_block_bytes", "q8o_ember_tile_bytes"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray, ctype):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _f32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _u8(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.uint8)
+
+
+def constants() -> dict:
+    lib = _load()
+    return {"qk": lib.q8o_qk(), "block_bytes": lib.q8o_block_bytes(),
+            "ember_tile_bytes": lib.q8o_ember_tile_bytes()}
+
+
+def f32_to_f16_bits(x) -> np.ndarray:
+    """binary32 -> binary16 bit patterns, round to nearest even (elementwise)."""
+    lib = _load()
+    flat = _f32(x).ravel()
+    out = np.empty(flat.shape, dtype=np.uint16)
+    for i, v in enumerate(flat):
+        out[i] = lib.q8o_f32_to_f16(float(v))
+    return out.reshape(np.shape(x))
+
+
+def f16_bits_to_f32(h) -> np.ndarray:
+    lib = _load()
+    flat = np.ascontiguousarray(h, dtype=np.uint16).ravel()
+    out = np.empty(flat.shape, dtype=np.float32)
+    for i, v in enumerate(flat):
+        out[i] = lib.q8o_f16_to_f32(int(v))
+    return out.reshape(np.shape(h))
+
+
+def quantize(x) -> np.ndarray:
+    """fp32 [rows][K] -> uint8 [rows][K/32*34] Q8_0 blocks."""
+    lib = _load()
+    x = _f32(x)
+    if x.ndim == 1:
+        x = x.reshape(1, -1)
+    rows, K = x.shape
+    if K % QK:
+        raise ValueError("K must be a multiple of 32")
+    out = np.zeros((rows, (K // QK) * BLOCK_BYTES), dtype=np.uint8)
+    lib.q8o_quantize_rows(_ptr(x, ctypes.c_float), rows, K, _ptr(out, ctypes.c_uint8))
+    return out
+
+
+def block_dots(W, A, K: int) -> np.ndarray:
+    """Exact per-block int32 dots: isum[m][n][b]."""
+    lib = _load()
+    W, A = _u8(W), _u8(A)
+    nb = K // QK
+    N = W.size // (nb * BLOCK_BYTES)
+    M = A.size // (nb * BLOCK_BYTES)
+    isum = np.zeros((M, N, nb), dtype=np.int32)
+    lib.q8o_block_dots(_ptr(W, ctypes.c_uint8), N, K, _ptr(A, ctypes.c_uint8), M,
+                       _ptr(isum, ctypes.c_int32))
+    return isum
+
+
+def gemm(W, A, K: int):
+    """(y, S): fp64 outputs [M][N] and the sum of |terms| per output."""
+    lib = _load()
+    W, A = _u8(W), _u8(A)
+    nb = K // QK
+    N = W.size // (nb * BLOCK_BYTES)
+    M = A.size // (nb * BLOCK_BYTES)
+    y = np.zeros((M, N), dtype=np.float64)
+    S = np.zeros((M, N), dtype=np.float64)
+    lib.q8o_gemm(_ptr(W, ctypes.c_uint8), N, K, _ptr(A, ctypes.c_uint8), M,
+                 _ptr(y, ctypes.c_double), _ptr(S, ctypes.c_double))
+    return y, S
+
+
+def quant_gemm(W, x, K: int):
+    """Fused form: quantize fp32 activations x [M][K], then the product.
+    Returns (y, S, A_blocks)."""
+    lib = _load()
+    W, x = _u8(W), _f32(x)
+    if x.ndim == 1:
+        x = x.reshape(1, -1)
+    nb = K // QK
+    N = W.size // (nb * BLOCK_BYTES)
+    M = x.shape[0]
+    A = np.zeros((M, nb * BLOCK_BYTES), dtype=np.uint8)
+    y = np.zeros((M, N), dtype=np.float64)
+    S = np.zeros((M, N), dtype=np.float64)
+    lib.q8o_quant_gemm(_ptr(W, ctypes.c_uint8), N, K, _ptr(x, ctypes.c_float), M,
+                       _ptr(A, ctypes.c_uint8), _ptr(y, ctypes.c_double),
+                       _ptr(S, ctypes.c_double))
+    return y, S, A
+
+
+def ember_tile_pack(blocks16) -> np.ndarray:
+    """16 row-contiguous blocks (uint8 [16][34]) -> one 544-byte Ember record."""
+    lib = _load()
+    src = _u8(blocks16).reshape(16 * BLOCK_BYTES)
+    out = np.zeros(EMBER_TILE_BYTES, dtype=np.uint8)
+    lib.q8o_ember_tile_pack(_ptr(src, ctypes.c_uint8), _ptr(out, ctypes.c_uint8))
+    return out
+
+
+def ember_tile_unpack(tile) -> np.ndarray:
+    lib = _load()
+    src = _u8(tile).reshape(EMBER_TILE_BYTES)
+    out = np.zeros((16, BLOCK_BYTES), dtype=np.uint8)
+    lib.q8o_ember_tile_unpack(_ptr(src, ctypes.c_uint8), _ptr(out, ctypes.c_uint8))
+    return out
+
+
+# --- byte views of a block array (no arithmetic): scale bits and quants -------
+
+def split_blocks(blocks, K: int):
+    """uint8 [rows][K/32*34] -> (d16 bits uint16 [rows][K/32], q int8 [rows][K/32][32])."""
+    b = _u8(blocks)
+    rows = b.size // ((K // QK) * BLOCK_BYTES)
+    b = b.reshape(rows, K // QK, BLOCK_BYTES)
+    d16 = b[:, :, 0].astype(np.uint16) | (b[:, :, 1].astype(np.uint16) << 8)
+    q = b[:, :, 2:].view(np.int8)
+    return d16, q

@@ -1,0 +1,258 @@
+/*
+ * q8_oracle.c -- the ORACLE for the Q8_0 block-quantized decode product.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is a plain, slow, obviously correct CPU
+ * restatement of what the GPU library computes.  Only the test suite, the
+ * smoke check and the benchmark's CPU-baseline leg may load it.  It shares no
+ * code, header, table or helper with the CUDA library and includes nothing
+ * from it; the CUDA library never loads it.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [Ferro]  "Ferro" README (github paragontasx/ferro), section "How the iGPU
+ *            path is fast", item 1: Q8_0 weights, activations quantized per
+ *            32-wide block "llama.cpp's scheme", int8 DP4A dot products.
+ *   [Ember]  "Ember: packed Q8 decode" post (voidwest.dev/ember/
+ *            packed-q8-decode), the row-contiguous source figure
+ *            ("row 0 [scale][q0 q1 ... q31]") and the packed 16-row tile
+ *            figure (eight 64-byte groups of four coordinates for 16 rows,
+ *            then 16 fp16 scales; one record = 544 bytes = 16 blocks).
+ *
+ * Readings taken where the pages are silent (each is listed in the design doc):
+ *   - scale rule: d = amax / 127 in fp32, q = roundf(x * (1/d)) (ties away
+ *     from zero), 1/d taken from the fp32 d (not from the stored fp16), d
+ *     stored as IEEE binary16 rounded to nearest-even, subnormals kept.
+ *   - amax == 0: d = 0, all q = 0.
+ *   - block byte order: fp16 d little-endian at bytes 0..1, q[0..31] at
+ *     bytes 2..33 (34 bytes per block).
+ *   - output: y[m][n] = sum_b isum_b * d_w * d_a, accumulated here in fp64;
+ *     every term is exact in fp64 (20 + 11 + 11 significant bits).
+ *
+ * Build: any C99 compiler, -O2 -ffp-contract=off, no fast-math.  Portable C:
+ * no intrinsics, no inline assembly, no reliance on the signedness of char.
+ *
+ * Every function here is pinned by the CPU tests (tests/test_oracle_pins.py)
+ * against closed forms, library routines (numpy float16), brute force and the
+ * pages' byte accounting.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define QK 32               /* values per block  [Ferro, item 1; Ember figure] */
+#define BLOCK_BYTES 34      /* 2-byte scale + 32 int8                [Ember]   */
+#define EMBER_ROWS 16       /* rows per packed tile                  [Ember]   */
+#define EMBER_TILE_BYTES 544
+
+int q8o_qk(void) { return QK; }
+int q8o_block_bytes(void) { return BLOCK_BYTES; }
+int q8o_ember_tile_bytes(void) { return EMBER_TILE_BYTES; }
+
+/* ---------------------------------------------------------------------------
+ * IEEE-754 binary32 -> binary16, round to nearest, ties to even.
+ * Written from the definition of the two formats: take the 24-bit significand,
+ * shift it to the binary16 grid (13 bits for normal results, more for
+ * subnormal ones), round on the discarded bits, and let a carry out of the
+ * significand bump the exponent (which also produces infinity on overflow).
+ * ------------------------------------------------------------------------- */
+uint16_t q8o_f32_to_f16(float f)
+{
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    uint32_t sign = (bits >> 31) << 15;
+    uint32_t exp = (bits >> 23) & 0xffu;
+    uint32_t mant = bits & 0x7fffffu;
+
+    if (exp == 0xffu)                       /* inf or NaN */
+        return (uint16_t)(sign | 0x7c00u | (mant ? 0x200u : 0u));
+    if (exp == 0u)                          /* zero or fp32 subnormal (< 2^-126) */
+        return (uint16_t)sign;
+
+    int e = (int)exp - 127;                 /* value = sig * 2^(e-23) */
+    uint32_t sig = mant | 0x800000u;        /* 24 significant bits    */
+    int shift;                              /* bits dropped from sig  */
+    if (e >= -14)
+        shift = 13;                         /* binary16 normal: 11-bit significand */
+    else
+        shift = 13 + (-14 - e);             /* binary16 subnormal: grid 2^-24      */
+    if (shift > 24)                         /* below half the smallest subnormal  */
+        return (uint16_t)sign;
+
+    uint32_t r = sig >> shift;
+    uint32_t rem = sig & ((1u << shift) - 1u);
+    uint32_t half = 1u << (shift - 1);
+    if (rem > half || (rem == half && (r & 1u)))
+        r += 1u;
+
+    uint32_t h;
+    if (e >= -14) {
+        if (e > 15)
+            return (uint16_t)(sign | 0x7c00u);
+        /* r in [1024, 2048]; a carry to 2048 moves into the exponent field */
+        h = ((uint32_t)(e + 15) << 10) + (r - 1024u);
+        if (h >= 0x7c00u)
+            h = 0x7c00u;
+    } else {
+        h = r;                              /* r <= 1024; 1024 is the smallest normal */
+    }
+    return (uint16_t)(sign | h);
+}
+
+/* binary16 -> binary32, exact (every binary16 value is a binary32 value). */
+float q8o_f16_to_f32(uint16_t h)
+{
+    uint32_t sign = h >> 15;
+    uint32_t exp = (h >> 10) & 0x1fu;
+    uint32_t mant = h & 0x3ffu;
+    float v;
+    if (exp == 0u)
+        v = ldexpf((float)mant, -24);
+    else if (exp == 31u)
+        v = mant ? NAN : INFINITY;
+    else
+        v = ldexpf((float)(1024u + mant), (int)exp - 25);
+    return sign ? -v : v;
+}
+
+/* ---------------------------------------------------------------------------
+ * Quantize one block of 32 fp32 values to one 34-byte Q8_0 block.
+ * [Ferro, item 1] names the per-32-block activation scheme; the rounding rule
+ * is the reading stated in the header.  All arithmetic is single precision,
+ * one operation at a time, in this order:
+ *   amax = max_i |x_i|;  d = amax / 127;  id = d != 0 ? 1/d : 0;
+ *   q_i = roundf(x_i * id)  (clamped to [-127, 127], which never binds);
+ *   stored scale = binary16(d).
+ * ------------------------------------------------------------------------- */
+void q8o_quantize_block(const float *x, uint8_t *out)
+{
+    float amax = 0.0f;
+    for (int i = 0; i < QK; ++i) {
+        float a = fabsf(x[i]);
+        if (a > amax)
+            amax = a;
+    }
+    float d = amax / 127.0f;
+    float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+    uint16_t d16 = q8o_f32_to_f16(d);
+    out[0] = (uint8_t)(d16 & 0xffu);
+    out[1] = (uint8_t)(d16 >> 8);
+    for (int i = 0; i < QK; ++i) {
+        float v = x[i] * id;
+        float r = roundf(v);
+        if (r > 127.0f) r = 127.0f;
+        if (r < -127.0f) r = -127.0f;
+        int qi = (int)r;
+        out[2 + i] = (uint8_t)(qi & 0xff);   /* two's-complement int8 byte */
+    }
+}
+
+/* Quantize a row-major [rows][K] fp32 matrix to [rows][K/32] blocks. */
+void q8o_quantize_rows(const float *x, int64_t rows, int64_t K, uint8_t *out)
+{
+    int64_t nb = K / QK;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nb; ++b)
+            q8o_quantize_block(x + r * K + b * QK, out + (r * nb + b) * BLOCK_BYTES);
+}
+
+static int8_t q_at(const uint8_t *block, int i)
+{
+    int v = block[2 + i];
+    return (int8_t)(v >= 128 ? v - 256 : v);
+}
+
+static float scale_of(const uint8_t *block)
+{
+    uint16_t h = (uint16_t)(block[0] | ((uint16_t)block[1] << 8));
+    return q8o_f16_to_f32(h);
+}
+
+/* ---------------------------------------------------------------------------
+ * Per-block integer dot products (exact, int32):
+ *   isum[m][n][b] = sum_{i<32} q_w[n][b][i] * q_a[m][b][i]
+ * [Ferro, item 1] (int8 DP4A dot products over per-32-block activations).
+ * W: [N][K/32] blocks, A: [M][K/32] blocks, isum: [M][N][K/32].
+ * ------------------------------------------------------------------------- */
+void q8o_block_dots(const uint8_t *W, int64_t N, int64_t K,
+                    const uint8_t *A, int64_t M, int32_t *isum)
+{
+    int64_t nb = K / QK;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t *wb = W + (n * nb + b) * BLOCK_BYTES;
+                const uint8_t *ab = A + (m * nb + b) * BLOCK_BYTES;
+                int32_t s = 0;
+                for (int i = 0; i < QK; ++i)
+                    s += (int32_t)q_at(wb, i) * (int32_t)q_at(ab, i);
+                isum[(m * N + n) * nb + b] = s;
+            }
+}
+
+/* ---------------------------------------------------------------------------
+ * The product: y[m][n] = sum_b isum_b * d_w[n][b] * d_a[m][b], in fp64, with
+ * the stored (binary16) scales.  Also returns S[m][n] = sum_b |term_b|, the
+ * magnitude the parity tolerance is scaled by.  Either output may be NULL.
+ * ------------------------------------------------------------------------- */
+void q8o_gemm(const uint8_t *W, int64_t N, int64_t K,
+              const uint8_t *A, int64_t M, double *y, double *S)
+{
+    int64_t nb = K / QK;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t *wb = W + (n * nb + b) * BLOCK_BYTES;
+                const uint8_t *ab = A + (m * nb + b) * BLOCK_BYTES;
+                int32_t s = 0;
+                for (int i = 0; i < QK; ++i)
+                    s += (int32_t)q_at(wb, i) * (int32_t)q_at(ab, i);
+                double term = (double)s * (double)scale_of(wb) * (double)scale_of(ab);
+                acc += term;
+                mag += fabs(term);
+            }
+            if (y) y[m * N + n] = acc;
+            if (S) S[m * N + n] = mag;
+        }
+}
+
+/* Quantize fp32 activations, then the product: the fused operation. */
+void q8o_quant_gemm(const uint8_t *W, int64_t N, int64_t K,
+                    const float *x, int64_t M, uint8_t *A_scratch,
+                    double *y, double *S)
+{
+    q8o_quantize_rows(x, M, K, A_scratch);
+    q8o_gemm(W, N, K, A_scratch, M, y, S);
+}
+
+/* ---------------------------------------------------------------------------
+ * [Ember] packed 16-row tile, used only to pin the byte accounting: 16
+ * row-contiguous blocks of one block column become one 544-byte record.
+ * Group g (g = 0..7) holds, for rows 0..15 in order, the four quants
+ * q[4g..4g+3] of that row (64 bytes); then the 16 fp16 scales follow in row
+ * order (32 bytes).  src: 16 blocks (row r at src + 34*r).
+ * ------------------------------------------------------------------------- */
+void q8o_ember_tile_pack(const uint8_t *src, uint8_t *out)
+{
+    uint8_t *p = out;
+    for (int g = 0; g < QK / 4; ++g)
+        for (int r = 0; r < EMBER_ROWS; ++r)
+            for (int k = 0; k < 4; ++k)
+                *p++ = src[r * BLOCK_BYTES + 2 + 4 * g + k];
+    for (int r = 0; r < EMBER_ROWS; ++r) {
+        *p++ = src[r * BLOCK_BYTES + 0];
+        *p++ = src[r * BLOCK_BYTES + 1];
+    }
+}
+
+void q8o_ember_tile_unpack(const uint8_t *tile, uint8_t *dst)
+{
+    const uint8_t *p = tile;
+    for (int g = 0; g < QK / 4; ++g)
+        for (int r = 0; r < EMBER_ROWS; ++r)
+            for (int k = 0; k < 4; ++k)
+                dst[r * BLOCK_BYTES + 2 + 4 * g + k] = *p++;
+    for (int r = 0; r < EMBER_ROWS; ++r) {
+        dst[r * BLOCK_BYTES + 0] = *p++;
+        dst[r * BLOCK_BYTES + 1] = *p++;
+    }
+}
