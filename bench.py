@@ -1,0 +1,384 @@
+"""Benchmark: Q8_0 decode projections of the Llama-3.2-1B stack on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--M 1] [--impl ours|reference]
+
+A step is one decode step of the whole projection stack (16 layers x
+{QKV, O, gate/up, down} + LM head) at M rows: activation quantization, the
+Q8_0 GEMVs and the fused quantize+GEMVs, captured once into a CUDA graph and
+replayed, calls chained with programmatic dependent launch.  The value is
+effective GB/s = (packed weight bytes + fp32 input bytes + fp32 output bytes)
+per step / time per step; tok/s = M / time per step.  Each step streams
+1.32 GB, ten times the 129 MB L2, so no L2 flush is needed between steps.
+
+Under torchrun (N > 1) every rank runs its own replica on its own GPU (the
+path has no exchange step); value = bytes of all ranks / max time over ranks.
+
+--impl reference times the oracle (plain C, one host core) on a bounded
+sample of the same workload and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Q8_0 decode GEMV effective HBM GB/s (% of GB300 peak) and tok/s, M=1–16"
+UNIT = "GB/s"
+DTYPE = "i8*i8->i32, f32 scale+sum"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def _workload_name(shape, M, layers):
+    return "%s q8_0 projection stack (%d layers x qkv/o/gate_up/down + lm_head), decode M=%d" % (
+        shape.name, layers, M)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+CLOCK_Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+           "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+           "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="q8clk", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + CLOCK_Q, "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.dev)],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        sm, mx, pw, reasons = [], None, [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                pw.append(float(r[3]))
+            except ValueError:
+                continue
+            for k, name in enumerate(names):
+                if r[5 + k].lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        # samples under load: power above the idle floor
+        thr = min(pw) + 0.3 * (max(pw) - min(pw)) if pw else 0
+        loaded = [s for s, p in zip(sm, pw) if p >= thr] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm), "samples_loaded": len(loaded),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle, as it stands, on a bounded sample
+# ---------------------------------------------------------------------------
+def cpu_baseline(shape, M, budget_s=12.0):
+    import numpy as np
+
+    import oracle
+    import q8_synth
+    oracle.build()
+    projs = shape.layer_projs()
+    data = []
+    for p in projs:
+        w = q8_synth.normal_np((p.N, p.K), q8_synth.WEIGHT_STD, q8_synth.derive_seed("cpu", p.name))
+        W = oracle.quantize(w)
+        del w
+        x = q8_synth.normal_np((M, p.K), 1.0, q8_synth.derive_seed("cpu-x", p.name))
+        data.append((p, W, x))
+    per_rep = sum(W.nbytes + x.nbytes + M * p.N * 4 for p, W, x in data)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        for p, W, x in data:
+            oracle.quant_gemm(W, x, p.K)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    gbs = per_rep * reps / el / 1e9
+    return {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "layer-0 projections of %s (qkv, o, gate_up, down; %.1f MB of Q8_0 "
+                      "weights) at M=%d, oracle quantize + fp64 product, %d repetitions in "
+                      "%.1f s on 1 host thread" % (shape.name, per_rep / 1e6, M, reps, el)}
+
+
+# ---------------------------------------------------------------------------
+# ours
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    import q8_synth
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        dist.barrier()
+        __graft_entry__.build()  # no-op once built; loads the library
+    import q8_block_quantized_gb300 as q8
+    from q8_block_quantized_gb300.stack import Q8Stack
+
+    shape = q8_synth.LLAMA_3B if args.model == "3b" else q8_synth.LLAMA_1B
+    st = Q8Stack(shape, M=args.M, mode=args.mode, layers=args.layers, seed=rank)
+    graph = st.capture()
+    stream = torch.cuda.current_stream()
+    bytes_step = st.bytes_per_step()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(args.warmup, 3)):
+        graph.replay()
+    barrier()
+
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record(stream)
+    barrier()
+    clocks = sampler.stop() if rank == 0 else None
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    value = bytes_step * world / (ms_max * 1e-3) / 1e9
+
+    # e2e: inputs from pinned host memory, result back to pinned host memory
+    x_host = torch.empty(st.x_all.shape, dtype=torch.float32, pin_memory=True)
+    x_host.copy_(st.x_all.cpu())
+    y_host = torch.empty(st.y_all.shape, dtype=torch.float32, pin_memory=True)
+    for _ in range(3):
+        st.x_all.copy_(x_host, non_blocking=True)
+        graph.replay()
+        y_host.copy_(st.y_all, non_blocking=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        st.x_all.copy_(x_host, non_blocking=True)
+        graph.replay()
+        y_host.copy_(st.y_all, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    ms_e2e = e0.elapsed_time(e1) / args.steps
+    t = torch.tensor([ms_e2e], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_e2e = float(t.item())
+    e2e_value = bytes_step * world / (ms_e2e * 1e-3) / 1e9
+
+    roof = roofline(st, q8) if rank == 0 else None
+    peak, peak_kind = _peaks()
+    if rank == 0:
+        cpu = cpu_baseline(shape, args.M) if (world == 1 and not args.no_cpu) else None
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE,
+            "data": "synthetic: seeded N(0,0.02) weights, N(0,1) activations",
+            "config": {
+                "workload": _workload_name(shape, args.M, st.n_layers), "M": args.M,
+                "layers": st.n_layers, "mode": args.mode, "bytes_per_step": bytes_step,
+                "weight_bytes_per_step": st.weight_bytes(),
+                "l2": "no flush: each step streams %.2f GB > 129 MB L2" % (bytes_step / 1e9),
+                "graph": True, "pdl": True, "parallelism": "replicas" if world > 1 else "single",
+            },
+            "tok_s": round(args.M * world / (ms_max * 1e-3), 1),
+            "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
+            "hbm_peak_gbs": peak, "hbm_peak_kind": peak_kind,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
+                    "h2d_bytes_per_step": st.x_all.numel() * 4,
+                    "d2h_bytes_per_step": st.y_all.numel() * 4,
+                    "ms_per_step": round(ms_e2e, 5)},
+            "gpu_launches": st.launches_per_step() * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def roofline(st, q8, reps=3):
+    """Per-kernel timing of the dominant kernel: the step run call by call with
+    CUDA events around every GEMV launch (no graph, no PDL, so each launch is
+    timed alone); every launch's weights are cold because the rest of the
+    step's 1.3 GB passed through L2 since their last use."""
+    import torch
+    stream = torch.cuda.current_stream()
+    ws = st.workspace
+    agg = {}
+    for _ in range(reps):
+        for c in st.calls:
+            if c.kind == "quant":
+                q8.q8_quantize_act(c.x, c.A)
+                continue
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            if c.kind == "gemm":
+                q8.q8_gemm(c.W, c.N, c.K, c.A, st.M, c.y, workspace=ws)
+                act = c.A.numel()
+            else:
+                q8.q8_fused_quant_gemm(c.W, c.N, c.K, c.x, st.M, c.y, workspace=ws)
+                act = c.x.numel() * 4
+            b.record(stream)
+            key = "gemv_kernel<MT=%d,%s>" % (min(16, 1 << (max(st.M, 1) - 1).bit_length()),
+                                              "fused" if c.kind == "fused" else "blocks")
+            agg.setdefault(key, []).append((c.W.numel() + act + c.y.numel() * 4, a, b))
+    torch.cuda.synchronize()
+    best = None
+    for key, lst in agg.items():
+        tot_b = sum(x[0] for x in lst)
+        tot_ms = sum(x[1].elapsed_time(x[2]) for x in lst)
+        if best is None or tot_ms > best[2]:
+            best = (key, tot_b, tot_ms, len(lst))
+    key, tot_b, tot_ms, n = best
+    peak, kind = _peaks()
+    achieved = tot_b / (tot_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": key, "achieved": round(achieved, 1), "peak": peak,
+            "peak_kind": kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": None, "launches_timed": n,
+            "bytes_per_launch_avg": int(tot_b / n), "ms_per_launch_avg": round(tot_ms / n, 5)}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    import q8_synth
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    shape = q8_synth.LLAMA_3B if args.model == "3b" else q8_synth.LLAMA_1B
+    layers = shape.layers if args.layers is None else args.layers
+    # Each step is one bounded sample of the workload: the first R rows of each
+    # layer-0 projection, R sized so the K timed steps take about a minute.
+    import oracle
+    oracle.build()
+    full = []
+    for p in shape.layer_projs():
+        w = q8_synth.normal_np((p.N, p.K), q8_synth.WEIGHT_STD, q8_synth.derive_seed("cpu", p.name))
+        full.append((p, oracle.quantize(w), q8_synth.normal_np((args.M, p.K), 1.0, 1)))
+        del w
+    t0 = time.perf_counter()
+    for p, W, x in full:
+        oracle.quant_gemm(W, x, p.K)
+    t_layer = time.perf_counter() - t0
+    frac = min(1.0, (60.0 / max(args.steps, 1)) / t_layer)
+    data = []
+    for p, W, x in full:
+        rows = max(1, int(p.N * frac))
+        data.append((p, rows, W[:rows].copy(), x))
+    per_step = sum(W.nbytes + x.nbytes + args.M * rows * 4 for p, rows, W, x in data)
+
+    def one():
+        for p, rows, W, x in data:
+            oracle.quant_gemm(W, x, p.K)
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    el = time.perf_counter() - t0
+    value = per_step * args.steps / el / 1e9
+    cpu = {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": "each step = the first %.1f%% of the output rows of each layer-0 projection "
+                     "(qkv, o, gate_up, down) of %s at M=%d, %.2f MB per step, 1 host thread"
+                     % (100 * frac, shape.name, args.M, per_step / 1e6)}
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "i32 dots, f64 sum",
+        "data": "synthetic: seeded N(0,0.02) weights, N(0,1) activations",
+        "config": {"workload": _workload_name(shape, args.M, layers), "M": args.M,
+                   "sample_bytes_per_step": per_step},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--M", type=int, default=1)
+    ap.add_argument("--model", choices=["1b", "3b"], default="1b")
+    ap.add_argument("--layers", type=int, default=None)
+    ap.add_argument("--mode", choices=["shared", "fused", "unfused"], default="shared")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,214 @@
+/*
+ * q8.h -- C ABI of libq8, the Q8_0 block-quantized decode product on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (sources are web pages, cited by title and section):
+ *
+ *   Q8_0 block: one fp16 scale d followed by 32 int8 quants q, 34 bytes
+ *   ("Ember: packed Q8 decode", the row-contiguous source figure, which shows
+ *   each row's block as a scale and then the quants q0..q31; and the
+ *   packed-tile figure, whose 544-byte record holds exactly 16 blocks).  Byte 0..1: d, IEEE binary16, little-endian;
+ *   bytes 2..33: q[0..31] as two's-complement int8.
+ *
+ *   Activations are quantized once per 32-wide block ("Ferro" README, "How
+ *   the iGPU path is fast", item 1), and one quantization is shared by every
+ *   projection that reads the same input (Ember, the paragraph on the runtime
+ *   pass before the packed layout: Q/K/V share one, gate/up share one).  Rounding rule (the
+ *   llama.cpp-style scheme the Ferro README names; the pages do not spell it
+ *   out): d = amax / 127 in fp32, q_i = roundf(x_i * (1/d)) with ties away
+ *   from zero and 1/d taken from the fp32 d, scale stored as binary16 rounded
+ *   to nearest even; amax == 0 gives d = 0 and q = 0.
+ *
+ *   y[m][n] = sum over blocks b of  isum(n,m,b) * d_w[n][b] * d_a[m][b],
+ *   isum = sum_{i<32} q_w[n][b][i] * q_a[m][b][i] computed exactly in int32
+ *   (Ferro, item 1: int8 DP4A dot products over per-32-block activations).
+ *
+ *   Batch invariance (Ferro README, "Exactness, scheduling and operations",
+ *   "Exactness contract": a decode row gets the same result whatever else is
+ *   batched with it).  Each block term is rounded once in fp32 as
+ *   t_b = float(isum) * (float(d_w) * float(d_a)), where the inner product of
+ *   two binary16 values is exact in fp32, and the terms are summed in fp32 in
+ *   one fixed order: the pairwise tree over the block index b, padded with
+ *   zeros to the next power of two.  The result for (m, n) therefore depends
+ *   only on row n of W, row m of the activations and K: it is bitwise the
+ *   same for every M, every position of the row in the batch, every split of
+ *   the work and every kernel path.
+ *
+ * Conventions for every call:
+ *   - Pointers named W, A_blocks, x, y, workspace, src/dst are DEVICE
+ *     pointers owned by the caller (allocated on the current device); the
+ *     library never frees or retains them after the call returns.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous on that stream; a return of Q8_OK means
+ *     the work was enqueued, not that it finished.
+ *   - Arguments are checked on the host before anything is enqueued; on any
+ *     error nothing is launched and the status says why.  Q8_ECUDA means a
+ *     CUDA runtime call failed (cudaGetLastError is left set).
+ *   - K must be a positive multiple of 32.  Row counts are positive.
+ *   - The library owns no device memory and allocates none in these calls.
+ *   - Only sm_103 devices are accepted (Q8_EDEVICE otherwise).
+ *   - There is no CPU fallback.
+ */
+#ifndef Q8_H
+#define Q8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define Q8_API __attribute__((visibility("default")))
+#else
+#define Q8_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define Q8_QK 32            /* values per block                               */
+#define Q8_BLOCK_BYTES 34   /* bytes per block: fp16 scale + 32 int8          */
+#define Q8_MAX_M 64         /* most activation rows per q8_gemm call          */
+#define Q8_TILE_ROWS 128    /* packed layout: output rows per tile            */
+#define Q8_CHUNK_BLOCKS 8   /* packed layout: blocks per chunk                */
+
+/* Flags for the compute calls. */
+#define Q8_FLAG_PDL 1u      /* launch as a programmatic dependent of the
+                               previous work on the stream (see q8_gemm)     */
+
+typedef enum q8_status {
+    Q8_OK = 0,
+    Q8_EINVAL = -1,      /* null pointer or bad flag                          */
+    Q8_ESHAPE = -2,      /* K not a positive multiple of 32, M or N out of range */
+    Q8_EALIGN = -3,      /* a pointer is not aligned as documented            */
+    Q8_EDEVICE = -4,     /* current device is not sm_103                      */
+    Q8_ECUDA = -5,       /* a CUDA runtime call failed                        */
+    Q8_EWORKSPACE = -6,  /* workspace missing or smaller than required        */
+    Q8_ETIMEOUT = -7     /* (q8_device_error only) a device wait gave up      */
+} q8_status;
+
+/* Human-readable name of a status code.  Static string, never NULL. */
+Q8_API const char *q8_strerror(int status);
+
+/* ABI version of this header/library pair: 1. */
+Q8_API int q8_abi_version(void);
+
+/* Bytes of `rows` rows of K/32 row-contiguous Q8_0 blocks: rows*(K/32)*34. */
+Q8_API size_t q8_blocks_bytes(int64_t rows, int64_t K);
+
+/* Bytes of the packed weight layout for an N x K matrix.  Equal to
+ * q8_blocks_bytes(N, K): repacking moves bytes, it adds none (Ember's packed
+ * tile is likewise exactly the size of the blocks it holds). */
+Q8_API size_t q8_packed_bytes(int64_t N, int64_t K);
+
+/* Workspace bytes q8_gemm / q8_fused_quant_gemm need for this shape on the
+ * current device (0 when the work is not split along K).  Returns 0 for
+ * invalid shapes. */
+Q8_API size_t q8_workspace_bytes(int64_t N, int64_t K, int M);
+
+/*
+ * q8_quantize_act -- quantize fp32 activations to Q8_0 blocks.
+ * (Ferro README, "How the iGPU path is fast", item 1; rounding rule above.)
+ *
+ *   x          [M][K] fp32, row-major, 4-byte aligned.
+ *   M          rows, 1 <= M <= 2^31-1 (also used to quantize weight rows).
+ *   K          positive multiple of 32.
+ *   out_blocks [M][K/32] blocks of 34 bytes, row-contiguous; 2-byte aligned;
+ *              q8_blocks_bytes(M, K) bytes.
+ *   flags      0 or Q8_FLAG_PDL.
+ * Bit-exact with the rule above for finite inputs; NaN/Inf inputs and scales
+ * beyond the binary16 range (amax > 65504*127) are outside the contract.
+ */
+Q8_API int q8_quantize_act(const float *x, int64_t M, int64_t K, void *out_blocks,
+                    unsigned flags, void *stream);
+
+/*
+ * q8_repack_weights -- move row-contiguous Q8_0 weight blocks into the packed
+ * layout the GEMV streams.  A one-time step (Ember repacks each layer's projection
+ * weights once at load time into 16-row tiles; Ferro keeps its device weights
+ * in a coalesced block-major, row-minor layout, item 1).
+ *
+ *   src_blocks [N][K/32] blocks (34 bytes each), 2-byte aligned.
+ *   dst        q8_packed_bytes(N, K) bytes, 16-byte aligned; must not
+ *              overlap src.
+ *
+ * Packed layout (same bytes, new order).  Rows are grouped in tiles of 128
+ * (the last tile holds r = N - 128*t rows), blocks in chunks of 8 (the last
+ * chunk holds kb = K/32 - 8*c blocks).  Tile t starts at byte 128*t*(K/32)*34;
+ * inside it chunk c starts at byte r*8*c*34 and holds, for j < kb, h < 2,
+ * i < r, the 16 quants q[128t+i][8c+j][16h..16h+15] at byte ((2j+h)*r+i)*16,
+ * followed by the kb*r scales, scale (j, i) at byte kb*r*32 + (j*r+i)*2.
+ * Every chunk starts on a 16-byte boundary of dst.
+ */
+Q8_API int q8_repack_weights(const void *src_blocks, int64_t N, int64_t K, void *dst,
+                      void *stream);
+
+/*
+ * q8_gemm -- y = W (Q8_0, packed) times the quantized activations.
+ * (Ferro item 1; Ferro README, "Using LFM2.5 language models": decode batches
+ * of one to four tokens run a GEMV split along K; the exactness contract
+ * above.)
+ *
+ *   W         packed weights from q8_repack_weights, 16-byte aligned.
+ *   N         output rows, 1 <= N <= 2^31-1.
+ *   K         positive multiple of 32.
+ *   A_blocks  [M][K/32] activation blocks (q8_quantize_act), 2-byte aligned.
+ *   M         activation rows, 1 <= M <= Q8_MAX_M.
+ *   y         [M][N] fp32 output, row-major, 4-byte aligned; overwritten.
+ *   workspace q8_workspace_bytes(N, K, M) bytes (may be NULL when that is 0),
+ *             16-byte aligned, zero-filled before its first use.  The call
+ *             leaves it zero-filled again when it completes.  Calls that may
+ *             run at the same time must not share a workspace.
+ *   flags     0 or Q8_FLAG_PDL.  With Q8_FLAG_PDL the kernel is launched as a
+ *             programmatic dependent of the previous work on `stream` and
+ *             starts streaming W before that work has finished; it waits for
+ *             it before reading A_blocks or writing y/workspace.  The caller
+ *             promises that no unfinished earlier work on the stream writes W.
+ */
+Q8_API int q8_gemm(const void *W, int64_t N, int64_t K, const void *A_blocks, int M,
+            float *y, void *workspace, size_t workspace_bytes, unsigned flags,
+            void *stream);
+
+/*
+ * q8_fused_quant_gemm -- quantize fp32 activations inside the GEMV, then the
+ * product (Ferro item 3: the producing kernels emit the next GEMM's int8 input; the
+ * README also measures GEMVs with the quantization fused into their
+ * prologue).  Every CTA quantizes the activation blocks it
+ * needs with the same rule as q8_quantize_act, bit for bit, so
+ * y equals q8_gemm(W, q8_quantize_act(x)) bitwise.
+ *
+ *   x            [M][K] fp32, row-major, 4-byte aligned.
+ *   A_blocks_out optional (may be NULL): receives q8_quantize_act(x), for
+ *                reuse by a later GEMV that reads the same input; 2-byte
+ *                aligned, q8_blocks_bytes(M, K) bytes.
+ *   Other arguments as q8_gemm.
+ */
+Q8_API int q8_fused_quant_gemm(const void *W, int64_t N, int64_t K, const float *x,
+                        int M, float *y, void *A_blocks_out, void *workspace,
+                        size_t workspace_bytes, unsigned flags, void *stream);
+
+/* ---- test hooks (not on the hot path) ----------------------------------- */
+
+/* Inverse of q8_repack_weights: packed (16-byte aligned) -> [N][K/32] blocks
+ * (2-byte aligned). */
+Q8_API int q8_unpack_weights(const void *packed, int64_t N, int64_t K,
+                      void *dst_blocks, void *stream);
+
+/* Exact per-block int32 dots from packed W and activation blocks:
+ * isum[m][n][b] (int32, [M][N][K/32], 4-byte aligned), 1 <= M <= Q8_MAX_M. */
+Q8_API int q8_block_dots(const void *W, int64_t N, int64_t K, const void *A_blocks,
+                  int M, int32_t *isum, void *stream);
+
+/* Read and clear the device-side error word of the current device (waits for
+ * the device).  *code = 0 when no kernel reported a failed wait; otherwise
+ * Q8_ETIMEOUT's magnitude ORed with where it happened.  Returns a status. */
+Q8_API int q8_device_error(unsigned *code);
+
+/* Properties the library uses: SM count and compute capability of the
+ * current device. */
+Q8_API int q8_device_info(int *sm_count, int *cc_major, int *cc_minor);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q8_H */

@@ -10,12 +10,12 @@
  * Sources (web pages, cited by title and section):
  *   [Ferro]  "Ferro" README (github paragontasx/ferro), section "How the iGPU
  *            path is fast", item 1: Q8_0 weights, activations quantized per
- *            32-wide block "llama.cpp's scheme", int8 DP4A dot products.
+ *            32-wide block following llama.cpp, int8 DP4A dot products.
  *   [Ember]  "Ember: packed Q8 decode" post (voidwest.dev/ember/
- *            packed-q8-decode), the row-contiguous source figure
- *            ("row 0 [scale][q0 q1 ... q31]") and the packed 16-row tile
- *            figure (eight 64-byte groups of four coordinates for 16 rows,
- *            then 16 fp16 scales; one record = 544 bytes = 16 blocks).
+ *            packed-q8-decode), the row-contiguous source figure (each row's
+ *            block is a scale, then quants q0..q31) and the packed 16-row
+ *            tile figure (eight 64-byte groups of four coordinates for 16
+ *            rows, then 16 fp16 scales; one record = 544 bytes = 16 blocks).
  *
  * Readings taken where the pages are silent (each is listed in the design doc):
  *   - scale rule: d = amax / 127 in fp32, q = roundf(x * (1/d)) (ties away

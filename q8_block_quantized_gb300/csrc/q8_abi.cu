@@ -1,0 +1,211 @@
+// q8_abi.cu -- the extern "C" entry points of libq8 (declared in q8.h):
+// host-side argument checks, device checks, launch planning, launches.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "q8.h"
+#include "q8_device.cuh"
+#include "q8_internal.h"
+
+namespace q8 {
+
+namespace {
+constexpr int MAX_DEVICES = 64;
+std::mutex g_dev_mu;
+DeviceInfo g_dev_cache[MAX_DEVICES];
+bool g_dev_known[MAX_DEVICES] = {};
+}  // namespace
+
+cudaError_t current_device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= MAX_DEVICES) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_dev_known[dev]) {
+    DeviceInfo d;
+    d.device = dev;
+    if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return e;
+    g_dev_cache[dev] = d;
+    g_dev_known[dev] = true;
+  }
+  *out = g_dev_cache[dev];
+  return cudaSuccess;
+}
+
+}  // namespace q8
+
+using namespace q8;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool k_ok(int64_t K) { return K > 0 && (K % QK) == 0 && K / QK <= ((int64_t)1 << 30); }
+
+// Shared device check: sm_103 only.
+int device_ok(DeviceInfo* d) {
+  if (current_device_info(d) != cudaSuccess) return Q8_ECUDA;
+  if (d->cc_major != 10 || d->cc_minor != 3) return Q8_EDEVICE;
+  return Q8_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? Q8_OK : Q8_ECUDA; }
+
+int check_gemm_common(const void* W, int64_t N, int64_t K, int M, const float* y, unsigned flags) {
+  if (W == nullptr || y == nullptr) return Q8_EINVAL;
+  if ((flags & ~Q8_FLAG_PDL) != 0) return Q8_EINVAL;
+  if (N <= 0 || N > INT32_MAX || !k_ok(K) || M < 1 || M > Q8_MAX_M) return Q8_ESHAPE;
+  if (!aligned(W, 16) || !aligned(y, 4)) return Q8_EALIGN;
+  return Q8_OK;
+}
+
+int check_workspace(const GemvPlan& p, void* ws, size_t ws_bytes) {
+  if (p.ws_bytes == 0) return Q8_OK;
+  if (ws == nullptr || ws_bytes < p.ws_bytes) return Q8_EWORKSPACE;
+  if (!aligned(ws, 16)) return Q8_EALIGN;
+  return Q8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* q8_strerror(int status) {
+  switch (status) {
+    case Q8_OK: return "Q8_OK";
+    case Q8_EINVAL: return "Q8_EINVAL: null pointer or bad flag";
+    case Q8_ESHAPE: return "Q8_ESHAPE: shape out of range (K must be a positive multiple of 32)";
+    case Q8_EALIGN: return "Q8_EALIGN: pointer not aligned as documented";
+    case Q8_EDEVICE: return "Q8_EDEVICE: current device is not sm_103";
+    case Q8_ECUDA: return "Q8_ECUDA: a CUDA runtime call failed";
+    case Q8_EWORKSPACE: return "Q8_EWORKSPACE: workspace missing or too small";
+    case Q8_ETIMEOUT: return "Q8_ETIMEOUT: a device-side wait gave up";
+    default: return "unknown q8 status";
+  }
+}
+
+int q8_abi_version(void) { return 1; }
+
+size_t q8_blocks_bytes(int64_t rows, int64_t K) {
+  if (rows <= 0 || !k_ok(K)) return 0;
+  return (size_t)rows * (size_t)(K / QK) * BLOCK_BYTES;
+}
+
+size_t q8_packed_bytes(int64_t N, int64_t K) { return q8_blocks_bytes(N, K); }
+
+size_t q8_workspace_bytes(int64_t N, int64_t K, int M) {
+  if (N <= 0 || N > INT32_MAX || !k_ok(K) || M < 1 || M > Q8_MAX_M) return 0;
+  DeviceInfo d;
+  if (device_ok(&d) != Q8_OK) return 0;
+  GemvPlan p, pf;
+  if (!plan_gemv(d, N, K, M, false, &p) || !plan_gemv(d, N, K, M, true, &pf)) return 0;
+  return p.ws_bytes > pf.ws_bytes ? p.ws_bytes : pf.ws_bytes;
+}
+
+int q8_quantize_act(const float* x, int64_t M, int64_t K, void* out_blocks, unsigned flags,
+                    void* stream) {
+  if (x == nullptr || out_blocks == nullptr || (flags & ~Q8_FLAG_PDL) != 0) return Q8_EINVAL;
+  if (M <= 0 || M > INT32_MAX || !k_ok(K)) return Q8_ESHAPE;
+  if (!aligned(x, 4) || !aligned(out_blocks, 2)) return Q8_EALIGN;
+  DeviceInfo d;
+  int st = device_ok(&d);
+  if (st != Q8_OK) return st;
+  return cuda_status(launch_quantize(x, M, K, static_cast<uint8_t*>(out_blocks),
+                                     (flags & Q8_FLAG_PDL) != 0, static_cast<cudaStream_t>(stream)));
+}
+
+int q8_repack_weights(const void* src_blocks, int64_t N, int64_t K, void* dst, void* stream) {
+  if (src_blocks == nullptr || dst == nullptr) return Q8_EINVAL;
+  if (N <= 0 || N > INT32_MAX || !k_ok(K)) return Q8_ESHAPE;
+  if (!aligned(src_blocks, 2) || !aligned(dst, 16)) return Q8_EALIGN;
+  DeviceInfo d;
+  int st = device_ok(&d);
+  if (st != Q8_OK) return st;
+  return cuda_status(launch_repack(static_cast<const uint8_t*>(src_blocks), N, K,
+                                   static_cast<uint8_t*>(dst), static_cast<cudaStream_t>(stream)));
+}
+
+int q8_unpack_weights(const void* packed, int64_t N, int64_t K, void* dst_blocks, void* stream) {
+  if (packed == nullptr || dst_blocks == nullptr) return Q8_EINVAL;
+  if (N <= 0 || N > INT32_MAX || !k_ok(K)) return Q8_ESHAPE;
+  if (!aligned(packed, 16) || !aligned(dst_blocks, 2)) return Q8_EALIGN;
+  DeviceInfo d;
+  int st = device_ok(&d);
+  if (st != Q8_OK) return st;
+  return cuda_status(launch_unpack(static_cast<const uint8_t*>(packed), N, K,
+                                   static_cast<uint8_t*>(dst_blocks), static_cast<cudaStream_t>(stream)));
+}
+
+int q8_gemm(const void* W, int64_t N, int64_t K, const void* A_blocks, int M, float* y,
+            void* workspace, size_t workspace_bytes, unsigned flags, void* stream) {
+  if (A_blocks == nullptr) return Q8_EINVAL;
+  int st = check_gemm_common(W, N, K, M, y, flags);
+  if (st != Q8_OK) return st;
+  if (!aligned(A_blocks, 2)) return Q8_EALIGN;
+  DeviceInfo d;
+  if ((st = device_ok(&d)) != Q8_OK) return st;
+  GemvPlan p;
+  if (!plan_gemv(d, N, K, M, false, &p)) return Q8_ESHAPE;
+  if ((st = check_workspace(p, workspace, workspace_bytes)) != Q8_OK) return st;
+  return cuda_status(launch_gemv(p, static_cast<const uint8_t*>(W), static_cast<const uint8_t*>(A_blocks),
+                                 nullptr, nullptr, y, workspace, (flags & Q8_FLAG_PDL) != 0,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+int q8_fused_quant_gemm(const void* W, int64_t N, int64_t K, const float* x, int M, float* y,
+                        void* A_blocks_out, void* workspace, size_t workspace_bytes, unsigned flags,
+                        void* stream) {
+  if (x == nullptr) return Q8_EINVAL;
+  int st = check_gemm_common(W, N, K, M, y, flags);
+  if (st != Q8_OK) return st;
+  if (!aligned(x, 4) || (A_blocks_out != nullptr && !aligned(A_blocks_out, 2))) return Q8_EALIGN;
+  DeviceInfo d;
+  if ((st = device_ok(&d)) != Q8_OK) return st;
+  GemvPlan p;
+  if (!plan_gemv(d, N, K, M, true, &p)) return Q8_ESHAPE;
+  if ((st = check_workspace(p, workspace, workspace_bytes)) != Q8_OK) return st;
+  return cuda_status(launch_gemv(p, static_cast<const uint8_t*>(W), nullptr, x,
+                                 static_cast<uint8_t*>(A_blocks_out), y, workspace,
+                                 (flags & Q8_FLAG_PDL) != 0, static_cast<cudaStream_t>(stream)));
+}
+
+int q8_block_dots(const void* W, int64_t N, int64_t K, const void* A_blocks, int M, int32_t* isum,
+                  void* stream) {
+  if (W == nullptr || A_blocks == nullptr || isum == nullptr) return Q8_EINVAL;
+  if (N <= 0 || N > INT32_MAX || !k_ok(K) || M < 1 || M > Q8_MAX_M) return Q8_ESHAPE;
+  if (!aligned(W, 16) || !aligned(A_blocks, 2) || !aligned(isum, 4)) return Q8_EALIGN;
+  DeviceInfo d;
+  int st = device_ok(&d);
+  if (st != Q8_OK) return st;
+  return cuda_status(launch_block_dots(static_cast<const uint8_t*>(W), N, K,
+                                       static_cast<const uint8_t*>(A_blocks), M, isum,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+int q8_device_error(unsigned* code) {
+  if (code == nullptr) return Q8_EINVAL;
+  DeviceInfo d;
+  int st = device_ok(&d);
+  if (st != Q8_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return Q8_ECUDA;
+  unsigned v = 0;
+  if (read_and_clear_gemv_error(&v) != cudaSuccess) return Q8_ECUDA;
+  *code = v ? ((unsigned)(-Q8_ETIMEOUT) << 8) | v : 0u;
+  return Q8_OK;
+}
+
+int q8_device_info(int* sm_count, int* cc_major, int* cc_minor) {
+  DeviceInfo d;
+  if (current_device_info(&d) != cudaSuccess) return Q8_ECUDA;
+  if (sm_count) *sm_count = d.sm_count;
+  if (cc_major) *cc_major = d.cc_major;
+  if (cc_minor) *cc_minor = d.cc_minor;
+  return Q8_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,188 @@
+// q8_device.cuh -- device-side building blocks shared by the libq8 kernels:
+// the packed layout arithmetic, the quantization rule, the int8 block dot,
+// the canonical block-term rounding and the fixed reduction tree, plus thin
+// wrappers for mbarrier, bulk copy and programmatic-dependent-launch PTX.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "q8.h"
+
+namespace q8 {
+
+constexpr int QK = Q8_QK;
+constexpr int BLOCK_BYTES = Q8_BLOCK_BYTES;
+constexpr int TILE_ROWS = Q8_TILE_ROWS;
+constexpr int CHUNK_BLOCKS = Q8_CHUNK_BLOCKS;
+constexpr int CHUNK_FULL_BYTES = TILE_ROWS * CHUNK_BLOCKS * BLOCK_BYTES;  // 34816
+
+// ---------------------------------------------------------------------------
+// Packed layout (described in q8.h, q8_repack_weights).
+// ---------------------------------------------------------------------------
+__host__ __device__ __forceinline__ int tile_rows(int64_t t, int64_t N) {
+  int64_t r = N - t * TILE_ROWS;
+  return (int)(r < TILE_ROWS ? r : TILE_ROWS);
+}
+__host__ __device__ __forceinline__ int64_t tile_offset(int64_t t, int64_t nb) {
+  return t * TILE_ROWS * nb * BLOCK_BYTES;
+}
+__host__ __device__ __forceinline__ int64_t chunk_offset(int64_t t, int64_t c, int r, int64_t nb) {
+  return tile_offset(t, nb) + (int64_t)r * (c * CHUNK_BLOCKS) * BLOCK_BYTES;
+}
+// byte offset, inside a chunk of kb blocks x r rows, of the 16 quants
+// (block j, half h, row i) and of the scale (block j, row i)
+__host__ __device__ __forceinline__ int chunk_quant_off(int j, int h, int i, int r) {
+  return ((2 * j + h) * r + i) * 16;
+}
+__host__ __device__ __forceinline__ int chunk_scale_off(int j, int i, int r, int kb) {
+  return kb * r * 32 + (j * r + i) * 2;
+}
+
+// ---------------------------------------------------------------------------
+// Quantization of one 32-value block, one value per lane of a full warp.
+// d = amax / 127 (fp32, IEEE division), id = 1/d (0 when d == 0),
+// q = roundf(x * id) (ties away from zero), scale stored as binary16 (RNE).
+// Every operation is an explicitly rounded single-precision intrinsic, so the
+// result does not depend on compiler flags.
+// ---------------------------------------------------------------------------
+struct LaneQuant {
+  int q;            // this lane's quant, in [-127, 127]
+  uint16_t d16;     // the block's binary16 scale bits (same on every lane)
+  float d_stored;   // float value of d16 (what the products use)
+};
+
+__device__ __forceinline__ LaneQuant quantize_lane(float x) {
+  float amax = fabsf(x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float d = __fdiv_rn(amax, 127.0f);
+  const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+  float r = roundf(__fmul_rn(x, id));
+  r = fminf(fmaxf(r, -127.0f), 127.0f);
+  LaneQuant out;
+  out.q = (int)r;
+  const __half h = __float2half_rn(d);
+  out.d16 = __half_as_ushort(h);
+  out.d_stored = __half2float(h);
+  return out;
+}
+
+// ---------------------------------------------------------------------------
+// int8 block dot (exact int32) and the canonical block term.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int dot_block(const uint4& w0, const uint4& w1, const uint4& a0,
+                                         const uint4& a1) {
+  int s = 0;
+  s = __dp4a((int)w0.x, (int)a0.x, s);
+  s = __dp4a((int)w0.y, (int)a0.y, s);
+  s = __dp4a((int)w0.z, (int)a0.z, s);
+  s = __dp4a((int)w0.w, (int)a0.w, s);
+  s = __dp4a((int)w1.x, (int)a1.x, s);
+  s = __dp4a((int)w1.y, (int)a1.y, s);
+  s = __dp4a((int)w1.z, (int)a1.z, s);
+  s = __dp4a((int)w1.w, (int)a1.w, s);
+  return s;
+}
+
+// t_b = float(isum) * (d_w * d_a): the scale product of two binary16 values is
+// exact in fp32, float(isum) is exact (|isum| <= 516128 < 2^24), so the term
+// is rounded exactly once.
+__device__ __forceinline__ float block_term(int isum, float dw, float da) {
+  return __fmul_rn(__int2float_rn(isum), __fmul_rn(dw, da));
+}
+
+__device__ __forceinline__ float tadd(float a, float b) { return __fadd_rn(a, b); }
+
+// ---------------------------------------------------------------------------
+// Small PTX wrappers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on an mbarrier phase: false after `limit_ns` without progress.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+// One contiguous global -> shared bulk copy, completing on `bar` (tx bytes).
+// dst and src 16-byte aligned, bytes a positive multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// Programmatic dependent launch: no-ops when the grid was launched normally.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(const void* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+
+// 32 quants of an unaligned 34-byte block (2-byte aligned) as two uint4.
+// Loads bypass L1 (ld.global.cg): the block may have been written by the
+// kernel this one depends on.
+__device__ __forceinline__ void load_block_quants_u16(const uint8_t* blk, uint4& a0, uint4& a1) {
+  const unsigned short* p = reinterpret_cast<const unsigned short*>(blk + 2);
+  uint32_t w[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    w[k] = (uint32_t)__ldcg(p + 2 * k) | ((uint32_t)__ldcg(p + 2 * k + 1) << 16);
+  a0 = make_uint4(w[0], w[1], w[2], w[3]);
+  a1 = make_uint4(w[4], w[5], w[6], w[7]);
+}
+__device__ __forceinline__ uint16_t load_block_scale_bits(const uint8_t* blk) {
+  return __ldcg(reinterpret_cast<const unsigned short*>(blk));
+}
+
+// Device time limit for every spin on an mbarrier (2 s).
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+
+}  // namespace q8

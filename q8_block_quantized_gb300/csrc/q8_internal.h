@@ -1,0 +1,48 @@
+// q8_internal.h -- host-side launch helpers shared between the libq8
+// translation units (not part of the C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace q8 {
+
+// Launch plan of one GEMV call: the work is cut into units of one 128-row
+// tile x C blocks (C = 8 * 2^k), S units per tile along K.
+struct GemvPlan {
+  int64_t N = 0, K = 0, NB = 0;
+  int M = 0;
+  int MT = 0;        // activation rows per kernel instantiation (1,2,4,8,16)
+  int T = 0;         // row tiles
+  int C = 0;         // blocks per unit
+  int S = 0;         // units per tile (splits along K)
+  int units = 0;
+  int grid = 0;      // persistent CTAs
+  size_t smem = 0;   // dynamic shared memory per CTA
+  size_t ws_bytes = 0;
+};
+
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+};
+
+cudaError_t current_device_info(DeviceInfo* out);
+bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, GemvPlan* p);
+
+// Kernel launchers (q8_aux.cu / q8_gemv.cu).  Each returns the CUDA error of
+// the launch.  `pdl` launches with programmatic stream serialization.
+cudaError_t launch_quantize(const float* x, int64_t M, int64_t K, uint8_t* out, bool pdl,
+                            cudaStream_t s);
+cudaError_t launch_repack(const uint8_t* src, int64_t N, int64_t K, uint8_t* dst, cudaStream_t s);
+cudaError_t launch_unpack(const uint8_t* packed, int64_t N, int64_t K, uint8_t* dst,
+                          cudaStream_t s);
+cudaError_t launch_block_dots(const uint8_t* W, int64_t N, int64_t K, const uint8_t* A, int M,
+                              int32_t* isum, cudaStream_t s);
+cudaError_t launch_gemv(const GemvPlan& p, const uint8_t* W, const uint8_t* A, const float* x,
+                        uint8_t* A_out, float* y, void* workspace, bool pdl, cudaStream_t s);
+cudaError_t read_and_clear_gemv_error(unsigned* code);
+
+}  // namespace q8

@@ -1,0 +1,100 @@
+"""CPU checks of the C ABI: libq8.so builds, loads, exports every function
+include/q8.h declares, the binding covers exactly those, and host-side
+argument checks reject bad calls before anything touches a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            with open(os.path.join(ROOT, "include", fn)) as f:
+                names += re.findall(r"^Q8_API\s+[\w\s\*]*?\b(q8_\w+)\s*\(", f.read(), re.M)
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from q8_block_quantized_gb300 import build
+    build.build()
+    import q8_block_quantized_gb300 as q8
+    return q8.lib()
+
+
+def test_header_declares_the_four_calls():
+    d = set(_declared())
+    for name in ("q8_quantize_act", "q8_repack_weights", "q8_gemm", "q8_fused_quant_gemm"):
+        assert name in d
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 10
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_binding_signatures_match_header(lib):
+    import q8_block_quantized_gb300 as q8
+    assert set(q8.SIGNATURES) == set(_declared())
+
+
+def test_sizes_and_strings(lib):
+    import q8_block_quantized_gb300 as q8
+    assert q8.q8_blocks_bytes(3, 96) == 3 * 3 * 34
+    assert q8.q8_packed_bytes(128256, 2048) == 128256 * 64 * 34
+    assert q8.q8_packed_bytes(7, 33) == 0
+    assert q8.q8_blocks_bytes(0, 32) == 0
+    assert lib.q8_abi_version() == 1
+    for code in (0, -1, -2, -3, -4, -5, -6, -7):
+        assert lib.q8_strerror(code).decode().startswith(q8.STATUS[code])
+
+
+def test_host_argument_checks_reject_before_any_device_work(lib):
+    # every case fails in the host-side checks, which run before the device
+    # is queried; no GPU is needed
+    fake = ctypes.c_void_p(0x10000)      # 16-byte aligned, never dereferenced
+    odd = ctypes.c_void_p(0x10001)
+    y = ctypes.c_void_p(0x20000)
+    g = lib.q8_gemm
+    assert g(None, 8, 64, fake, 1, y, None, 0, 0, None) == -1          # null W
+    assert g(fake, 8, 64, None, 1, y, None, 0, 0, None) == -1          # null A
+    assert g(fake, 8, 64, fake, 1, y, None, 0, 2, None) == -1          # unknown flag
+    assert g(fake, 8, 63, fake, 1, y, None, 0, 0, None) == -2          # K % 32
+    assert g(fake, 8, 0, fake, 1, y, None, 0, 0, None) == -2           # K = 0
+    assert g(fake, 0, 64, fake, 1, y, None, 0, 0, None) == -2          # N = 0
+    assert g(fake, 8, 64, fake, 0, y, None, 0, 0, None) == -2          # M = 0
+    assert g(fake, 8, 64, fake, 65, y, None, 0, 0, None) == -2         # M > 64
+    assert g(odd, 8, 64, fake, 1, y, None, 0, 0, None) == -3           # W misaligned
+    assert g(fake, 8, 64, odd, 1, y, None, 0, 0, None) == -3           # A misaligned
+    f = lib.q8_fused_quant_gemm
+    assert f(fake, 8, 64, None, 1, y, None, None, 0, 0, None) == -1
+    assert f(fake, 8, 64, odd, 1, y, None, None, 0, 0, None) == -3
+    assert f(fake, 8, 64, fake, 1, y, odd, None, 0, 0, None) == -3
+    q = lib.q8_quantize_act
+    assert q(None, 1, 64, fake, 0, None) == -1
+    assert q(fake, 1, 48, fake, 0, None) == -2
+    assert q(fake, -1, 64, fake, 0, None) == -2
+    assert q(odd, 1, 64, fake, 0, None) == -3
+    r = lib.q8_repack_weights
+    assert r(fake, 8, 64, None, None) == -1
+    assert r(fake, 8, 64, ctypes.c_void_p(0x10008), None) == -3        # dst 8-aligned only
+    assert r(fake, 8, 40, fake, None) == -2
+    assert lib.q8_block_dots(fake, 8, 64, fake, 1, odd, None) == -3
+    assert lib.q8_unpack_weights(fake, 8, 64, None, None) == -1
+
+
+def test_no_device_means_an_error_not_a_fallback(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    fake = ctypes.c_void_p(0x10000)
+    st = lib.q8_gemm(fake, 8, 64, fake, 1, fake, None, 0, 0, None)
+    assert st in (-5, -4)
+    assert lib.q8_workspace_bytes(2048, 2048, 1) == 0
