@@ -155,9 +155,13 @@ Q8_API int q8_repack_weights(const void *src_blocks, int64_t N, int64_t K, void 
  *   M         activation rows, 1 <= M <= Q8_MAX_M.
  *   y         [M][N] fp32 output, row-major, 4-byte aligned; overwritten.
  *   workspace q8_workspace_bytes(N, K, M) bytes (may be NULL when that is 0),
- *             16-byte aligned, zero-filled before its first use.  The call
- *             leaves it zero-filled again when it completes.  Calls that may
- *             run at the same time must not share a workspace.
+ *             16-byte aligned.  Its first 16384 bytes hold per-tile tickets
+ *             and must be zero before the first call that uses it; every
+ *             call leaves them zero when it completes, and the rest of the
+ *             workspace is scratch.  One workspace (sized for the largest
+ *             shape) can therefore serve any sequence of calls on one stream;
+ *             calls that may run at the same time must not share one.  After
+ *             q8_device_error reports a failure, zero it again.
  *   flags     0 or Q8_FLAG_PDL.  With Q8_FLAG_PDL the kernel is launched as a
  *             programmatic dependent of the previous work on `stream` and
  *             starts streaming W before that work has finished; it waits for

@@ -41,6 +41,11 @@ constexpr int STAGES = 3;
 constexpr int ACT_SMEM_BUDGET = 36864;      // bytes for one unit's activation blocks
 constexpr int MAX_SPLITS = 128;
 constexpr int SPLIT_LEVELS = 8;             // binary counter levels for S <= 128
+// Workspace layout: a fixed prefix of tile tickets, then the partials.  The
+// prefix has the same size for every call, so partials written by one call
+// never land on the tickets of another call that shares the workspace.
+constexpr int MAX_SPLIT_TILES = 4096;       // split along K only when T <= 4096
+constexpr size_t TICKET_BYTES = (size_t)MAX_SPLIT_TILES * 4;
 
 template <int MT>
 struct MtCfg {
@@ -470,12 +475,20 @@ bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, G
   while (chosen > CHUNK_BLOCKS && chosen / 2 >= q.NB) chosen >>= 1;
   q.C = chosen;
   q.S = (int)((q.NB + q.C - 1) / q.C);
+  if (q.S > 1 && T > MAX_SPLIT_TILES) {
+    // prefer no split for very tall matrices; impossible only when one
+    // unit's activations cannot fit shared memory
+    if ((q.NB + cmax - 1) / cmax > 1) return false;
+    q.C = cmax;
+    while (q.C > CHUNK_BLOCKS && q.C / 2 >= q.NB) q.C >>= 1;
+    q.S = 1;
+  }
   const int64_t units = T * q.S;
   if (units > ((int64_t)1 << 31) - 1) return false;
   q.units = (int)units;
   q.grid = (int)(units < target ? units : target);
   q.smem = smem_of(q.MT);
-  q.ws_bytes = q.S > 1 ? ((size_t)q.T * 4 + 255) / 256 * 256 + (size_t)q.S * Mp * N * 4 : 0;
+  q.ws_bytes = q.S > 1 ? TICKET_BYTES + (size_t)q.S * Mp * N * 4 : 0;
   *p = q;
   return true;
 }
@@ -483,7 +496,7 @@ bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, G
 cudaError_t launch_gemv(const GemvPlan& p, const uint8_t* W, const uint8_t* A, const float* x,
                         uint8_t* A_out, float* y, void* workspace, bool pdl, cudaStream_t s) {
   const bool fused = (x != nullptr);
-  const size_t cnt_bytes = ((size_t)p.T * 4 + 255) / 256 * 256;
+  const size_t cnt_bytes = TICKET_BYTES;
   for (int m0 = 0; m0 < p.M; m0 += 16) {
     const int Mp = (p.M - m0) < 16 ? (p.M - m0) : 16;
     GemvArgs args;

@@ -263,8 +263,25 @@ def test_workspace_left_zero_and_reusable(q8):
         outs.append(y.clone())
     torch.cuda.synchronize()
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
-    nt = (N + 127) // 128
-    assert int(ws[:nt * 4].view(torch.int32).abs().sum()) == 0
+    assert int(ws[:16384].view(torch.int32).abs().sum()) == 0
+
+
+def test_workspace_shared_across_shapes(q8):
+    # one workspace serves calls of different shapes in sequence (tickets
+    # live in a fixed prefix that partials never touch)
+    K, M = 2048, 2
+    shapes = [(2048, 2048), (16384, 2048), (3072, 2048), (2048, 8192), (16384, 2048)]
+    need = max(q8.q8_workspace_bytes(N, K_, M) for N, K_ in shapes)
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    for N, K_ in shapes:
+        w, x = _case(N, K_, M, 9)
+        W = _gpu_pack(q8, w)
+        A = q8.empty_blocks(M, K_)
+        q8.q8_quantize_act(x.to(DEV), A)
+        y = torch.empty((M, N), dtype=torch.float32, device=DEV)
+        q8.q8_gemm(W, N, K_, A, M, y, workspace=ws)
+        own = _run_gemm(q8, W, N, K_, A, M)
+        assert torch.equal(y, own), (N, K_)
 
 
 def test_host_errors_raise(q8):
