@@ -148,6 +148,25 @@ def cpu_baseline(shape, M, budget_s=12.0):
 
 
 # ---------------------------------------------------------------------------
+# multi-rank bookkeeping (replicas: no data-path collective)
+# ---------------------------------------------------------------------------
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest rank's time per step (all_reduce MAX); `ms` itself at N=1."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(bytes_per_step_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job effective GB/s: the bytes every rank processed / the max time."""
+    return bytes_per_step_per_rank * world / (ms_max * 1e-3) / 1e9
+
+
+# ---------------------------------------------------------------------------
 # ours
 # ---------------------------------------------------------------------------
 def run_ours(args):
@@ -198,11 +217,8 @@ def run_ours(args):
     barrier()
     clocks = sampler.stop() if rank == 0 else None
     ms = e0.elapsed_time(e1) / args.steps
-    ms_t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
-    value = bytes_step * world / (ms_max * 1e-3) / 1e9
+    ms_max = max_over_ranks(ms, world, device="cuda")
+    value = aggregate_gbs(bytes_step, world, ms_max)
 
     # e2e: inputs from pinned host memory, result back to pinned host memory
     x_host = torch.empty(st.x_all.shape, dtype=torch.float32, pin_memory=True)
@@ -220,12 +236,8 @@ def run_ours(args):
         y_host.copy_(st.y_all, non_blocking=True)
     e1.record(stream)
     barrier()
-    ms_e2e = e0.elapsed_time(e1) / args.steps
-    t = torch.tensor([ms_e2e], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_e2e = float(t.item())
-    e2e_value = bytes_step * world / (ms_e2e * 1e-3) / 1e9
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device="cuda")
+    e2e_value = aggregate_gbs(bytes_step, world, ms_e2e)
 
     roof = roofline(st, q8) if rank == 0 else None
     peak, peak_kind = _peaks()
@@ -261,46 +273,74 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def kernel_class(q8, c, M):
+    """The GEMV kernel instantiation a call runs: packed tile height, rows per
+    pass, fused or not (the names ncu shows as gemv_kernel<R, MT, fused>)."""
+    mt = min(16, 1 << (max(M, 1) - 1).bit_length())
+    return "gemv_kernel<%d,%d,%d>" % (q8.q8_packed_tile_rows(c.N), mt, 1 if c.kind == "fused" else 0)
+
+
 def roofline(st, q8, reps=3):
-    """Per-kernel timing of the dominant kernel: the step run call by call with
-    CUDA events around every GEMV launch (no graph, no PDL, so each launch is
-    timed alone); every launch's weights are cold because the rest of the
-    step's 1.3 GB passed through L2 since their last use."""
+    """Roofline of the dominant kernel.  For every GEMV kernel instantiation
+    the step's calls that run it are captured, in step order, into a CUDA
+    graph of their own (no programmatic dependent launch, so each launch runs
+    alone) and timed with CUDA events on the stream it is replayed on.  Every class
+    streams more than 300 MB of distinct weights per replay, more than L2
+    holds, so each launch reads its weights from HBM.  The dominant kernel is
+    the class with the largest time per step; achieved = its algorithmic
+    bytes (packed weights + fp32 input + fp32 output per launch) / its time."""
     import torch
-    stream = torch.cuda.current_stream()
     ws = st.workspace
-    agg = {}
-    for _ in range(reps):
-        for c in st.calls:
-            if c.kind == "quant":
-                q8.q8_quantize_act(c.x, c.A)
-                continue
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
+    classes = {}
+    for c in st.calls:
+        if c.kind == "quant":
+            continue
+        classes.setdefault(kernel_class(q8, c, st.M), []).append(c)
+
+    def run(calls):
+        for c in calls:
             if c.kind == "gemm":
                 q8.q8_gemm(c.W, c.N, c.K, c.A, st.M, c.y, workspace=ws)
-                act = c.A.numel()
             else:
                 q8.q8_fused_quant_gemm(c.W, c.N, c.K, c.x, st.M, c.y, workspace=ws)
-                act = c.x.numel() * 4
-            b.record(stream)
-            key = "gemv_kernel<MT=%d,%s>" % (min(16, 1 << (max(st.M, 1) - 1).bit_length()),
-                                              "fused" if c.kind == "fused" else "blocks")
-            agg.setdefault(key, []).append((c.W.numel() + act + c.y.numel() * 4, a, b))
-    torch.cuda.synchronize()
-    best = None
-    for key, lst in agg.items():
-        tot_b = sum(x[0] for x in lst)
-        tot_ms = sum(x[1].elapsed_time(x[2]) for x in lst)
-        if best is None or tot_ms > best[2]:
-            best = (key, tot_b, tot_ms, len(lst))
-    key, tot_b, tot_ms, n = best
+
+    rows = []
+    for key, calls in classes.items():
+        stream = torch.cuda.Stream()
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            run(calls)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            run(calls)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        best = None
+        cur = torch.cuda.current_stream()  # replay() launches on the current stream
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(cur)
+            g.replay()
+            b.record(cur)
+            b.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        nbytes = sum(c.W.numel() + 4 * c.x.numel() + 4 * c.y.numel() if c.kind == "fused"
+                     else c.W.numel() + c.A.numel() + 4 * c.y.numel() for c in calls)
+        rows.append((best, key, nbytes, len(calls)))
+        del g
+    rows.sort(reverse=True)
+    ms, key, nbytes, n = rows[0]
     peak, kind = _peaks()
-    achieved = tot_b / (tot_ms * 1e-3) / 1e9
+    achieved = nbytes / (ms * 1e-3) / 1e9
     return {"bound": "hbm", "kernel": key, "achieved": round(achieved, 1), "peak": peak,
             "peak_kind": kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "traffic": None, "launches_timed": n,
-            "bytes_per_launch_avg": int(tot_b / n), "ms_per_launch_avg": round(tot_ms / n, 5)}
+            "traffic": None, "launches_per_step": n,
+            "bytes_per_launch_avg": int(nbytes / n), "us_per_launch_avg": round(ms * 1e3 / n, 3),
+            "classes": {k: {"launches": nn, "us": round(t * 1e3, 2), "GB/s": round(b / (t * 1e-3) / 1e9, 1)}
+                        for t, k, b, nn in rows}}
 
 
 # ---------------------------------------------------------------------------
@@ -370,7 +410,7 @@ def main():
     ap.add_argument("--M", type=int, default=1)
     ap.add_argument("--model", choices=["1b", "3b"], default="1b")
     ap.add_argument("--layers", type=int, default=None)
-    ap.add_argument("--mode", choices=["shared", "fused", "unfused"], default="shared")
+    ap.add_argument("--mode", choices=["shared", "fused", "unfused"], default="fused")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     args = ap.parse_args()

@@ -68,7 +68,7 @@ extern "C" {
 #define Q8_QK 32            /* values per block                               */
 #define Q8_BLOCK_BYTES 34   /* bytes per block: fp16 scale + 32 int8          */
 #define Q8_MAX_M 64         /* most activation rows per q8_gemm call          */
-#define Q8_TILE_ROWS 128    /* packed layout: output rows per tile            */
+#define Q8_MAX_TILE_ROWS 128 /* packed layout: most output rows per tile       */
 #define Q8_CHUNK_BLOCKS 8   /* packed layout: blocks per chunk                */
 
 /* Flags for the compute calls. */
@@ -99,6 +99,10 @@ Q8_API size_t q8_blocks_bytes(int64_t rows, int64_t K);
  * q8_blocks_bytes(N, K): repacking moves bytes, it adds none (Ember's packed
  * tile is likewise exactly the size of the blocks it holds). */
 Q8_API size_t q8_packed_bytes(int64_t N, int64_t K);
+
+/* Rows per tile of the packed layout of an N-row matrix (16, 32, 64 or
+ * 128; see q8_repack_weights).  Returns 0 for N <= 0. */
+Q8_API int q8_packed_tile_rows(int64_t N);
 
 /* Workspace bytes q8_gemm / q8_fused_quant_gemm need for this shape on the
  * current device (0 when the work is not split along K).  Returns 0 for
@@ -131,13 +135,17 @@ Q8_API int q8_quantize_act(const float *x, int64_t M, int64_t K, void *out_block
  *   dst        q8_packed_bytes(N, K) bytes, 16-byte aligned; must not
  *              overlap src.
  *
- * Packed layout (same bytes, new order).  Rows are grouped in tiles of 128
- * (the last tile holds r = N - 128*t rows), blocks in chunks of 8 (the last
- * chunk holds kb = K/32 - 8*c blocks).  Tile t starts at byte 128*t*(K/32)*34;
- * inside it chunk c starts at byte r*8*c*34 and holds, for j < kb, h < 2,
- * i < r, the 16 quants q[128t+i][8c+j][16h..16h+15] at byte ((2j+h)*r+i)*16,
- * followed by the kb*r scales, scale (j, i) at byte kb*r*32 + (j*r+i)*2.
- * Every chunk starts on a 16-byte boundary of dst.
+ * Packed layout (same bytes, new order).  Rows are grouped in tiles of R
+ * rows, R = q8_packed_tile_rows(N): the smallest of 16, 32, 64 for which the
+ * tile count ceil(N/R) is at most 152 (about one tile per SM of a GB300),
+ * else 128.  The last tile holds r = N - R*t rows.  Blocks are grouped in
+ * chunks of 8 (the last chunk holds kb = K/32 - 8*c blocks).  Tile t starts
+ * at byte R*t*(K/32)*34; inside it chunk c starts at byte r*8*c*34 and holds,
+ * for j < kb, h < 2, i < r, the 16 quants q[R*t+i][8c+j][16h..16h+15] at byte
+ * ((2j+h)*r+i)*16, followed by the kb*r scales, scale (j, i) at byte
+ * kb*r*32 + (j*r+i)*2.  Every chunk starts on a 16-byte boundary of dst, and
+ * the chunks of a tile are contiguous, so a kernel streams each chunk with
+ * one bulk copy.
  */
 Q8_API int q8_repack_weights(const void *src_blocks, int64_t N, int64_t K, void *dst,
                       void *stream);
@@ -180,7 +188,7 @@ Q8_API int q8_gemm(const void *W, int64_t N, int64_t K, const void *A_blocks, in
  * needs with the same rule as q8_quantize_act, bit for bit, so
  * y equals q8_gemm(W, q8_quantize_act(x)) bitwise.
  *
- *   x            [M][K] fp32, row-major, 4-byte aligned.
+ *   x            [M][K] fp32, row-major, 16-byte aligned.
  *   A_blocks_out optional (may be NULL): receives q8_quantize_act(x), for
  *                reuse by a later GEMV that reads the same input; 2-byte
  *                aligned, q8_blocks_bytes(M, K) bytes.

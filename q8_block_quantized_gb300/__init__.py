@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libq8.so")
 QK = 32
 BLOCK_BYTES = 34
 MAX_M = 64
-TILE_ROWS = 128
+MAX_TILE_ROWS = 128
 CHUNK_BLOCKS = 8
 FLAG_PDL = 1
 
@@ -36,6 +36,7 @@ SIGNATURES = {
     "q8_abi_version": (_int, []),
     "q8_blocks_bytes": (_sz, [_i64, _i64]),
     "q8_packed_bytes": (_sz, [_i64, _i64]),
+    "q8_packed_tile_rows": (_int, [_i64]),
     "q8_workspace_bytes": (_sz, [_i64, _i64, _int]),
     "q8_quantize_act": (_int, [_vp, _i64, _i64, _vp, _u, _vp]),
     "q8_repack_weights": (_int, [_vp, _i64, _i64, _vp, _vp]),
@@ -107,6 +108,10 @@ def q8_blocks_bytes(rows: int, K: int) -> int:
 
 def q8_packed_bytes(N: int, K: int) -> int:
     return int(lib().q8_packed_bytes(N, K))
+
+
+def q8_packed_tile_rows(N: int) -> int:
+    return int(lib().q8_packed_tile_rows(N))
 
 
 def q8_workspace_bytes(N: int, K: int, M: int) -> int:

@@ -18,8 +18,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libq8.so")
 
-SOURCES = ["q8_abi.cu", "q8_aux.cu", "q8_gemv.cu"]
-HEADERS = ["q8_device.cuh", "q8_internal.h"]
+SOURCES = ["q8_abi.cu", "q8_aux.cu", "q8_gemv.cu", "q8_gemv_r16.cu", "q8_gemv_r32.cu",
+           "q8_gemv_r64.cu", "q8_gemv_r128.cu"]
+HEADERS = ["q8_device.cuh", "q8_internal.h", "q8_gemv_impl.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

@@ -98,6 +98,8 @@ size_t q8_blocks_bytes(int64_t rows, int64_t K) {
 
 size_t q8_packed_bytes(int64_t N, int64_t K) { return q8_blocks_bytes(N, K); }
 
+int q8_packed_tile_rows(int64_t N) { return N > 0 ? layout_tile_rows(N) : 0; }
+
 size_t q8_workspace_bytes(int64_t N, int64_t K, int M) {
   if (N <= 0 || N > INT32_MAX || !k_ok(K) || M < 1 || M > Q8_MAX_M) return 0;
   DeviceInfo d;
@@ -163,7 +165,7 @@ int q8_fused_quant_gemm(const void* W, int64_t N, int64_t K, const float* x, int
   if (x == nullptr) return Q8_EINVAL;
   int st = check_gemm_common(W, N, K, M, y, flags);
   if (st != Q8_OK) return st;
-  if (!aligned(x, 4) || (A_blocks_out != nullptr && !aligned(A_blocks_out, 2))) return Q8_EALIGN;
+  if (!aligned(x, 16) || (A_blocks_out != nullptr && !aligned(A_blocks_out, 2))) return Q8_EALIGN;
   DeviceInfo d;
   if ((st = device_ok(&d)) != Q8_OK) return st;
   GemvPlan p;

@@ -35,21 +35,22 @@ __global__ void __launch_bounds__(QUANT_THREADS) quantize_kernel(const float* __
 // `rows` holds [N][nb] row-contiguous blocks, `packed` the packed layout;
 // inverse == false copies rows -> packed, inverse == true packed -> rows.
 __global__ void repack_kernel(uint8_t* rows, int64_t N, int64_t nb, uint8_t* packed, bool inverse) {
-  const int64_t T = (N + TILE_ROWS - 1) / TILE_ROWS;
-  const int64_t total = T * nb * TILE_ROWS;
+  const int R = layout_tile_rows(N);
+  const int64_t T = (N + R - 1) / R;
+  const int64_t total = T * nb * R;
   for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
        g += (int64_t)gridDim.x * blockDim.x) {
-    const int i = (int)(g % TILE_ROWS);
-    const int64_t rest = g / TILE_ROWS;
+    const int i = (int)(g % R);
+    const int64_t rest = g / R;
     const int64_t b = rest % nb;
     const int64_t t = rest / nb;
-    const int r = tile_rows(t, N);
+    const int r = tile_rows(t, N, R);
     if (i >= r) continue;
-    const int64_t n = t * TILE_ROWS + i;
+    const int64_t n = t * R + i;
     const int64_t c = b / CHUNK_BLOCKS;
     const int j = (int)(b % CHUNK_BLOCKS);
-    const int kb = (int)((nb - c * CHUNK_BLOCKS) < CHUNK_BLOCKS ? (nb - c * CHUNK_BLOCKS) : CHUNK_BLOCKS);
-    uint8_t* chunk = packed + chunk_offset(t, c, r, nb);
+    const int kb = chunk_blocks(c, nb);
+    uint8_t* chunk = packed + chunk_offset(t, c, r, R, nb);
     uint16_t* s16 = reinterpret_cast<uint16_t*>(rows + (n * nb + b) * BLOCK_BYTES);
     uint4* q0 = reinterpret_cast<uint4*>(chunk + chunk_quant_off(j, 0, i, r));
     uint4* q1 = reinterpret_cast<uint4*>(chunk + chunk_quant_off(j, 1, i, r));
@@ -86,12 +87,13 @@ __global__ void block_dots_kernel(const uint8_t* __restrict__ W, int64_t N, int6
     const int64_t b = g % nb;
     const int64_t n = (g / nb) % N;
     const int64_t m = g / (nb * N);
-    const int64_t t = n / TILE_ROWS;
-    const int i = (int)(n % TILE_ROWS);
-    const int r = tile_rows(t, N);
+    const int R = layout_tile_rows(N);
+    const int64_t t = n / R;
+    const int i = (int)(n % R);
+    const int r = tile_rows(t, N, R);
     const int64_t c = b / CHUNK_BLOCKS;
     const int j = (int)(b % CHUNK_BLOCKS);
-    const uint8_t* chunk = W + chunk_offset(t, c, r, nb);
+    const uint8_t* chunk = W + chunk_offset(t, c, r, R, nb);
     const uint4 w0 = *reinterpret_cast<const uint4*>(chunk + chunk_quant_off(j, 0, i, r));
     const uint4 w1 = *reinterpret_cast<const uint4*>(chunk + chunk_quant_off(j, 1, i, r));
     uint4 a0, a1;
@@ -112,6 +114,10 @@ int grid_for(int64_t work, int per_cta) {
 cudaError_t launch_quantize(const float* x, int64_t M, int64_t K, uint8_t* out, bool pdl,
                             cudaStream_t s) {
   const int64_t nblocks = M * (K / QK);
+  // same carveout as the GEMV kernels, so it can share SMs with them
+  cudaError_t e = cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid_for(nblocks, QUANT_THREADS / 32));
   cfg.blockDim = dim3(QUANT_THREADS);
@@ -127,7 +133,8 @@ cudaError_t launch_quantize(const float* x, int64_t M, int64_t K, uint8_t* out, 
 
 cudaError_t launch_repack(const uint8_t* src, int64_t N, int64_t K, uint8_t* dst, cudaStream_t s) {
   const int64_t nb = K / QK;
-  const int64_t total = ((N + TILE_ROWS - 1) / TILE_ROWS) * nb * TILE_ROWS;
+  const int R = layout_tile_rows(N);
+  const int64_t total = ((N + R - 1) / R) * nb * R;
   repack_kernel<<<grid_for(total, 256), 256, 0, s>>>(const_cast<uint8_t*>(src), N, nb, dst, false);
   return cudaGetLastError();
 }
@@ -135,7 +142,8 @@ cudaError_t launch_repack(const uint8_t* src, int64_t N, int64_t K, uint8_t* dst
 cudaError_t launch_unpack(const uint8_t* packed, int64_t N, int64_t K, uint8_t* dst,
                           cudaStream_t s) {
   const int64_t nb = K / QK;
-  const int64_t total = ((N + TILE_ROWS - 1) / TILE_ROWS) * nb * TILE_ROWS;
+  const int R = layout_tile_rows(N);
+  const int64_t total = ((N + R - 1) / R) * nb * R;
   repack_kernel<<<grid_for(total, 256), 256, 0, s>>>(dst, N, nb, const_cast<uint8_t*>(packed), true);
   return cudaGetLastError();
 }

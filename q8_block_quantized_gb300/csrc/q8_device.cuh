@@ -13,22 +13,33 @@ namespace q8 {
 
 constexpr int QK = Q8_QK;
 constexpr int BLOCK_BYTES = Q8_BLOCK_BYTES;
-constexpr int TILE_ROWS = Q8_TILE_ROWS;
+constexpr int MAX_TILE_ROWS = 128;
 constexpr int CHUNK_BLOCKS = Q8_CHUNK_BLOCKS;
-constexpr int CHUNK_FULL_BYTES = TILE_ROWS * CHUNK_BLOCKS * BLOCK_BYTES;  // 34816
+// Tile count the packed layout aims at: about one tile per SM of a GB300.
+constexpr int LAYOUT_TARGET_TILES = 152;
 
 // ---------------------------------------------------------------------------
-// Packed layout (described in q8.h, q8_repack_weights).
+// Packed layout (described in q8.h, q8_repack_weights).  Rows are grouped in
+// tiles of R rows (R depends only on N), blocks in chunks of 8.
 // ---------------------------------------------------------------------------
-__host__ __device__ __forceinline__ int tile_rows(int64_t t, int64_t N) {
-  int64_t r = N - t * TILE_ROWS;
-  return (int)(r < TILE_ROWS ? r : TILE_ROWS);
+__host__ __device__ __forceinline__ int layout_tile_rows(int64_t N) {
+  for (int R = 16; R < MAX_TILE_ROWS; R *= 2)
+    if ((N + R - 1) / R <= LAYOUT_TARGET_TILES) return R;
+  return MAX_TILE_ROWS;
 }
-__host__ __device__ __forceinline__ int64_t tile_offset(int64_t t, int64_t nb) {
-  return t * TILE_ROWS * nb * BLOCK_BYTES;
+__host__ __device__ __forceinline__ int tile_rows(int64_t t, int64_t N, int R) {
+  int64_t r = N - t * R;
+  return (int)(r < R ? r : R);
 }
-__host__ __device__ __forceinline__ int64_t chunk_offset(int64_t t, int64_t c, int r, int64_t nb) {
-  return tile_offset(t, nb) + (int64_t)r * (c * CHUNK_BLOCKS) * BLOCK_BYTES;
+__host__ __device__ __forceinline__ int64_t tile_offset(int64_t t, int R, int64_t nb) {
+  return t * R * nb * BLOCK_BYTES;
+}
+__host__ __device__ __forceinline__ int64_t chunk_offset(int64_t t, int64_t c, int r, int R, int64_t nb) {
+  return tile_offset(t, R, nb) + (int64_t)r * (c * CHUNK_BLOCKS) * BLOCK_BYTES;
+}
+__host__ __device__ __forceinline__ int chunk_blocks(int64_t c, int64_t nb) {
+  const int64_t k = nb - c * CHUNK_BLOCKS;
+  return (int)(k < CHUNK_BLOCKS ? k : CHUNK_BLOCKS);
 }
 // byte offset, inside a chunk of kb blocks x r rows, of the 16 quants
 // (block j, half h, row i) and of the scale (block j, row i)
@@ -66,6 +77,45 @@ __device__ __forceinline__ LaneQuant quantize_lane(float x) {
   out.d16 = __half_as_ushort(h);
   out.d_stored = __half2float(h);
   return out;
+}
+
+// The same rule for one block held by one thread (32 values in 8 float4):
+// the same single-precision results, so the bits match quantize_lane's.
+//  - amax: max is exact and order-free, so a tree of maxima is used;
+//  - 1/d: __frcp_rn is the correctly rounded reciprocal, i.e. the IEEE
+//    quotient 1/d;
+//  - no clamp: |x * (1/d)| <= 127 * (1 + 2^-22) < 127.5 for every value of
+//    the block, so roundf already lands in [-127, 127].
+// packed[k] holds quants 4k..4k+3, low byte first.
+// cvt.pack.sat.s8.s32.b32 d, x, y, z puts y in byte 0, x in byte 1 and the
+// low 16 bits of z in bytes 2-3; so (a, b, c, d) land in bytes 0..3.
+__device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
+  uint32_t hi, r;
+  asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, 0;" : "=r"(hi) : "r"(d), "r"(c));
+  asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(b), "r"(a), "r"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void quantize_block_thread(const float4 (&v)[8], uint32_t (&packed)[8],
+                                                      float& d_stored) {
+  float m4[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const float a0 = fmaxf(fabsf(v[2 * c].x), fabsf(v[2 * c].y));
+    const float a1 = fmaxf(fabsf(v[2 * c].z), fabsf(v[2 * c].w));
+    const float a2 = fmaxf(fabsf(v[2 * c + 1].x), fabsf(v[2 * c + 1].y));
+    const float a3 = fmaxf(fabsf(v[2 * c + 1].z), fabsf(v[2 * c + 1].w));
+    m4[c] = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+  }
+  const float amax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+  const float d = __fdiv_rn(amax, 127.0f);
+  const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    packed[k] = pack4_s8((int)roundf(__fmul_rn(v[k].x, id)), (int)roundf(__fmul_rn(v[k].y, id)),
+                         (int)roundf(__fmul_rn(v[k].z, id)), (int)roundf(__fmul_rn(v[k].w, id)));
+  }
+  d_stored = __half2float(__float2half_rn(d));
 }
 
 // ---------------------------------------------------------------------------
@@ -149,11 +199,54 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+// Bulk prefetch of a contiguous range into L2 (no shared-memory destination).
+// src 16-byte aligned, bytes a positive multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+// Thread-block clusters: rank, size, barrier, distributed shared memory.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// all threads of every warp that calls these must call them together
+__device__ __forceinline__ void cluster_arrive_aligned() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_aligned() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// arrival of a single thread (no wait)
+__device__ __forceinline__ void cluster_arrive_one() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+// address of the same shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                              uint32_t d) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 // Programmatic dependent launch: no-ops when the grid was launched normally.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -1,0 +1,762 @@
+// q8_gemv_impl.cuh -- the Q8_0 decode GEMV kernel (int8 dot products on the
+// DP4A path), templated on the packed tile height R, the activation rows per
+// pass MT and whether the activation is quantized in the kernel (FUSED).
+//
+// Work decomposition.  The packed layout groups rows in tiles of R rows
+// (R in {16, 32, 64, 128}, chosen from N so a matrix has about one tile per
+// SM) and blocks in chunks of 8.  A work unit is one tile times CU aligned
+// chunks (CU a power of two); usually CU covers all of K and a tile is one
+// unit.  Inside the CTA the 128 consumer threads are R rows x P = 128/R
+// K-parts: thread (i, p) owns row i and the p-th aligned slice of cpp = CU/P
+// chunks of the unit.  The stages of the pipeline are rounds: in round rho
+// every part's chunk number rho lands in shared memory (P bulk copies, one
+// per part, placed at staggered offsets so the parts' reads do not collide
+// in the banks).
+//
+// Pipeline.  Warp 4 is the producer: one lane issues cp.async.bulk copies
+// (the chunks are contiguous and 16-byte aligned in the packed layout) into
+// a ring of stages, completing on mbarriers.  Warps 0-3 consume: for each
+// block of its chunk, a thread computes the exact int32 dot of its row with
+// every activation row (__dp4a), the canonical term
+// t_b = float(isum) * (d_w * d_a), and the pairwise tree of the chunk.
+//
+// Reduction order.  The sum over blocks b is the pairwise tree over b,
+// padded with zeros to a power of two.  A chunk (8 aligned blocks) is a
+// subtree; a thread merges its chunk values with a binary counter (merge
+// with the left sibling while the index bit is 1; what is left at the end
+// merges from the lowest level up, which is what zero padding gives), so a
+// part (cpp aligned chunks) is a subtree; the P parts of a row sit in P
+// consecutive lanes and a butterfly (shuffle-xor 1, 2, 4, ...) merges them,
+// each step adding two aligned sibling subtrees.  A unit is therefore a
+// subtree too, and when a tile is split along K into S > 1 units, the unit
+// values are merged the same way.  The result for an output depends only on
+// its row of W, its row of activations and K.
+//
+// Split along K (S > 1: large K with many activation rows, or few tiles).
+// Each unit writes its row values to the workspace and takes a ticket on the
+// tile's counter; the CTA holding the last ticket merges the S values in
+// index order, writes y and resets the counter.  No CTA waits for another.
+//
+// Programmatic dependent launch.  The producer starts streaming W at once
+// (W is immutable); the consumers execute griddepcontrol.wait before reading
+// activations or writing anything.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "q8_device.cuh"
+#include "q8_internal.h"
+
+namespace q8 {
+
+constexpr int MAX_SPLITS = 128;
+constexpr int SPLIT_LEVELS = 8;  // binary counter levels for S <= 128
+// Workspace layout: a fixed prefix of tile tickets, then the partials.  The
+// prefix has the same size for every call, so partials written by one call
+// never land on the tickets of another call that shares the workspace.
+constexpr int MAX_SPLIT_TILES = 4096;
+constexpr size_t TICKET_BYTES = (size_t)MAX_SPLIT_TILES * 4;
+
+enum : unsigned { ERR_PRODUCER_WAIT = 1u, ERR_CONSUMER_WAIT = 2u, ERR_DRAIN_WAIT = 4u };
+
+template <int R>
+struct RCfg {
+  static constexpr int P = 128 / R;                          // K-parts per row
+  static constexpr int PAD = P > 1 ? 16 * (8 / P) : 0;       // bank stagger between parts
+  static constexpr int PSTRIDE = R * CHUNK_BLOCKS * BLOCK_BYTES + PAD;
+  static constexpr int STAGE_BYTES = P * PSTRIDE;
+};
+
+template <int MT>
+struct MCfg {
+  static constexpr int NCW = 4;                       // consumer warps: 128 threads
+  static constexpr int THREADS = (NCW + 1) * 32;      // + the producer warp
+  static constexpr int STAGES = MT <= 2 ? 3 : 2;
+  // bytes of staged activations; for MT <= 2 the whole shared-memory use
+  // stays below half an SM's, so two CTAs (of consecutive kernels) fit
+  static constexpr int ACT_BUDGET = MT == 1 ? 9728 : MT == 2 ? 8704 : 40960;
+};
+
+// activation bytes of one unit in shared memory
+__host__ __device__ constexpr int act_bytes(int M, int P, int cpp) {
+  return M * P * (cpp * CHUNK_BLOCKS * 32 + (P > 1 ? 16 * (8 / P) : 0) + (cpp * CHUNK_BLOCKS + 1) * 4);
+}
+
+template <int R, int MT>
+__host__ __device__ constexpr int cpp_max() {
+  int c = 64;
+  while (c > 1 && act_bytes(MT, RCfg<R>::P, c) > MCfg<MT>::ACT_BUDGET) c >>= 1;
+  return c;
+}
+__host__ __device__ constexpr int log2_floor(int v) { return v <= 1 ? 0 : 1 + log2_floor(v >> 1); }
+
+template <int R, int MT>
+constexpr size_t gemv_smem_bytes() {
+  return (size_t)MCfg<MT>::STAGES * RCfg<R>::STAGE_BYTES + MCfg<MT>::ACT_BUDGET +
+         2 * MCfg<MT>::STAGES * sizeof(uint64_t) + 4 * sizeof(int);
+}
+
+struct GemvArgs {
+  const uint8_t* W;
+  const uint8_t* A;      // activation blocks [M][NB] (unfused)
+  const float* x;        // fp32 activations [M][K] (fused)
+  uint8_t* A_out;        // fused: optional activation blocks out
+  float* y;              // [M][N]
+  float* ws_part;        // [S][M][N] partials (S > 1)
+  unsigned* ws_cnt;      // [T] tickets (S > 1)
+  unsigned* err;         // device error word
+  int64_t N;
+  int NB, nch, T, M, CU, cpp, S, units;
+};
+
+// ---- producer: one lane streams the rounds of every unit of this CTA ----
+// In a cluster (CL > 1) the producer lane takes part in the two cluster
+// barrier phases (see the kernel): it arrives for phase 1 before streaming,
+// issues the first STAGES rounds (which never wait), then waits for phase 1
+// and arrives for phase 2, so the start of streaming does not wait for the
+// rest of the cluster.
+template <int R, int STAGES>
+__device__ __forceinline__ void produce(const GemvArgs& a, uint8_t* stage_buf, uint64_t* full,
+                                        uint64_t* empty, volatile int* misc, uint32_t CL) {
+  constexpr int P = RCfg<R>::P;
+  const uint64_t pol = l2_policy_evict_first();
+  int stage = 0;
+  uint32_t phase = 0;
+  int issued = 0;
+  bool cluster_done = (CL == 1);
+  bool stop = false;
+  for (int u = blockIdx.x; u < a.units && !stop; u += gridDim.x) {
+    const int t = u / a.S, s = u - (u / a.S) * a.S;
+    const int r = tile_rows(t, a.N, R);
+    const int c0 = s * a.CU;
+    const int nrounds = min(a.cpp, a.nch - c0);
+    for (int rho = 0; rho < nrounds; ++rho) {
+      if (!cluster_done && issued == STAGES) {
+        asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+        cluster_arrive_one();
+        cluster_done = true;
+      }
+      if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, WAIT_LIMIT_NS)) {
+        atomicOr(a.err, ERR_PRODUCER_WAIT);
+        misc[0] = 1;
+        stop = true;
+        break;
+      }
+      if (misc[0]) {
+        stop = true;
+        break;
+      }
+      uint8_t* sb = stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES;
+      uint32_t total = 0;
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        const int c = c0 + p * a.cpp + rho;
+        if (c < a.nch) {
+          const uint8_t* src = a.W + chunk_offset(t, c, r, R, a.NB);
+          uint8_t* dst = sb + p * RCfg<R>::PSTRIDE;
+          const uint32_t bytes = (uint32_t)(chunk_blocks(c, a.NB) * r * BLOCK_BYTES);
+          const uint32_t bulk = bytes & ~15u;
+          for (uint32_t k = bulk; k < bytes; ++k) dst[k] = src[k];  // ragged tail < 16 B
+          total += bulk;
+        }
+      }
+      mbar_arrive_expect_tx(&full[stage], total);
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        const int c = c0 + p * a.cpp + rho;
+        if (c < a.nch) {
+          const uint8_t* src = a.W + chunk_offset(t, c, r, R, a.NB);
+          const uint32_t bulk = (uint32_t)(chunk_blocks(c, a.NB) * r * BLOCK_BYTES) & ~15u;
+          bulk_g2s(sb + p * RCfg<R>::PSTRIDE, src, bulk, &full[stage], pol);
+        }
+      }
+      misc[2] = ++issued;
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  if (!cluster_done) {
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+    cluster_arrive_one();
+  }
+}
+
+// Shared-memory positions of the staged activation blocks of a unit: for
+// row m and block jj of part p, quants at act_q + (m*P + p)*qpart + jj*32 and
+// the scale (as float) at act_d[(m*P + p)*dpart + jj].
+struct ActLayout {
+  uint8_t* q;
+  float* d;
+  int qpart, dpart, APB;
+};
+
+template <int R>
+__device__ __forceinline__ ActLayout act_layout(uint8_t* base, int M, int cpp) {
+  constexpr int P = RCfg<R>::P;
+  ActLayout L;
+  L.APB = cpp * CHUNK_BLOCKS;
+  L.qpart = L.APB * 32 + (P > 1 ? 16 * (8 / P) : 0);
+  L.dpart = L.APB + 1;
+  L.q = base;
+  L.d = reinterpret_cast<float*>(base + (size_t)M * P * L.qpart);
+  return L;
+}
+
+// Stage the activation blocks [b0, b0 + nblk) of rows < M, one thread per
+// block.  With a cluster of CL CTAs that all need the same blocks, CTA c
+// stages every CL-th block (c, c+CL, ...) and writes it into the staging
+// area of every CTA of the cluster (distributed shared memory); the caller
+// then waits on the cluster barrier.  Loads of two blocks per thread are
+// issued before either is used.
+template <int R>
+__device__ __forceinline__ void put_block(const ActLayout& L, int m, int blk, const uint32_t (&w)[8],
+                                          float d, uint32_t CL) {
+  constexpr int P = RCfg<R>::P;
+  const int p = blk / L.APB, jj = blk - p * L.APB;
+  uint8_t* dst = L.q + (m * P + p) * L.qpart + jj * 32;
+  float* dd = L.d + (m * P + p) * L.dpart + jj;
+  if (CL == 1) {
+    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+    *dd = d;
+  } else {
+    const uint32_t q0 = smem_u32(dst), d0 = smem_u32(dd);
+    for (uint32_t c = 0; c < CL; ++c) {
+      const uint32_t q = mapa_shared(q0, c);
+      st_cluster_v4(q, w[0], w[1], w[2], w[3]);
+      st_cluster_v4(q + 16, w[4], w[5], w[6], w[7]);
+      st_cluster_f32(mapa_shared(d0, c), d);
+    }
+  }
+}
+
+template <int R, bool FUSED>
+__device__ __forceinline__ void stage_one(const GemvArgs& a, const ActLayout& L, int b0, int nblk,
+                                          int idx0, int idx1, bool h0, bool h1, uint32_t CL) {
+  const int64_t K = (int64_t)a.NB * QK;
+  const int m0 = h0 ? idx0 / nblk : 0, k0 = h0 ? idx0 - m0 * nblk : 0;
+  const int m1 = h1 ? idx1 / nblk : 0, k1 = h1 ? idx1 - m1 * nblk : 0;
+  if constexpr (FUSED) {
+    const float4* s0 = reinterpret_cast<const float4*>(a.x + (int64_t)m0 * K + (int64_t)(b0 + k0) * QK);
+    const float4* s1 = reinterpret_cast<const float4*>(a.x + (int64_t)m1 * K + (int64_t)(b0 + k1) * QK);
+    float4 v0[8], v1[8];
+    uint32_t w0[8], w1[8];
+    float d0, d1;
+    if (h1) {  // two blocks: both loads in flight, then both quantizations
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        v0[k] = __ldcg(s0 + k);
+        v1[k] = __ldcg(s1 + k);
+      }
+      quantize_block_thread(v0, w0, d0);
+      quantize_block_thread(v1, w1, d1);
+      put_block<R>(L, m0, k0, w0, d0, CL);
+      put_block<R>(L, m1, k1, w1, d1, CL);
+    } else if (h0) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v0[k] = __ldcg(s0 + k);
+      quantize_block_thread(v0, w0, d0);
+      put_block<R>(L, m0, k0, w0, d0, CL);
+    }
+  } else {
+    uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0, r0 = q0, r1 = q0;
+    uint16_t d0 = 0, d1 = 0;
+    const uint8_t* s0 = a.A + ((int64_t)m0 * a.NB + b0 + k0) * BLOCK_BYTES;
+    const uint8_t* s1 = a.A + ((int64_t)m1 * a.NB + b0 + k1) * BLOCK_BYTES;
+    if (h0) {
+      load_block_quants_u16(s0, q0, q1);
+      d0 = load_block_scale_bits(s0);
+    }
+    if (h1) {
+      load_block_quants_u16(s1, r0, r1);
+      d1 = load_block_scale_bits(s1);
+    }
+    if (h0) {
+      const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+      put_block<R>(L, m0, k0, w, __half2float(__ushort_as_half(d0)), CL);
+    }
+    if (h1) {
+      const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+      put_block<R>(L, m1, k1, w, __half2float(__ushort_as_half(d1)), CL);
+    }
+  }
+}
+
+template <int R, bool FUSED, int NT>
+__device__ __forceinline__ void stage_activations(const GemvArgs& a, const ActLayout& L, int b0,
+                                                  int nblk, uint32_t rank, uint32_t CL) {
+  const int total = a.M * nblk;
+  const int mine = (total - (int)rank + (int)CL - 1) / (int)CL;  // blocks rank, rank+CL, ...
+  for (int base = 0; base < mine; base += 2 * NT) {
+    const int j0 = base + threadIdx.x, j1 = j0 + NT;
+    stage_one<R, FUSED>(a, L, b0, nblk, j0 * (int)CL + (int)rank, j1 * (int)CL + (int)rank, j0 < mine,
+                        j1 < mine, CL);
+  }
+}
+
+// Fused path: the CTAs that own row tile 0 publish the quantized activations
+// of their K range (every K range is covered once by tile 0).
+template <int R, int NT>
+__device__ __forceinline__ void write_act_blocks(const GemvArgs& a, const ActLayout& L, int b0,
+                                                 int nblk) {
+  constexpr int P = RCfg<R>::P;
+  const int total = a.M * nblk;
+  for (int idx = threadIdx.x; idx < total; idx += NT) {
+    const int m = idx / nblk, blk = idx - m * nblk;
+    const int p = blk / L.APB, jj = blk - p * L.APB;
+    uint8_t* ob = a.A_out + ((int64_t)m * a.NB + b0 + blk) * BLOCK_BYTES;
+    const float d = L.d[(m * P + p) * L.dpart + jj];
+    const uint16_t d16 = __half_as_ushort(__float2half_rn(d));  // exact: d came from binary16
+    const uint8_t* q = L.q + (m * P + p) * L.qpart + jj * 32;
+    unsigned short* o16 = reinterpret_cast<unsigned short*>(ob);
+    o16[0] = d16;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) o16[1 + k] = (unsigned short)(q[2 * k] | (q[2 * k + 1] << 8));
+  }
+}
+
+// Block term of row i for block j of the chunk against every activation row.
+// Two independent dp4a chains per block keep the dependent latency short.
+template <int MT>
+__device__ __forceinline__ void block_terms(const uint8_t* cq, const uint8_t* sc, int r, int i,
+                                            int j, const uint8_t* aq, const float* ad, int mq,
+                                            int md, float (&out)[MT]) {
+  const uint4 w0 = lds128(cq + ((2 * j) * r + i) * 16);
+  const uint4 w1 = lds128(cq + ((2 * j + 1) * r + i) * 16);
+  const float dw =
+      __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(sc + (j * r + i) * 2)));
+#pragma unroll
+  for (int m = 0; m < MT; ++m) {
+    const uint8_t* am = aq + m * mq + j * 32;
+    const uint4 a0 = lds128(am), a1 = lds128(am + 16);
+    int s0 = __dp4a((int)w0.x, (int)a0.x, 0);
+    int s1 = __dp4a((int)w1.x, (int)a1.x, 0);
+    s0 = __dp4a((int)w0.y, (int)a0.y, s0);
+    s1 = __dp4a((int)w1.y, (int)a1.y, s1);
+    s0 = __dp4a((int)w0.z, (int)a0.z, s0);
+    s1 = __dp4a((int)w1.z, (int)a1.z, s1);
+    s0 = __dp4a((int)w0.w, (int)a0.w, s0);
+    s1 = __dp4a((int)w1.w, (int)a1.w, s1);
+    out[m] = block_term(s0 + s1, dw, ad[m * md + j]);  // integer sum: exact
+  }
+}
+
+// Blocks j0 .. j0+NBLK-1 (NBLK = 8: a chunk, 4: half a chunk; blocks at or
+// past kb count as zero) of row i: their pairwise tree, per activation row.
+// aq/ad point at this part's first block of the chunk; mq/md are the strides
+// between activation rows.  Rows m >= M are computed on whatever the staging
+// area holds and never stored.
+template <int MT, int NBLK>
+__device__ __forceinline__ void chunk_value(const uint8_t* cq, int r, int kb, int i, int j0,
+                                            const uint8_t* aq, const float* ad, int mq, int md,
+                                            float (&v)[MT]) {
+  const uint8_t* sc = cq + kb * r * 32;
+  const bool full = (j0 + NBLK <= kb);
+  float q[NBLK / 4][MT];
+#pragma unroll
+  for (int h4 = 0; h4 < NBLK / 4; ++h4) {
+    float p0[MT], p1[MT];
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      float ta[MT], tb[MT];
+      const int j = j0 + 4 * h4 + 2 * h2;
+      if (full || j < kb) {
+        block_terms<MT>(cq, sc, r, i, j, aq, ad, mq, md, ta);
+      } else {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) ta[m] = 0.0f;
+      }
+      if (full || j + 1 < kb) {
+        block_terms<MT>(cq, sc, r, i, j + 1, aq, ad, mq, md, tb);
+      } else {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) tb[m] = 0.0f;
+      }
+#pragma unroll
+      for (int m = 0; m < MT; ++m) (h2 ? p1 : p0)[m] = tadd(ta[m], tb[m]);
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) q[h4][m] = tadd(p0[m], p1[m]);
+  }
+#pragma unroll
+  for (int m = 0; m < MT; ++m) v[m] = NBLK == 8 ? tadd(q[0][m], q[NBLK / 4 - 1][m]) : q[0][m];
+}
+
+template <int R, int MT, bool FUSED>
+__global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvArgs a) {
+  constexpr int P = RCfg<R>::P;
+  constexpr int NCW = MCfg<MT>::NCW;
+  constexpr int NT = NCW * 32;  // consumer threads
+  constexpr int STAGES = MCfg<MT>::STAGES;
+  constexpr int LV = log2_floor(cpp_max<R, MT>()) + 1;
+  constexpr int BAR_CONSUMERS = 1;  // named barrier of the consumer warps
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* stage_buf = smem;
+  uint8_t* act_base = smem + (size_t)STAGES * RCfg<R>::STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(act_base + MCfg<MT>::ACT_BUDGET);
+  uint64_t* empty = full + STAGES;
+  volatile int* misc = reinterpret_cast<volatile int*>(empty + STAGES);
+  // misc[0]: abort flag, misc[1]: "this CTA combines the tile", misc[2]: rounds issued
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NCW);
+    }
+    misc[0] = 0;
+    misc[1] = 0;
+    misc[2] = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  // A cluster (launched only when every unit covers all of K, so every CTA
+  // stages the same blocks) stages its activations cooperatively.  Barrier
+  // phase 1: every CTA of the cluster is running before any writes into
+  // another's shared memory.  Phase 2: all staged blocks have landed; the
+  // producer lane arrives for it up front, the producer warp's other lanes
+  // have exited by then (exited threads do not take part).
+  const uint32_t CL = cluster_nctarank();
+  const uint32_t crank = cluster_ctarank();
+  if (warp == NCW) {
+    if (CL > 1) {
+      // phase 1 for the producer warp: lane 0 arrives and waits inside
+      // produce(); lanes 1-31 arrive, wait, and exit (exited threads do not
+      // take part in phase 2)
+      __syncwarp();
+      cluster_arrive_aligned();
+      if (lane != 0) {
+        asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+        return;
+      }
+    }
+    if (lane == 0) produce<R, STAGES>(a, stage_buf, full, empty, misc, CL);
+    return;
+  }
+  if (CL > 1) {  // phase 1: every CTA of the cluster is running
+    cluster_arrive_aligned();
+    cluster_wait_aligned();
+  }
+
+  const int p = threadIdx.x % P;  // K-part
+  const int i = threadIdx.x / P;  // row inside the tile
+  // laid out for MT rows (the planner sized the unit for MT), so rows
+  // M <= m < MT read inside the staging area
+  const ActLayout L = act_layout<R>(act_base, MT, a.cpp);
+  const int mq = P * L.qpart, md = P * L.dpart;
+  int stage = 0;
+  uint32_t phase = 0;
+  int consumed = 0;
+  bool ok = true;
+  bool waited = false;
+  int staged_s = -1;
+
+  for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
+    const int t = u / a.S, s = u - (u / a.S) * a.S;
+    const int r = tile_rows(t, a.N, R);
+    const int c0 = s * a.CU;
+    const int nrounds = min(a.cpp, a.nch - c0);
+    const int b0 = c0 * CHUNK_BLOCKS;
+    const int nblk = min(a.CU * CHUNK_BLOCKS, a.NB - b0);
+    const int64_t n = (int64_t)t * R + i;
+
+    if (!waited) {
+      pdl_wait();
+      waited = true;
+    }
+    if (s != staged_s) {  // units with the same K range reuse the staged blocks
+      if (CL > 1) {        // once per CTA: the planner clusters only when S == 1
+        stage_activations<R, FUSED, NT>(a, L, b0, nblk, crank, CL);
+        __syncwarp();
+        cluster_arrive_aligned();
+        cluster_wait_aligned();
+      } else {
+        named_bar_sync(BAR_CONSUMERS, NT);
+        stage_activations<R, FUSED, NT>(a, L, b0, nblk, 0u, 1u);
+        named_bar_sync(BAR_CONSUMERS, NT);
+      }
+      staged_s = s;
+    }
+    if constexpr (FUSED) {
+      if (a.A_out != nullptr && t == 0) write_act_blocks<R, NT>(a, L, b0, nblk);
+    }
+
+    float slot[MT][LV];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+      for (int l = 0; l < LV; ++l) slot[m][l] = 0.0f;
+
+    for (int rho = 0; rho < nrounds; ++rho) {
+      if (ok && misc[0]) ok = false;
+      if (!ok) break;
+      if (!mbar_wait_bounded(&full[stage], phase, WAIT_LIMIT_NS)) {
+        atomicOr(a.err, ERR_CONSUMER_WAIT);
+        misc[0] = 1;
+        ok = false;
+        break;
+      }
+      const int c = c0 + p * a.cpp + rho;
+      float v[MT];
+#pragma unroll
+      for (int m = 0; m < MT; ++m) v[m] = 0.0f;
+      if (c < a.nch) {
+        const int jj0 = rho * CHUNK_BLOCKS;
+        chunk_value<MT, CHUNK_BLOCKS>(stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES + p * RCfg<R>::PSTRIDE,
+                                      r, chunk_blocks(c, a.NB), i, 0, L.q + p * L.qpart + jj0 * 32,
+                                      L.d + p * L.dpart + jj0, mq, md, v);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+      ++consumed;
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      // binary counter over this part's chunk subtrees
+      bool placed = false;
+#pragma unroll
+      for (int l = 0; l < LV; ++l) {
+        if (!placed) {
+          if ((rho >> l) & 1) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) v[m] = tadd(slot[m][l], v[m]);
+          } else {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) slot[m][l] = v[m];
+            placed = true;
+          }
+        }
+      }
+    }
+
+    // what is left merges from the lowest level up (= zero padding)
+    float pv[MT];
+    bool have = false;
+#pragma unroll
+    for (int m = 0; m < MT; ++m) pv[m] = 0.0f;
+#pragma unroll
+    for (int l = 0; l < LV; ++l) {
+      if ((nrounds >> l) & 1) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) pv[m] = have ? tadd(slot[m][l], pv[m]) : slot[m][l];
+        have = true;
+      }
+    }
+    // the P parts of row i are P consecutive lanes: butterfly over parts
+#pragma unroll
+    for (int off = 1; off < P; off <<= 1)
+#pragma unroll
+      for (int m = 0; m < MT; ++m) pv[m] = tadd(pv[m], __shfl_xor_sync(0xffffffffu, pv[m], off));
+
+    if (a.S == 1) {
+      if (ok && i < r) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+          if (m < a.M && (m % P) == p) a.y[(int64_t)m * a.N + n] = pv[m];
+      }
+      continue;
+    }
+
+    // split along K: publish the unit value, take a ticket, last one combines
+    if (ok && i < r) {
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+        if (m < a.M && (m % P) == p) a.ws_part[((int64_t)s * a.M + m) * a.N + n] = pv[m];
+    }
+    __threadfence();
+    named_bar_sync(BAR_CONSUMERS, NT);
+    if (threadIdx.x == 0) {
+      const bool any_abort = misc[0] != 0;
+      const unsigned prev = any_abort ? 0u : atomicAdd(&a.ws_cnt[t], 1u);
+      misc[1] = (!any_abort && prev == (unsigned)(a.S - 1)) ? 1 : 0;
+    }
+    named_bar_sync(BAR_CONSUMERS, NT);
+    if (misc[1]) {
+      __threadfence();
+      if (i < r) {
+        for (int m = p; m < a.M; m += P) {
+          float sl[SPLIT_LEVELS];
+#pragma unroll
+          for (int l = 0; l < SPLIT_LEVELS; ++l) sl[l] = 0.0f;
+          const float* part = a.ws_part + (int64_t)m * a.N + n;
+          const int64_t sstride = (int64_t)a.M * a.N;
+          for (int s0 = 0; s0 < a.S; s0 += 16) {
+            float pv16[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k)  // 16 independent loads in flight
+              pv16[k] = (s0 + k < a.S) ? __ldcg(part + (int64_t)(s0 + k) * sstride) : 0.0f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int ss = s0 + k;
+              if (ss < a.S) {
+                float v = pv16[k];
+                bool placed = false;
+#pragma unroll
+                for (int l = 0; l < SPLIT_LEVELS; ++l) {
+                  if (!placed) {
+                    if ((ss >> l) & 1) {
+                      v = tadd(sl[l], v);
+                    } else {
+                      sl[l] = v;
+                      placed = true;
+                    }
+                  }
+                }
+              }
+            }
+          }
+          float out = 0.0f;
+          bool h = false;
+#pragma unroll
+          for (int l = 0; l < SPLIT_LEVELS; ++l) {
+            if ((a.S >> l) & 1) {
+              out = h ? tadd(sl[l], out) : sl[l];
+              h = true;
+            }
+          }
+          a.y[(int64_t)m * a.N + n] = out;
+        }
+      }
+      if (threadIdx.x == 0) a.ws_cnt[t] = 0u;
+    }
+  }
+
+  // After a failed wait: let rounds that were issued but not consumed land
+  // before the CTA's shared memory goes away (bounded as well).
+  if (threadIdx.x == 0 && misc[0]) {
+    for (int k = consumed; k < misc[2]; ++k) {
+      if (!mbar_wait_bounded(&full[k % STAGES], (uint32_t)((k / STAGES) & 1), WAIT_LIMIT_NS / 4)) {
+        atomicOr(a.err, ERR_DRAIN_WAIT);
+        break;
+      }
+    }
+  }
+}
+
+// Every libq8 kernel asks for the largest shared-memory carveout, so CTAs of
+// consecutive kernels can share an SM (a programmatic dependent starts while
+// its predecessor still runs); kernels with different carveouts cannot.
+template <int R, int MT, bool FUSED>
+cudaError_t set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<R, MT, FUSED>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)gemv_smem_bytes<R, MT>());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(gemv_kernel<R, MT, FUSED>,
+                              cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared);
+}
+
+template <int R, int MT, bool FUSED>
+cudaError_t launch_gemv_t(const GemvArgs& args, int grid, int cluster, bool pdl, cudaStream_t s) {
+  cudaError_t e = set_attributes<R, MT, FUSED>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(MCfg<MT>::THREADS);
+  cfg.dynamicSmemBytes = gemv_smem_bytes<R, MT>();
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (cluster > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<R, MT, FUSED>, args);
+}
+
+template <int R, int MT, bool FUSED>
+int occupancy_t() {
+  if (set_attributes<R, MT, FUSED>() != cudaSuccess) return 0;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_kernel<R, MT, FUSED>, MCfg<MT>::THREADS,
+                                                    gemv_smem_bytes<R, MT>()) != cudaSuccess)
+    return 0;
+  return occ;
+}
+
+// Whether clusters of `cluster` CTAs of this kernel can be resident at all.
+template <int R, int MT, bool FUSED>
+bool cluster_fits_t(int cluster) {
+  if (set_attributes<R, MT, FUSED>() != cudaSuccess) return false;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cluster);
+  cfg.blockDim = dim3(MCfg<MT>::THREADS);
+  cfg.dynamicSmemBytes = gemv_smem_bytes<R, MT>();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemv_kernel<R, MT, FUSED>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return n > 0;
+}
+
+// Per-R translation units instantiate these for every MT and FUSED.
+template <int R>
+cudaError_t launch_gemv_r(const GemvArgs& args, int MT, bool fused, int grid, int cluster, bool pdl,
+                         cudaStream_t s);
+template <int R>
+int occupancy_r(int MT, bool fused);
+template <int R>
+bool cluster_fits_r(int MT, bool fused, int cluster);
+
+#define Q8_INSTANTIATE_R(R)                                                                          \
+  template <>                                                                                        \
+  cudaError_t launch_gemv_r<R>(const GemvArgs& args, int MT, bool fused, int grid, int cluster,      \
+                               bool pdl, cudaStream_t s) {                                           \
+    switch (MT) {                                                                                    \
+      case 1: return fused ? launch_gemv_t<R, 1, true>(args, grid, cluster, pdl, s)                           \
+                           : launch_gemv_t<R, 1, false>(args, grid, cluster, pdl, s);                         \
+      case 2: return fused ? launch_gemv_t<R, 2, true>(args, grid, cluster, pdl, s)                           \
+                           : launch_gemv_t<R, 2, false>(args, grid, cluster, pdl, s);                         \
+      case 4: return fused ? launch_gemv_t<R, 4, true>(args, grid, cluster, pdl, s)                           \
+                           : launch_gemv_t<R, 4, false>(args, grid, cluster, pdl, s);                         \
+      case 8: return fused ? launch_gemv_t<R, 8, true>(args, grid, cluster, pdl, s)                           \
+                           : launch_gemv_t<R, 8, false>(args, grid, cluster, pdl, s);                         \
+      default: return fused ? launch_gemv_t<R, 16, true>(args, grid, cluster, pdl, s)                         \
+                            : launch_gemv_t<R, 16, false>(args, grid, cluster, pdl, s);                       \
+    }                                                                                                \
+  }                                                                                                  \
+  template <>                                                                                        \
+  int occupancy_r<R>(int MT, bool fused) {                                                           \
+    switch (MT) {                                                                                    \
+      case 1: return fused ? occupancy_t<R, 1, true>() : occupancy_t<R, 1, false>();                 \
+      case 2: return fused ? occupancy_t<R, 2, true>() : occupancy_t<R, 2, false>();                 \
+      case 4: return fused ? occupancy_t<R, 4, true>() : occupancy_t<R, 4, false>();                 \
+      case 8: return fused ? occupancy_t<R, 8, true>() : occupancy_t<R, 8, false>();                 \
+      default: return fused ? occupancy_t<R, 16, true>() : occupancy_t<R, 16, false>();              \
+    }                                                                                                \
+  }                                                                                                  \
+  template <>                                                                                        \
+  bool cluster_fits_r<R>(int MT, bool fused, int c) {                                                \
+    switch (MT) {                                                                                    \
+      case 1: return fused ? cluster_fits_t<R, 1, true>(c) : cluster_fits_t<R, 1, false>(c);         \
+      case 2: return fused ? cluster_fits_t<R, 2, true>(c) : cluster_fits_t<R, 2, false>(c);         \
+      case 4: return fused ? cluster_fits_t<R, 4, true>(c) : cluster_fits_t<R, 4, false>(c);         \
+      case 8: return fused ? cluster_fits_t<R, 8, true>(c) : cluster_fits_t<R, 8, false>(c);         \
+      default: return fused ? cluster_fits_t<R, 16, true>(c) : cluster_fits_t<R, 16, false>(c);      \
+    }                                                                                                \
+  }
+
+}  // namespace q8

@@ -8,17 +8,22 @@
 
 namespace q8 {
 
-// Launch plan of one GEMV call: the work is cut into units of one 128-row
-// tile x C blocks (C = 8 * 2^k), S units per tile along K.
+// Launch plan of one GEMV call: the work is cut into units of one R-row
+// tile x CU chunks of 8 blocks (CU = P * cpp, P = 128 / R parts of cpp
+// chunks each), S units per tile along K.
 struct GemvPlan {
   int64_t N = 0, K = 0, NB = 0;
   int M = 0;
   int MT = 0;        // activation rows per kernel instantiation (1,2,4,8,16)
+  int R = 0;         // packed tile height
   int T = 0;         // row tiles
-  int C = 0;         // blocks per unit
+  int nch = 0;       // chunks along K
+  int cpp = 0;       // chunks per part
+  int CU = 0;        // chunks per unit
   int S = 0;         // units per tile (splits along K)
   int units = 0;
   int grid = 0;      // persistent CTAs
+  int cluster = 1;   // CTAs per thread-block cluster (shared activation staging)
   size_t smem = 0;   // dynamic shared memory per CTA
   size_t ws_bytes = 0;
 };

@@ -43,7 +43,7 @@ class Call:
 class Q8Stack:
     shape: q8_synth.StackShape
     M: int
-    mode: str = "shared"
+    mode: str = "fused"
     layers: int | None = None
     seed: int = 0
     pdl: bool = True

@@ -111,9 +111,13 @@ def test_weight_quantize_repack_round_trip(q8):
         assert np.array_equal(np.sort(W.cpu().numpy()), np.sort(ref.ravel()))
 
 
-def test_packed_layout_matches_header_description(q8):
-    # spot-check the byte positions stated in q8.h for a ragged tile and chunk
-    N, K = 131, 11 * 32
+@pytest.mark.parametrize("N,K", [(131, 11 * 32), (3000, 5 * 32), (9000, 17 * 32), (20000, 96)])
+def test_packed_layout_matches_header_description(q8, N, K):
+    # the byte positions stated in q8.h, for ragged tiles and chunks and
+    # every tile height
+    R = q8.q8_packed_tile_rows(N)
+    exp_R = next((c for c in (16, 32, 64) if -(-N // c) <= 152), 128)
+    assert R == exp_R
     nb = K // 32
     rng = np.random.default_rng(4)
     blocks = rng.integers(0, 256, size=(N, nb * 34), dtype=np.uint8)
@@ -121,18 +125,19 @@ def test_packed_layout_matches_header_description(q8):
     W = q8.empty_packed(N, K)
     q8.q8_repack_weights(src, N, K, W)
     P = W.cpu().numpy()
-    for n, b in [(0, 0), (5, 9), (127, 10), (128, 3), (130, 10), (129, 8)]:
-        t, i = divmod(n, 128)
-        r = min(128, N - 128 * t)
-        c, j = divmod(b, 8)
-        kb = min(8, nb - 8 * c)
-        base = 128 * t * nb * 34 + r * 8 * c * 34
-        blk = blocks[n, b * 34:(b + 1) * 34]
-        for h in range(2):
-            off = base + ((2 * j + h) * r + i) * 16
-            assert np.array_equal(P[off:off + 16], blk[2 + 16 * h:2 + 16 * h + 16])
-        so = base + kb * r * 32 + (j * r + i) * 2
-        assert np.array_equal(P[so:so + 2], blk[0:2])
+    for n in sorted(set([0, 5, R - 1, R, N - 1, N - 2, N // 2])):
+        for b in sorted(set([0, nb - 1, nb // 2, min(9, nb - 1)])):
+            t, i = divmod(n, R)
+            r = min(R, N - R * t)
+            c, j = divmod(b, 8)
+            kb = min(8, nb - 8 * c)
+            base = R * t * nb * 34 + r * 8 * c * 34
+            blk = blocks[n, b * 34:(b + 1) * 34]
+            for h in range(2):
+                off = base + ((2 * j + h) * r + i) * 16
+                assert np.array_equal(P[off:off + 16], blk[2 + 16 * h:2 + 16 * h + 16])
+            so = base + kb * r * 32 + (j * r + i) * 2
+            assert np.array_equal(P[so:so + 2], blk[0:2])
 
 
 # ---------------------------------------------------------------------------
@@ -249,7 +254,7 @@ def test_pdl_flag_same_bits(q8):
 
 
 def test_workspace_left_zero_and_reusable(q8):
-    N, K, M = 2048, 8192, 1
+    N, K, M = 256, 8192, 16
     w, x = _case(N, K, M, 6)
     W = _gpu_pack(q8, w)
     A = q8.empty_blocks(M, K)
@@ -258,7 +263,7 @@ def test_workspace_left_zero_and_reusable(q8):
     assert ws is not None  # this shape is split along K
     y = torch.empty((M, N), dtype=torch.float32, device=DEV)
     outs = []
-    for _ in range(3):
+    for _ in range(3):  # noqa: B007
         q8.q8_gemm(W, N, K, A, M, y, workspace=ws)
         outs.append(y.clone())
     torch.cuda.synchronize()
@@ -269,8 +274,8 @@ def test_workspace_left_zero_and_reusable(q8):
 def test_workspace_shared_across_shapes(q8):
     # one workspace serves calls of different shapes in sequence (tickets
     # live in a fixed prefix that partials never touch)
-    K, M = 2048, 2
-    shapes = [(2048, 2048), (16384, 2048), (3072, 2048), (2048, 8192), (16384, 2048)]
+    K, M = 2048, 16
+    shapes = [(256, 8192), (512, 2048), (2048, 2048), (300, 4096), (256, 8192)]
     need = max(q8.q8_workspace_bytes(N, K_, M) for N, K_ in shapes)
     ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
     for N, K_ in shapes:
