@@ -83,7 +83,9 @@ typedef enum q8_status {
     Q8_EDEVICE = -4,     /* current device is not sm_103                      */
     Q8_ECUDA = -5,       /* a CUDA runtime call failed                        */
     Q8_EWORKSPACE = -6,  /* workspace missing or smaller than required        */
-    Q8_ETIMEOUT = -7     /* (q8_device_error only) a device wait gave up      */
+    Q8_ETIMEOUT = -7,    /* (q8_device_error only) a device wait gave up      */
+    Q8_ESCRATCH = -8     /* (q8_gemm_noalloc only) shape needs more scratch
+                            than the built-in Q8_NOALLOC_SCRATCH_BYTES         */
 } q8_status;
 
 /* Human-readable name of a status code.  Static string, never NULL. */
@@ -197,6 +199,36 @@ Q8_API int q8_gemm(const void *W, int64_t N, int64_t K, const void *A_blocks, in
 Q8_API int q8_fused_quant_gemm(const void *W, int64_t N, int64_t K, const float *x,
                         int M, float *y, void *A_blocks_out, void *workspace,
                         size_t workspace_bytes, unsigned flags, void *stream);
+
+/*
+ * q8_gemm_noalloc -- q8_gemm without a workspace argument, for callers that
+ * cannot allocate device memory (for example a plugin inside an application
+ * whose own allocator owns the device, or a latency-critical loop that must
+ * not pay cudaMalloc's latency and implicit synchronization).  The pages have
+ * no counterpart; it is a packaging variant of q8_gemm and computes the same
+ * bits.
+ *
+ * When the work is split along K, the partial sums go to a scratch array of
+ * Q8_NOALLOC_SCRATCH_BYTES compiled into the library: it occupies that much
+ * memory on every GPU that loads the library, until the process exits.
+ * Neither this call nor the library allocates anything.  Shapes whose split
+ * would need more scratch than that return Q8_ESCRATCH before anything is
+ * enqueued (q8_workspace_bytes(N, K, M) tells the size; 0 means no scratch
+ * is used and any size works).
+ *
+ * Every call shares the one array and it keeps the last call's contents:
+ * calls that may run at the same time on the GPU (other streams, other host
+ * threads) race on it and must be serialized by the caller.  Each split call
+ * first clears the array's ticket area with an asynchronous memset on
+ * `stream`.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.
+ *
+ * Arguments, alignment and errors otherwise as q8_gemm.
+ */
+#define Q8_NOALLOC_SCRATCH_BYTES (4u << 20)
+Q8_API int q8_gemm_noalloc(const void *W, int64_t N, int64_t K, const void *A_blocks,
+                           int M, float *y, unsigned flags, void *stream);
 
 /* ---- test hooks (not on the hot path) ----------------------------------- */
 

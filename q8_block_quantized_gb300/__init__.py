@@ -27,7 +27,8 @@ CHUNK_BLOCKS = 8
 FLAG_PDL = 1
 
 STATUS = {0: "Q8_OK", -1: "Q8_EINVAL", -2: "Q8_ESHAPE", -3: "Q8_EALIGN", -4: "Q8_EDEVICE",
-          -5: "Q8_ECUDA", -6: "Q8_EWORKSPACE", -7: "Q8_ETIMEOUT"}
+          -5: "Q8_ECUDA", -6: "Q8_EWORKSPACE", -7: "Q8_ETIMEOUT", -8: "Q8_ESCRATCH"}
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 # Every function q8.h declares, with its ctypes signature.
 _vp, _i64, _int, _u, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
@@ -42,6 +43,7 @@ SIGNATURES = {
     "q8_repack_weights": (_int, [_vp, _i64, _i64, _vp, _vp]),
     "q8_gemm": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _vp, _sz, _u, _vp]),
     "q8_fused_quant_gemm": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _vp, _vp, _sz, _u, _vp]),
+    "q8_gemm_noalloc": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _u, _vp]),
     "q8_unpack_weights": (_int, [_vp, _i64, _i64, _vp, _vp]),
     "q8_block_dots": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _vp]),
     "q8_device_error": (_int, [ctypes.POINTER(ctypes.c_uint)]),
@@ -153,6 +155,16 @@ def q8_fused_quant_gemm(W: torch.Tensor, N: int, K: int, x: torch.Tensor, M: int
         _dev(W, torch.uint8, "W"), N, K, _dev(x, torch.float32, "x"), M,
         _dev(y, torch.float32, "y"), _opt(A_blocks_out, torch.uint8, "A_blocks_out"), ws,
         0 if workspace is None else workspace.numel(), flags, _stream(stream)))
+    return y
+
+
+def q8_gemm_noalloc(W: torch.Tensor, N: int, K: int, A_blocks: torch.Tensor, M: int,
+                    y: torch.Tensor, flags: int = 0, stream=None):
+    """q8_gemm for callers that cannot allocate: split-K scratch is the
+    library's built-in array (shared by all calls; do not overlap calls)."""
+    _check("q8_gemm_noalloc", lib().q8_gemm_noalloc(
+        _dev(W, torch.uint8, "W"), N, K, _dev(A_blocks, torch.uint8, "A_blocks"), M,
+        _dev(y, torch.float32, "y"), flags, _stream(stream)))
     return y
 
 

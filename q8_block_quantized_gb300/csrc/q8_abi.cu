@@ -85,6 +85,7 @@ const char* q8_strerror(int status) {
     case Q8_ECUDA: return "Q8_ECUDA: a CUDA runtime call failed";
     case Q8_EWORKSPACE: return "Q8_EWORKSPACE: workspace missing or too small";
     case Q8_ETIMEOUT: return "Q8_ETIMEOUT: a device-side wait gave up";
+    case Q8_ESCRATCH: return "Q8_ESCRATCH: shape needs more than the built-in no-allocation scratch";
     default: return "unknown q8 status";
   }
 }

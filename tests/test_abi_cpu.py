@@ -52,7 +52,7 @@ def test_sizes_and_strings(lib):
     assert q8.q8_packed_bytes(7, 33) == 0
     assert q8.q8_blocks_bytes(0, 32) == 0
     assert lib.q8_abi_version() == 1
-    for code in (0, -1, -2, -3, -4, -5, -6, -7):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8):
         assert lib.q8_strerror(code).decode().startswith(q8.STATUS[code])
 
 

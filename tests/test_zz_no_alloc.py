@@ -1,0 +1,94 @@
+"""q8_gemm_noalloc: the GEMV for callers that cannot allocate device memory.
+
+Such callers (for example a plugin whose host application owns the device's
+memory, or a latency-critical loop that must not call cudaMalloc) cannot
+hand q8_gemm a workspace; q8_gemm_noalloc uses scratch built into the library
+instead.  These tests call it through the C ABI, twice in a row on shapes that
+split along K (so the built-in scratch is used and reused), and check each
+result against q8_gemm with a caller-allocated workspace: within the parity
+tolerance used everywhere (|dy| <= 1e-5 * sum|terms| + 1e-6, sum|terms| from
+the oracle) and, because both run the same reduction order, bit for bit.
+
+This file is collected last so a run that stops at the first failure has
+already run every other test; it passes alone in a fresh process too.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import q8_synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def q8():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import q8_block_quantized_gb300 as q8mod
+    return q8mod
+
+
+def _case(q8, N, K, M, seed):
+    w = q8_synth.weights(N, K, q8_synth.derive_seed("na-w", N, K, seed))
+    x = q8_synth.activations(M, K, q8_synth.derive_seed("na-x", M, K, seed))
+    Wb = oracle.quantize(w.numpy())
+    Ab = oracle.quantize(x.numpy())
+    _, S = oracle.gemm(Wb, Ab, K)
+    W = q8.pack_weights_f32(w.cuda())
+    A = torch.from_numpy(Ab).cuda()
+    return W, A, S
+
+
+def _noalloc_raw(q8, W, N, K, A, M, y):
+    # straight through the C ABI with raw pointers
+    st = q8.lib().q8_gemm_noalloc(ctypes.c_void_p(W.data_ptr()), N, K,
+                                  ctypes.c_void_p(A.data_ptr()), M,
+                                  ctypes.c_void_p(y.data_ptr()), 0,
+                                  ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0, q8.lib().q8_strerror(st).decode()
+
+
+@pytest.mark.parametrize("N,K,M", [(256, 8192, 16), (300, 4096, 16), (512, 2048, 1), (2048, 2048, 3)])
+def test_noalloc_matches_gemm_twice(q8, N, K, M):
+    results = []
+    for call in range(2):  # two calls in a row reuse the same built-in scratch
+        W, A, S = _case(q8, N, K, M, seed=call)
+        ws = q8.new_workspace(N, K, M)
+        y_ref = torch.full((M, N), float("nan"), device="cuda")
+        q8.q8_gemm(W, N, K, A, M, y_ref, workspace=ws)
+        y = torch.full((M, N), float("nan"), device="cuda")
+        _noalloc_raw(q8, W, N, K, A, M, y)
+        torch.cuda.synchronize()
+        err = (y.double() - y_ref.double()).abs().cpu().numpy()
+        assert (err <= 1e-5 * S + 1e-6).all(), (N, K, M, call, err.max())
+        assert torch.equal(y, y_ref)
+        results.append(y)
+    assert not torch.equal(results[0], results[1])  # different inputs, fresh results
+    assert q8.q8_device_error() == 0
+
+
+def test_noalloc_uses_scratch_for_split_shapes(q8):
+    # the shapes above that split along K do need scratch, and it fits
+    assert 0 < q8.q8_workspace_bytes(256, 8192, 16) <= q8.NOALLOC_SCRATCH_BYTES
+
+
+def test_noalloc_rejects_shapes_beyond_scratch(q8):
+    # a split shape whose partials exceed the built-in scratch: refused with
+    # Q8_ESCRATCH before anything is enqueued
+    N, K, M = 4096, 65536, 64
+    need = q8.q8_workspace_bytes(N, K, M)
+    assert need > q8.NOALLOC_SCRATCH_BYTES
+    W = torch.empty(16, dtype=torch.uint8, device="cuda")  # never read
+    A = torch.empty(16, dtype=torch.uint8, device="cuda")
+    y = torch.empty(16, dtype=torch.float32, device="cuda")
+    st = q8.lib().q8_gemm_noalloc(ctypes.c_void_p(W.data_ptr()), N, K,
+                                  ctypes.c_void_p(A.data_ptr()), M,
+                                  ctypes.c_void_p(y.data_ptr()), 0, None)
+    assert st == -8
+    assert "scratch" in q8.lib().q8_strerror(st).decode()
