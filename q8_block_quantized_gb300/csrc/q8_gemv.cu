@@ -92,24 +92,23 @@ bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, G
   q.T = (int)T;
   q.nch = (int)nch;
   if (occupancy(q.R, q.MT, fused) < 1) return false;  // also sets the smem attribute
-  int64_t nch2 = 1;
-  while (nch2 < nch) nch2 <<= 1;
-  int64_t cpp = nch2 / P > 1 ? nch2 / P : 1;
-  if (cpp > 64) cpp = 64;
+  // rounds of P chunks; a unit is RU rounds (a power of two)
+  const int64_t nrounds_all = (nch + P - 1) / P;
+  int64_t ru = 1;
+  while (ru < nrounds_all && ru < MAX_ROUNDS_PER_UNIT) ru <<= 1;
   // sized for MT rows: the kernel's reduction depth is fixed by MT, not M
   const int budget = budget_of(q.MT);
-  while (cpp > 1 && act_bytes(q.MT, P, (int)cpp) > budget) cpp >>= 1;
-  if (act_bytes(q.MT, P, (int)cpp) > budget) return false;
-  int64_t S = (nch + P * cpp - 1) / (P * cpp);
+  while (ru > 1 && act_bytes(q.MT, P, (int)ru) > budget) ru >>= 1;
+  if (act_bytes(q.MT, P, (int)ru) > budget) return false;
+  int64_t S = (nrounds_all + ru - 1) / ru;
   // too few tiles to occupy the GPU: split along K while that helps
-  while (T * S < dev.sm_count / 2 && cpp > 1) {
-    cpp >>= 1;
-    S = (nch + P * cpp - 1) / (P * cpp);
+  while (T * S < dev.sm_count / 2 && ru > 1) {
+    ru >>= 1;
+    S = (nrounds_all + ru - 1) / ru;
   }
   if (S > MAX_SPLITS) return false;
   if (S > 1 && T > MAX_SPLIT_TILES) return false;
-  q.cpp = (int)cpp;
-  q.CU = (int)(P * cpp);
+  q.RU = (int)ru;
   q.S = (int)S;
   const int64_t units = T * S;
   if (units > ((int64_t)1 << 31) - 1) return false;
@@ -117,13 +116,16 @@ bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, G
   // one CTA per SM: the second slot of each SM stays free for the next
   // kernel in the stream, which starts streaming its weights early (PDL)
   q.grid = (int)(units < dev.sm_count ? units : dev.sm_count);
-  // When every unit covers all of K, the CTAs stage the same activation
-  // blocks: clusters of up to 8 CTAs share that work (each stages 1/8 and
-  // writes it to all).  The grid is rounded down to a multiple of the
-  // cluster size (persistent CTAs pick up the remaining units).
+  // When every unit covers all of K and every CTA has exactly one unit, the
+  // CTAs stage the same activation blocks on the critical path: clusters of
+  // 4 CTAs share that work (each stages 1/4 and writes it to all).  CTAs that
+  // loop over several units stage once and amortize it, so they run
+  // unclustered (no co-scheduling constraint).  The grid is rounded down to
+  // a multiple of the cluster size (persistent CTAs pick up the remaining
+  // units).
   q.cluster = 1;
-  if (q.S == 1) {
-    for (int c = 8; c >= 2; c >>= 1) {
+  if (q.S == 1 && units <= dev.sm_count) {
+    for (int c = 4; c >= 2; c >>= 1) {
       if (q.grid >= c && cluster_fits(q.R, q.MT, fused, c)) {
         q.cluster = c;
         q.grid = q.grid / c * c;
@@ -161,8 +163,7 @@ cudaError_t launch_gemv(const GemvPlan& p, const uint8_t* W, const uint8_t* A, c
     args.nch = p.nch;
     args.T = p.T;
     args.M = Mp;
-    args.CU = p.CU;
-    args.cpp = p.cpp;
+    args.RU = p.RU;
     args.S = p.S;
     args.units = p.units;
     // A last pass with fewer rows (M > 16) may use a smaller MT.  MT 4 and 8

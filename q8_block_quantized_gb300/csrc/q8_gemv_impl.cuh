@@ -4,33 +4,32 @@
 //
 // Work decomposition.  The packed layout groups rows in tiles of R rows
 // (R in {16, 32, 64, 128}, chosen from N so a matrix has about one tile per
-// SM) and blocks in chunks of 8.  A work unit is one tile times CU aligned
-// chunks (CU a power of two); usually CU covers all of K and a tile is one
-// unit.  Inside the CTA the 128 consumer threads are R rows x P = 128/R
-// K-parts: thread (i, p) owns row i and the p-th aligned slice of cpp = CU/P
-// chunks of the unit.  The stages of the pipeline are rounds: in round rho
-// every part's chunk number rho lands in shared memory (P bulk copies, one
-// per part, placed at staggered offsets so the parts' reads do not collide
-// in the banks).
+// SM) and blocks in chunks of 8; the chunks of a tile are contiguous.  The
+// 128 consumer threads of a CTA are P = 128/R parts x R rows: thread t owns
+// row i = t % R and part p = t / R.  A pipeline round is P consecutive chunks
+// of one tile (one contiguous bulk copy of up to 34,816 bytes); part p
+// computes chunk p of the round for its row.  A work unit is one tile times
+// RU consecutive rounds; usually a unit covers all of K and a tile is one
+// unit.
 //
-// Pipeline.  Warp 4 is the producer: one lane issues cp.async.bulk copies
-// (the chunks are contiguous and 16-byte aligned in the packed layout) into
-// a ring of stages, completing on mbarriers.  Warps 0-3 consume: for each
-// block of its chunk, a thread computes the exact int32 dot of its row with
-// every activation row (__dp4a), the canonical term
-// t_b = float(isum) * (d_w * d_a), and the pairwise tree of the chunk.
+// Pipeline.  Warp 4 is the producer: one lane issues one cp.async.bulk copy
+// per round into a ring of shared-memory stages, completing on mbarriers.
+// Warps 0-3 consume: for each block of its chunk, a thread computes the exact
+// int32 dot of its row with every activation row (__dp4a), the canonical
+// term t_b = float(isum) * (d_w * d_a), and the pairwise tree of the chunk.
+// Within a quarter warp the 8 lanes read 8 consecutive rows of one chunk
+// (distinct banks) and the same activation block (a broadcast).
 //
 // Reduction order.  The sum over blocks b is the pairwise tree over b,
 // padded with zeros to a power of two.  A chunk (8 aligned blocks) is a
-// subtree; a thread merges its chunk values with a binary counter (merge
+// subtree; a round (P aligned chunks) is a subtree, formed by the part-0
+// thread of each row from the P chunk values (exchanged through shared
+// memory) in pairwise order; rounds are merged with a binary counter (merge
 // with the left sibling while the index bit is 1; what is left at the end
 // merges from the lowest level up, which is what zero padding gives), so a
-// part (cpp aligned chunks) is a subtree; the P parts of a row sit in P
-// consecutive lanes and a butterfly (shuffle-xor 1, 2, 4, ...) merges them,
-// each step adding two aligned sibling subtrees.  A unit is therefore a
-// subtree too, and when a tile is split along K into S > 1 units, the unit
-// values are merged the same way.  The result for an output depends only on
-// its row of W, its row of activations and K.
+// unit is a subtree too, and when a tile is split along K into S > 1 units,
+// the unit values are merged the same way.  The result for an output depends
+// only on its row of W, its row of activations and K.
 //
 // Split along K (S > 1: large K with many activation rows, or few tiles).
 // Each unit writes its row values to the workspace and takes a ticket on the
@@ -56,15 +55,15 @@ constexpr int SPLIT_LEVELS = 8;  // binary counter levels for S <= 128
 // never land on the tickets of another call that shares the workspace.
 constexpr int MAX_SPLIT_TILES = 4096;
 constexpr size_t TICKET_BYTES = (size_t)MAX_SPLIT_TILES * 4;
+constexpr int MAX_ROUNDS_PER_UNIT = 64;
+
 
 enum : unsigned { ERR_PRODUCER_WAIT = 1u, ERR_CONSUMER_WAIT = 2u, ERR_DRAIN_WAIT = 4u };
 
 template <int R>
 struct RCfg {
-  static constexpr int P = 128 / R;                          // K-parts per row
-  static constexpr int PAD = P > 1 ? 16 * (8 / P) : 0;       // bank stagger between parts
-  static constexpr int PSTRIDE = R * CHUNK_BLOCKS * BLOCK_BYTES + PAD;
-  static constexpr int STAGE_BYTES = P * PSTRIDE;
+  static constexpr int P = 128 / R;                                  // parts (chunks per round)
+  static constexpr int STAGE_BYTES = P * R * CHUNK_BLOCKS * BLOCK_BYTES;  // 34816
 };
 
 template <int MT>
@@ -74,25 +73,33 @@ struct MCfg {
   static constexpr int STAGES = MT <= 2 ? 3 : 2;
   // bytes of staged activations; for MT <= 2 the whole shared-memory use
   // stays below half an SM's, so two CTAs (of consecutive kernels) fit
-  static constexpr int ACT_BUDGET = MT == 1 ? 9728 : MT == 2 ? 8704 : 40960;
+  static constexpr int ACT_BUDGET = MT == 1 ? 9216 : MT == 2 ? 9088 : 40960;
 };
 
-// activation bytes of one unit in shared memory
-__host__ __device__ constexpr int act_bytes(int M, int P, int cpp) {
-  return M * P * (cpp * CHUNK_BLOCKS * 32 + (P > 1 ? 16 * (8 / P) : 0) + (cpp * CHUNK_BLOCKS + 1) * 4);
+// activation bytes of one unit (RU rounds of P chunks) in shared memory,
+// laid out for MT rows: quants [MT][blocks][32], then scales [MT][blocks]
+__host__ __device__ constexpr int act_bytes(int MT, int P, int RU) {
+  return MT * P * RU * CHUNK_BLOCKS * 36;
 }
 
 template <int R, int MT>
-__host__ __device__ constexpr int cpp_max() {
-  int c = 64;
+__host__ __device__ constexpr int ru_max() {
+  int c = MAX_ROUNDS_PER_UNIT;
   while (c > 1 && act_bytes(MT, RCfg<R>::P, c) > MCfg<MT>::ACT_BUDGET) c >>= 1;
   return c;
 }
 __host__ __device__ constexpr int log2_floor(int v) { return v <= 1 ? 0 : 1 + log2_floor(v >> 1); }
 
+// per-round exchange of chunk values between the parts of a row:
+// [2 buffers][P parts][R rows][MT]
+template <int R, int MT>
+constexpr int red_bytes() {
+  return RCfg<R>::P > 1 ? 2 * 128 * MT * 4 : 0;
+}
+
 template <int R, int MT>
 constexpr size_t gemv_smem_bytes() {
-  return (size_t)MCfg<MT>::STAGES * RCfg<R>::STAGE_BYTES + MCfg<MT>::ACT_BUDGET +
+  return (size_t)MCfg<MT>::STAGES * RCfg<R>::STAGE_BYTES + MCfg<MT>::ACT_BUDGET + red_bytes<R, MT>() +
          2 * MCfg<MT>::STAGES * sizeof(uint64_t) + 4 * sizeof(int);
 }
 
@@ -106,7 +113,7 @@ struct GemvArgs {
   unsigned* ws_cnt;      // [T] tickets (S > 1)
   unsigned* err;         // device error word
   int64_t N;
-  int NB, nch, T, M, CU, cpp, S, units;
+  int NB, nch, T, M, RU, S, units;
 };
 
 // ---- producer: one lane streams the rounds of every unit of this CTA ----
@@ -128,8 +135,8 @@ __device__ __forceinline__ void produce(const GemvArgs& a, uint8_t* stage_buf, u
   for (int u = blockIdx.x; u < a.units && !stop; u += gridDim.x) {
     const int t = u / a.S, s = u - (u / a.S) * a.S;
     const int r = tile_rows(t, a.N, R);
-    const int c0 = s * a.CU;
-    const int nrounds = min(a.cpp, a.nch - c0);
+    const int c0 = s * a.RU * P;
+    const int nrounds = min(a.RU, (a.nch - c0 + P - 1) / P);
     for (int rho = 0; rho < nrounds; ++rho) {
       if (!cluster_done && issued == STAGES) {
         asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
@@ -146,30 +153,17 @@ __device__ __forceinline__ void produce(const GemvArgs& a, uint8_t* stage_buf, u
         stop = true;
         break;
       }
-      uint8_t* sb = stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES;
-      uint32_t total = 0;
-#pragma unroll
-      for (int p = 0; p < P; ++p) {
-        const int c = c0 + p * a.cpp + rho;
-        if (c < a.nch) {
-          const uint8_t* src = a.W + chunk_offset(t, c, r, R, a.NB);
-          uint8_t* dst = sb + p * RCfg<R>::PSTRIDE;
-          const uint32_t bytes = (uint32_t)(chunk_blocks(c, a.NB) * r * BLOCK_BYTES);
-          const uint32_t bulk = bytes & ~15u;
-          for (uint32_t k = bulk; k < bytes; ++k) dst[k] = src[k];  // ragged tail < 16 B
-          total += bulk;
-        }
-      }
-      mbar_arrive_expect_tx(&full[stage], total);
-#pragma unroll
-      for (int p = 0; p < P; ++p) {
-        const int c = c0 + p * a.cpp + rho;
-        if (c < a.nch) {
-          const uint8_t* src = a.W + chunk_offset(t, c, r, R, a.NB);
-          const uint32_t bulk = (uint32_t)(chunk_blocks(c, a.NB) * r * BLOCK_BYTES) & ~15u;
-          bulk_g2s(sb + p * RCfg<R>::PSTRIDE, src, bulk, &full[stage], pol);
-        }
-      }
+      // the round's chunks are contiguous: one copy (ragged tail by hand)
+      const int cb = c0 + rho * P;
+      const int ce = min(cb + P, a.nch);
+      const uint8_t* src = a.W + chunk_offset(t, cb, r, R, a.NB);
+      const uint32_t bytes = (uint32_t)(((int64_t)min(ce * CHUNK_BLOCKS, a.NB) - (int64_t)cb * CHUNK_BLOCKS) *
+                                        r * BLOCK_BYTES);
+      const uint32_t bulk = bytes & ~15u;
+      uint8_t* dst = stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES;
+      for (uint32_t k = bulk; k < bytes; ++k) dst[k] = src[k];  // < 16 bytes
+      mbar_arrive_expect_tx(&full[stage], bulk);
+      bulk_g2s(dst, src, bulk, &full[stage], pol);
       misc[2] = ++issued;
       if (++stage == STAGES) {
         stage = 0;
@@ -183,24 +177,20 @@ __device__ __forceinline__ void produce(const GemvArgs& a, uint8_t* stage_buf, u
   }
 }
 
-// Shared-memory positions of the staged activation blocks of a unit: for
-// row m and block jj of part p, quants at act_q + (m*P + p)*qpart + jj*32 and
-// the scale (as float) at act_d[(m*P + p)*dpart + jj].
+// Staged activation blocks of a unit, in block order: quants of row m,
+// block blk at q + (m*UB + blk)*32, its scale (as float) at d[m*UB + blk],
+// UB = blocks per unit.
 struct ActLayout {
   uint8_t* q;
   float* d;
-  int qpart, dpart, APB;
+  int UB;
 };
 
-template <int R>
-__device__ __forceinline__ ActLayout act_layout(uint8_t* base, int M, int cpp) {
-  constexpr int P = RCfg<R>::P;
+__device__ __forceinline__ ActLayout act_layout(uint8_t* base, int MT, int UB) {
   ActLayout L;
-  L.APB = cpp * CHUNK_BLOCKS;
-  L.qpart = L.APB * 32 + (P > 1 ? 16 * (8 / P) : 0);
-  L.dpart = L.APB + 1;
+  L.UB = UB;
   L.q = base;
-  L.d = reinterpret_cast<float*>(base + (size_t)M * P * L.qpart);
+  L.d = reinterpret_cast<float*>(base + (size_t)MT * UB * 32);
   return L;
 }
 
@@ -210,13 +200,10 @@ __device__ __forceinline__ ActLayout act_layout(uint8_t* base, int M, int cpp) {
 // area of every CTA of the cluster (distributed shared memory); the caller
 // then waits on the cluster barrier.  Loads of two blocks per thread are
 // issued before either is used.
-template <int R>
 __device__ __forceinline__ void put_block(const ActLayout& L, int m, int blk, const uint32_t (&w)[8],
                                           float d, uint32_t CL) {
-  constexpr int P = RCfg<R>::P;
-  const int p = blk / L.APB, jj = blk - p * L.APB;
-  uint8_t* dst = L.q + (m * P + p) * L.qpart + jj * 32;
-  float* dd = L.d + (m * P + p) * L.dpart + jj;
+  uint8_t* dst = L.q + (m * L.UB + blk) * 32;
+  float* dd = L.d + m * L.UB + blk;
   if (CL == 1) {
     *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
     *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
@@ -232,7 +219,7 @@ __device__ __forceinline__ void put_block(const ActLayout& L, int m, int blk, co
   }
 }
 
-template <int R, bool FUSED>
+template <bool FUSED>
 __device__ __forceinline__ void stage_one(const GemvArgs& a, const ActLayout& L, int b0, int nblk,
                                           int idx0, int idx1, bool h0, bool h1, uint32_t CL) {
   const int64_t K = (int64_t)a.NB * QK;
@@ -252,13 +239,13 @@ __device__ __forceinline__ void stage_one(const GemvArgs& a, const ActLayout& L,
       }
       quantize_block_thread(v0, w0, d0);
       quantize_block_thread(v1, w1, d1);
-      put_block<R>(L, m0, k0, w0, d0, CL);
-      put_block<R>(L, m1, k1, w1, d1, CL);
+      put_block(L, m0, k0, w0, d0, CL);
+      put_block(L, m1, k1, w1, d1, CL);
     } else if (h0) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) v0[k] = __ldcg(s0 + k);
       quantize_block_thread(v0, w0, d0);
-      put_block<R>(L, m0, k0, w0, d0, CL);
+      put_block(L, m0, k0, w0, d0, CL);
     }
   } else {
     uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0, r0 = q0, r1 = q0;
@@ -275,41 +262,39 @@ __device__ __forceinline__ void stage_one(const GemvArgs& a, const ActLayout& L,
     }
     if (h0) {
       const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-      put_block<R>(L, m0, k0, w, __half2float(__ushort_as_half(d0)), CL);
+      put_block(L, m0, k0, w, __half2float(__ushort_as_half(d0)), CL);
     }
     if (h1) {
       const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-      put_block<R>(L, m1, k1, w, __half2float(__ushort_as_half(d1)), CL);
+      put_block(L, m1, k1, w, __half2float(__ushort_as_half(d1)), CL);
     }
   }
 }
 
-template <int R, bool FUSED, int NT>
+template <bool FUSED, int NT>
 __device__ __forceinline__ void stage_activations(const GemvArgs& a, const ActLayout& L, int b0,
                                                   int nblk, uint32_t rank, uint32_t CL) {
   const int total = a.M * nblk;
   const int mine = (total - (int)rank + (int)CL - 1) / (int)CL;  // blocks rank, rank+CL, ...
   for (int base = 0; base < mine; base += 2 * NT) {
     const int j0 = base + threadIdx.x, j1 = j0 + NT;
-    stage_one<R, FUSED>(a, L, b0, nblk, j0 * (int)CL + (int)rank, j1 * (int)CL + (int)rank, j0 < mine,
-                        j1 < mine, CL);
+    stage_one<FUSED>(a, L, b0, nblk, j0 * (int)CL + (int)rank, j1 * (int)CL + (int)rank, j0 < mine,
+                     j1 < mine, CL);
   }
 }
 
 // Fused path: the CTAs that own row tile 0 publish the quantized activations
 // of their K range (every K range is covered once by tile 0).
-template <int R, int NT>
+template <int NT>
 __device__ __forceinline__ void write_act_blocks(const GemvArgs& a, const ActLayout& L, int b0,
                                                  int nblk) {
-  constexpr int P = RCfg<R>::P;
   const int total = a.M * nblk;
   for (int idx = threadIdx.x; idx < total; idx += NT) {
     const int m = idx / nblk, blk = idx - m * nblk;
-    const int p = blk / L.APB, jj = blk - p * L.APB;
     uint8_t* ob = a.A_out + ((int64_t)m * a.NB + b0 + blk) * BLOCK_BYTES;
-    const float d = L.d[(m * P + p) * L.dpart + jj];
+    const float d = L.d[m * L.UB + blk];
     const uint16_t d16 = __half_as_ushort(__float2half_rn(d));  // exact: d came from binary16
-    const uint8_t* q = L.q + (m * P + p) * L.qpart + jj * 32;
+    const uint8_t* q = L.q + (m * L.UB + blk) * 32;
     unsigned short* o16 = reinterpret_cast<unsigned short*>(ob);
     o16[0] = d16;
 #pragma unroll
@@ -343,25 +328,25 @@ __device__ __forceinline__ void block_terms(const uint8_t* cq, const uint8_t* sc
   }
 }
 
-// Blocks j0 .. j0+NBLK-1 (NBLK = 8: a chunk, 4: half a chunk; blocks at or
-// past kb count as zero) of row i: their pairwise tree, per activation row.
-// aq/ad point at this part's first block of the chunk; mq/md are the strides
-// between activation rows.  Rows m >= M are computed on whatever the staging
-// area holds and never stored.
-template <int MT, int NBLK>
-__device__ __forceinline__ void chunk_value(const uint8_t* cq, int r, int kb, int i, int j0,
+// One chunk (kb <= 8 blocks; blocks at or past kb count as zero) of row i:
+// the pairwise tree of its blocks, per activation row.  aq/ad point at the
+// chunk's first activation block; mq/md are the strides between activation
+// rows.  Rows m >= M are computed on whatever the staging area holds and
+// never stored.
+template <int MT>
+__device__ __forceinline__ void chunk_value(const uint8_t* cq, int r, int kb, int i,
                                             const uint8_t* aq, const float* ad, int mq, int md,
                                             float (&v)[MT]) {
   const uint8_t* sc = cq + kb * r * 32;
-  const bool full = (j0 + NBLK <= kb);
-  float q[NBLK / 4][MT];
+  const bool full = (kb == CHUNK_BLOCKS);
+  float q[2][MT];
 #pragma unroll
-  for (int h4 = 0; h4 < NBLK / 4; ++h4) {
+  for (int h4 = 0; h4 < 2; ++h4) {
     float p0[MT], p1[MT];
 #pragma unroll
     for (int h2 = 0; h2 < 2; ++h2) {
       float ta[MT], tb[MT];
-      const int j = j0 + 4 * h4 + 2 * h2;
+      const int j = 4 * h4 + 2 * h2;
       if (full || j < kb) {
         block_terms<MT>(cq, sc, r, i, j, aq, ad, mq, md, ta);
       } else {
@@ -381,7 +366,17 @@ __device__ __forceinline__ void chunk_value(const uint8_t* cq, int r, int kb, in
     for (int m = 0; m < MT; ++m) q[h4][m] = tadd(p0[m], p1[m]);
   }
 #pragma unroll
-  for (int m = 0; m < MT; ++m) v[m] = NBLK == 8 ? tadd(q[0][m], q[NBLK / 4 - 1][m]) : q[0][m];
+  for (int m = 0; m < MT; ++m) v[m] = tadd(q[0][m], q[1][m]);
+}
+
+// pairwise tree of the P chunk values of a round (P a power of two)
+template <int P>
+__device__ __forceinline__ float tree_of(const float* w, int stride) {
+  if constexpr (P == 1) {
+    return w[0];
+  } else {
+    return tadd(tree_of<P / 2>(w, stride), tree_of<P / 2>(w + (P / 2) * stride, stride));
+  }
 }
 
 template <int R, int MT, bool FUSED>
@@ -390,12 +385,13 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
   constexpr int NCW = MCfg<MT>::NCW;
   constexpr int NT = NCW * 32;  // consumer threads
   constexpr int STAGES = MCfg<MT>::STAGES;
-  constexpr int LV = log2_floor(cpp_max<R, MT>()) + 1;
+  constexpr int LV = log2_floor(ru_max<R, MT>()) + 1;
   constexpr int BAR_CONSUMERS = 1;  // named barrier of the consumer warps
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stage_buf = smem;
   uint8_t* act_base = smem + (size_t)STAGES * RCfg<R>::STAGE_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(act_base + MCfg<MT>::ACT_BUDGET);
+  float* red = reinterpret_cast<float*>(act_base + MCfg<MT>::ACT_BUDGET);  // [2][P][R][MT]
+  uint64_t* full = reinterpret_cast<uint64_t*>(act_base + MCfg<MT>::ACT_BUDGET + red_bytes<R, MT>());
   uint64_t* empty = full + STAGES;
   volatile int* misc = reinterpret_cast<volatile int*>(empty + STAGES);
   // misc[0]: abort flag, misc[1]: "this CTA combines the tile", misc[2]: rounds issued
@@ -416,15 +412,13 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
   // A cluster (launched only when every unit covers all of K, so every CTA
   // stages the same blocks) stages its activations cooperatively.  Barrier
   // phase 1: every CTA of the cluster is running before any writes into
-  // another's shared memory.  Phase 2: all staged blocks have landed; the
-  // producer lane arrives for it up front, the producer warp's other lanes
-  // have exited by then (exited threads do not take part).
+  // another's shared memory.  Phase 2: all staged blocks have landed.
   const uint32_t CL = cluster_nctarank();
   const uint32_t crank = cluster_ctarank();
   if (warp == NCW) {
     if (CL > 1) {
-      // phase 1 for the producer warp: lane 0 arrives and waits inside
-      // produce(); lanes 1-31 arrive, wait, and exit (exited threads do not
+      // phase 1 for the producer warp: lane 0 arrives now and waits inside
+      // produce(); lanes 1-31 arrive, wait and exit (exited threads do not
       // take part in phase 2)
       __syncwarp();
       cluster_arrive_aligned();
@@ -441,12 +435,12 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
     cluster_wait_aligned();
   }
 
-  const int p = threadIdx.x % P;  // K-part
-  const int i = threadIdx.x / P;  // row inside the tile
+  const int i = threadIdx.x % R;  // row inside the tile
+  const int p = threadIdx.x / R;  // part: chunk p of each round
+  const int UB = a.RU * P * CHUNK_BLOCKS;  // activation blocks per unit
   // laid out for MT rows (the planner sized the unit for MT), so rows
   // M <= m < MT read inside the staging area
-  const ActLayout L = act_layout<R>(act_base, MT, a.cpp);
-  const int mq = P * L.qpart, md = P * L.dpart;
+  const ActLayout L = act_layout(act_base, MT, UB);
   int stage = 0;
   uint32_t phase = 0;
   int consumed = 0;
@@ -457,10 +451,10 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
   for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
     const int t = u / a.S, s = u - (u / a.S) * a.S;
     const int r = tile_rows(t, a.N, R);
-    const int c0 = s * a.CU;
-    const int nrounds = min(a.cpp, a.nch - c0);
+    const int c0 = s * a.RU * P;
+    const int nrounds = min(a.RU, (a.nch - c0 + P - 1) / P);
     const int b0 = c0 * CHUNK_BLOCKS;
-    const int nblk = min(a.CU * CHUNK_BLOCKS, a.NB - b0);
+    const int nblk = min(UB, a.NB - b0);
     const int64_t n = (int64_t)t * R + i;
 
     if (!waited) {
@@ -469,19 +463,19 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
     }
     if (s != staged_s) {  // units with the same K range reuse the staged blocks
       if (CL > 1) {        // once per CTA: the planner clusters only when S == 1
-        stage_activations<R, FUSED, NT>(a, L, b0, nblk, crank, CL);
+        stage_activations<FUSED, NT>(a, L, b0, nblk, crank, CL);
         __syncwarp();
         cluster_arrive_aligned();
         cluster_wait_aligned();
       } else {
         named_bar_sync(BAR_CONSUMERS, NT);
-        stage_activations<R, FUSED, NT>(a, L, b0, nblk, 0u, 1u);
+        stage_activations<FUSED, NT>(a, L, b0, nblk, 0u, 1u);
         named_bar_sync(BAR_CONSUMERS, NT);
       }
       staged_s = s;
     }
     if constexpr (FUSED) {
-      if (a.A_out != nullptr && t == 0) write_act_blocks<R, NT>(a, L, b0, nblk);
+      if (a.A_out != nullptr && t == 0) write_act_blocks<NT>(a, L, b0, nblk);
     }
 
     float slot[MT][LV];
@@ -491,32 +485,52 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
       for (int l = 0; l < LV; ++l) slot[m][l] = 0.0f;
 
     for (int rho = 0; rho < nrounds; ++rho) {
-      if (ok && misc[0]) ok = false;
-      if (!ok) break;
-      if (!mbar_wait_bounded(&full[stage], phase, WAIT_LIMIT_NS)) {
+      // the abort decision must be the same for every consumer (they meet
+      // at the exchange barrier below), so it is read after that barrier
+      const bool got = mbar_wait_bounded(&full[stage], phase, WAIT_LIMIT_NS);
+      if (!got) {
         atomicOr(a.err, ERR_CONSUMER_WAIT);
         misc[0] = 1;
-        ok = false;
-        break;
       }
-      const int c = c0 + p * a.cpp + rho;
+      const int c = c0 + rho * P + p;
       float v[MT];
 #pragma unroll
       for (int m = 0; m < MT; ++m) v[m] = 0.0f;
-      if (c < a.nch) {
-        const int jj0 = rho * CHUNK_BLOCKS;
-        chunk_value<MT, CHUNK_BLOCKS>(stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES + p * RCfg<R>::PSTRIDE,
-                                      r, chunk_blocks(c, a.NB), i, 0, L.q + p * L.qpart + jj0 * 32,
-                                      L.d + p * L.dpart + jj0, mq, md, v);
+      if (got && c < a.nch) {
+        const int blk = (rho * P + p) * CHUNK_BLOCKS;  // first block of the chunk in the unit
+        chunk_value<MT>(stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES + p * (r * CHUNK_BLOCKS * BLOCK_BYTES),
+                        r, chunk_blocks(c, a.NB), i, L.q + blk * 32, L.d + blk, UB * 32, UB, v);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stage]);
+      const int xpar = consumed & 1;
       ++consumed;
       if (++stage == STAGES) {
         stage = 0;
         phase ^= 1u;
       }
-      // binary counter over this part's chunk subtrees
+      if constexpr (P > 1) {
+        // the P chunk values of row i meet in shared memory; the buffer
+        // written in round k was last read in round k-2, before the barrier
+        // of round k-1 that every writer has passed
+        float* rb = red + (size_t)xpar * P * R * MT;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) rb[(p * R + i) * MT + m] = v[m];
+        named_bar_sync(BAR_CONSUMERS, NT);
+        if (misc[0]) {
+          ok = false;
+          break;
+        }
+        if (p != 0) continue;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) v[m] = tree_of<P>(rb + i * MT + m, R * MT);
+      } else {
+        if (!got || misc[0]) {
+          ok = false;
+          break;
+        }
+      }
+      // binary counter over the round subtrees (part-0 threads)
       bool placed = false;
 #pragma unroll
       for (int l = 0; l < LV; ++l) {
@@ -546,26 +560,21 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
         have = true;
       }
     }
-    // the P parts of row i are P consecutive lanes: butterfly over parts
-#pragma unroll
-    for (int off = 1; off < P; off <<= 1)
-#pragma unroll
-      for (int m = 0; m < MT; ++m) pv[m] = tadd(pv[m], __shfl_xor_sync(0xffffffffu, pv[m], off));
 
     if (a.S == 1) {
-      if (ok && i < r) {
+      if (ok && p == 0 && i < r) {
 #pragma unroll
         for (int m = 0; m < MT; ++m)
-          if (m < a.M && (m % P) == p) a.y[(int64_t)m * a.N + n] = pv[m];
+          if (m < a.M) a.y[(int64_t)m * a.N + n] = pv[m];
       }
       continue;
     }
 
     // split along K: publish the unit value, take a ticket, last one combines
-    if (ok && i < r) {
+    if (ok && p == 0 && i < r) {
 #pragma unroll
       for (int m = 0; m < MT; ++m)
-        if (m < a.M && (m % P) == p) a.ws_part[((int64_t)s * a.M + m) * a.N + n] = pv[m];
+        if (m < a.M) a.ws_part[((int64_t)s * a.M + m) * a.N + n] = pv[m];
     }
     __threadfence();
     named_bar_sync(BAR_CONSUMERS, NT);
@@ -578,7 +587,7 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
     if (misc[1]) {
       __threadfence();
       if (i < r) {
-        for (int m = p; m < a.M; m += P) {
+        for (int m = p; m < a.M; m += P) {  // every part thread of the row takes some m
           float sl[SPLIT_LEVELS];
 #pragma unroll
           for (int l = 0; l < SPLIT_LEVELS; ++l) sl[l] = 0.0f;

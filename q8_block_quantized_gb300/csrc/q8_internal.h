@@ -9,8 +9,8 @@
 namespace q8 {
 
 // Launch plan of one GEMV call: the work is cut into units of one R-row
-// tile x CU chunks of 8 blocks (CU = P * cpp, P = 128 / R parts of cpp
-// chunks each), S units per tile along K.
+// tile x RU rounds of P = 128 / R chunks (8 blocks each), S units per tile
+// along K.
 struct GemvPlan {
   int64_t N = 0, K = 0, NB = 0;
   int M = 0;
@@ -18,8 +18,7 @@ struct GemvPlan {
   int R = 0;         // packed tile height
   int T = 0;         // row tiles
   int nch = 0;       // chunks along K
-  int cpp = 0;       // chunks per part
-  int CU = 0;        // chunks per unit
+  int RU = 0;        // rounds per unit
   int S = 0;         // units per tile (splits along K)
   int units = 0;
   int grid = 0;      // persistent CTAs
