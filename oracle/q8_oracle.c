@@ -22,6 +22,8 @@
  *     from zero), 1/d taken from the fp32 d (not from the stored fp16), d
  *     stored as IEEE binary16 rounded to nearest-even, subnormals kept.
  *   - amax == 0: d = 0, all q = 0.
+ *   - d below 2^-128 (amax subnormal or nearly): 1/d overflows to inf, nonzero
+ *     values clamp to +-127, and a zero value (0 * inf = NaN) stays 0.
  *   - block byte order: fp16 d little-endian at bytes 0..1, q[0..31] at
  *     bytes 2..33 (34 bytes per block).
  *   - output: y[m][n] = sum_b isum_b * d_w * d_a, accumulated here in fp64;
@@ -140,6 +142,9 @@ void q8o_quantize_block(const float *x, uint8_t *out)
         float r = roundf(v);
         if (r > 127.0f) r = 127.0f;
         if (r < -127.0f) r = -127.0f;
+        /* x * (1/d) is NaN only for x = 0 with 1/d = inf (d below 2^-128):
+         * a zero value quantizes to zero */
+        if (r != r) r = 0.0f;
         int qi = (int)r;
         out[2 + i] = (uint8_t)(qi & 0xff);   /* two's-complement int8 byte */
     }

@@ -134,6 +134,19 @@ def test_quantize_unit_scale_ties_away_from_zero():
     assert not q[0, 0, len(vals):].any()
 
 
+def test_quantize_block_with_overflowing_reciprocal():
+    # amax = 1e-40 (subnormal): d = amax/127 is below 2^-128, so 1/d
+    # overflows to inf; every nonzero value then maps to +-inf before the
+    # clamp, i.e. to +-127, zeros (0 * inf) stay 0, and the scale rounds to
+    # binary16 zero
+    x = np.zeros(32, dtype=np.float32)
+    x[:5] = [-1e-40, 1e-40, 0.0, -0.0, -3e-45]
+    d16, q = oracle.split_blocks(oracle.quantize(x), 32)
+    assert d16[0, 0] == 0
+    assert q[0, 0, :5].tolist() == [-127, 127, 0, 0, -127]
+    assert not q[0, 0, 5:].any()
+
+
 def test_quantize_zero_constant_and_one_hot_blocks():
     z = oracle.quantize(np.zeros((1, 64), np.float32))
     assert not z.any()  # d = 0 and every q = 0: all 34 bytes zero, twice
