@@ -51,11 +51,65 @@ __host__ __device__ __forceinline__ int chunk_scale_off(int j, int i, int r, int
 }
 
 // ---------------------------------------------------------------------------
+// Correctly rounded amax / 127 and 1 / d without the division routines.  The
+// quantization rule needs both exactly (their bits decide the quants); the
+// IEEE division and reciprocal routines carry data-dependent slow paths
+// whose branches keep the compiler from overlapping the blocks of a batch.
+// Both functions below use only IEEE multiplies and fmas, so their results
+// do not depend on the machine; each was checked against IEEE division on
+// the host (every non-negative finite float for the quotient; every
+// subnormal and every significand at the boundary and typical exponents for
+// the reciprocal, whose steps are exponent-independent in between).
+// ---------------------------------------------------------------------------
+
+// a / 127 for a >= 0: Markstein's correction of the estimate q0 = a * RN(1/127)
+// with the exact fma remainder a - 127 q0 (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990).  inf and NaN pass through (a / 127 = a for them).
+__device__ __forceinline__ float div127_rn(float a) {
+  const float r = 0x1.020408p-7f;  // RN(1/127)
+  const float q0 = __fmul_rn(a, r);
+  const float rem = __fmaf_rn(-q0, 127.0f, a);
+  const float q1 = __fmaf_rn(rem, r, q0);
+  return (a <= 3.40282347e38f) ? q1 : a;
+}
+
+// 1 / d for a normal d with a normal reciprocal (d <= 2^126): a first
+// estimate from the bit pattern (exponent negated, significand mirrored;
+// relative error at most 1/8), then Newton-Raphson steps y += y (1 - d y)
+// with fma, each squaring the relative error.  After four steps the result
+// is the correctly rounded reciprocal except when the significand of d is all
+// ones: 1/d then lies just above a rounding tie that the last step resolves
+// downwards, so the answer is one ulp up (the known exception of the fma
+// correction step in Markstein's theorem).
+__device__ __forceinline__ float rcp_rn_normal(float d) {
+  float y = __uint_as_float(0x7EF00000u - __float_as_uint(d));
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float e = __fmaf_rn(-d, y, 1.0f);
+    y = __fmaf_rn(y, e, y);
+  }
+  return ((__float_as_uint(d) & 0x7FFFFFu) == 0x7FFFFFu) ? __uint_as_float(__float_as_uint(y) + 1u) : y;
+}
+
+// The reciprocal the quantization rule takes, for d = amax/127 (0 <= d <=
+// 2^121, or inf/NaN): 0 for d = 0 and for d = inf; a subnormal d is scaled by
+// 2^24 first and the result scaled back (exact, or the correctly rounded
+// overflow to inf).
+__device__ __forceinline__ float rcp_rn(float d) {
+  const bool sub = d < 0x1p-126f;
+  const float ds = sub ? __fmul_rn(d, 0x1p24f) : d;
+  const float ys = rcp_rn_normal(ds);
+  const float y = sub ? __fmul_rn(ys, 0x1p24f) : ys;
+  return (d == 0.0f || d > 3.40282347e38f) ? 0.0f : y;
+}
+
+// ---------------------------------------------------------------------------
 // Quantization of one 32-value block, one value per lane of a full warp.
-// d = amax / 127 (fp32, IEEE division), id = 1/d (0 when d == 0),
-// q = roundf(x * id) (ties away from zero), scale stored as binary16 (RNE).
-// Every operation is an explicitly rounded single-precision intrinsic, so the
-// result does not depend on compiler flags.
+// d = amax / 127 (fp32, correctly rounded), id = 1/d (correctly rounded; 0
+// when d == 0), q = roundf(x * id) (ties away from zero), scale stored as
+// binary16 (RNE).  Every operation is an explicitly rounded single-precision
+// intrinsic, so the result does not depend on compiler flags.
 // ---------------------------------------------------------------------------
 struct LaneQuant {
   int q;            // this lane's quant, in [-127, 127]
@@ -67,25 +121,30 @@ __device__ __forceinline__ LaneQuant quantize_lane(float x) {
   float amax = fabsf(x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const float d = __fdiv_rn(amax, 127.0f);
-  const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
-  float r = roundf(__fmul_rn(x, id));
-  r = fminf(fmaxf(r, -127.0f), 127.0f);
+  const float d = div127_rn(amax);
+  const float id = rcp_rn(d);
+  // the conversion (cvt.rzi, saturating) takes +-inf (1/d = inf, d below
+  // 2^-128) to the int range and NaN (0 * inf) to 0; the clamp then gives
+  // [-127, 127]
   LaneQuant out;
-  out.q = (int)r;
+  out.q = min(max(__float2int_rz(roundf(__fmul_rn(x, id))), -127), 127);
   const __half h = __float2half_rn(d);
   out.d16 = __half_as_ushort(h);
   out.d_stored = __half2float(h);
   return out;
 }
 
-// The same rule for one block held by one thread (32 values in 8 float4):
-// the same single-precision results, so the bits match quantize_lane's.
-//  - amax: max is exact and order-free, so a tree of maxima is used;
-//  - 1/d: __frcp_rn is the correctly rounded reciprocal, i.e. the IEEE
-//    quotient 1/d;
-//  - no clamp: |x * (1/d)| <= 127 * (1 + 2^-22) < 127.5 for every value of
-//    the block, so roundf already lands in [-127, 127].
+// The same rule with the block's 32 values spread over fewer lanes gives the
+// same single-precision results, so the bits match quantize_lane's:
+//  - amax: max is exact and order-free, so any tree of maxima will do;
+//  - d and 1/d come from the same correctly rounded functions;
+//  - the clamp: |x * (1/d)| <= 127 * (1 + 2^-22) < 127.5 whenever 1/d is
+//    finite, so roundf lands in [-127, 127]; with 1/d = inf (d below
+//    2^-128) the products are +-inf, which the conversion (cvt.rzi,
+//    saturating) takes to the int range and the lower bound to -127 (the
+//    pack saturates the upper side), or NaN for x = 0, which it takes to 0.
+__device__ __forceinline__ int q8_of(float v) { return max(__float2int_rz(roundf(v)), -127); }
+
 // packed[k] holds quants 4k..4k+3, low byte first.
 // cvt.pack.sat.s8.s32.b32 d, x, y, z puts y in byte 0, x in byte 1 and the
 // low 16 bits of z in bytes 2-3; so (a, b, c, d) land in bytes 0..3.
@@ -96,26 +155,35 @@ __device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
   return r;
 }
 
-__device__ __forceinline__ void quantize_block_thread(const float4 (&v)[8], uint32_t (&packed)[8],
-                                                      float& d_stored) {
-  float m4[4];
+// The same rule for B blocks at once, each spread over 8 consecutive lanes
+// of a warp: lane s of a group (s = lane % 8) holds values 4s..4s+3 of its
+// block in v[q] and gets back their 4 quants packed (low byte first) in
+// w[q]; every lane of the group gets the stored scale in d[q].  Each
+// shuffle level is taken for all B blocks together so their dependency
+// chains overlap.  All 32 lanes of the warp must call it (full-mask
+// shuffles; a lane with nothing to quantize passes zeros).
+template <int B>
+__device__ __forceinline__ void quantize_group8(const float4 (&v)[B], uint32_t (&w)[B], float (&d)[B]) {
+  float am[B];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const float a0 = fmaxf(fabsf(v[2 * c].x), fabsf(v[2 * c].y));
-    const float a1 = fmaxf(fabsf(v[2 * c].z), fabsf(v[2 * c].w));
-    const float a2 = fmaxf(fabsf(v[2 * c + 1].x), fabsf(v[2 * c + 1].y));
-    const float a3 = fmaxf(fabsf(v[2 * c + 1].z), fabsf(v[2 * c + 1].w));
-    m4[c] = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
-  }
-  const float amax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-  const float d = __fdiv_rn(amax, 127.0f);
-  const float id = (d != 0.0f) ? __frcp_rn(d) : 0.0f;
+  for (int q = 0; q < B; ++q)
+    am[q] = fmaxf(fmaxf(fabsf(v[q].x), fabsf(v[q].y)), fmaxf(fabsf(v[q].z), fabsf(v[q].w)));
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    packed[k] = pack4_s8((int)roundf(__fmul_rn(v[k].x, id)), (int)roundf(__fmul_rn(v[k].y, id)),
-                         (int)roundf(__fmul_rn(v[k].z, id)), (int)roundf(__fmul_rn(v[k].w, id)));
+  for (int o = 1; o < 8; o <<= 1) {
+    float t[B];
+#pragma unroll
+    for (int q = 0; q < B; ++q) t[q] = __shfl_xor_sync(0xffffffffu, am[q], o);
+#pragma unroll
+    for (int q = 0; q < B; ++q) am[q] = fmaxf(am[q], t[q]);
   }
-  d_stored = __half2float(__float2half_rn(d));
+#pragma unroll
+  for (int q = 0; q < B; ++q) {
+    const float dq = div127_rn(am[q]);
+    const float id = rcp_rn(dq);
+    d[q] = __half2float(__float2half_rn(dq));
+    w[q] = pack4_s8(q8_of(__fmul_rn(v[q].x, id)), q8_of(__fmul_rn(v[q].y, id)),
+                    q8_of(__fmul_rn(v[q].z, id)), q8_of(__fmul_rn(v[q].w, id)));
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -143,6 +211,34 @@ __device__ __forceinline__ float block_term(int isum, float dw, float da) {
 }
 
 __device__ __forceinline__ float tadd(float a, float b) { return __fadd_rn(a, b); }
+
+// ---------------------------------------------------------------------------
+// int8 -> fp16 for the tensor-core path.  For a byte x in [-128, 127],
+// (x + 128) written into the low byte of the binary16 pattern 0x6400
+// (= 1024, exponent 25, ulp 1) encodes 1024 + x + 128 exactly; subtracting
+// 1152 (0x6480) leaves x, exactly.  Four int8 -> two half2:
+//   lo = {x0, x1}, hi = {x2, x3} (low half first).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t f = w ^ 0x80808080u;
+  const uint32_t l = __byte_perm(f, 0x64646464u, 0x5140);
+  const uint32_t h = __byte_perm(f, 0x64646464u, 0x5342);
+  const __half2 bias = __halves2half2(__ushort_as_half((unsigned short)0x6480),
+                                      __ushort_as_half((unsigned short)0x6480));
+  const __half2 rl = __hsub2(*reinterpret_cast<const __half2*>(&l), bias);
+  const __half2 rh = __hsub2(*reinterpret_cast<const __half2*>(&h), bias);
+  lo = *reinterpret_cast<const uint32_t*>(&rl);
+  hi = *reinterpret_cast<const uint32_t*>(&rh);
+}
+
+// D = A * B + C, m16n8k16, fp16 inputs, fp32 accumulate (warp-wide).
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 
 // ---------------------------------------------------------------------------
 // Small PTX wrappers.
@@ -243,6 +339,9 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
                "r"(d)
                : "memory");
 }
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
@@ -257,6 +356,9 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 }
 __device__ __forceinline__ uint4 lds128(const void* p) {
   return *reinterpret_cast<const uint4*>(p);
+}
+__device__ __forceinline__ uint32_t lds32(const void* p) {
+  return *reinterpret_cast<const uint32_t*>(p);
 }
 
 // 32 quants of an unaligned 34-byte block (2-byte aligned) as two uint4.

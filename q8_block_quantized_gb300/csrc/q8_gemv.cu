@@ -117,15 +117,25 @@ bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, G
   // kernel in the stream, which starts streaming its weights early (PDL)
   q.grid = (int)(units < dev.sm_count ? units : dev.sm_count);
   // When every unit covers all of K and every CTA has exactly one unit, the
-  // CTAs stage the same activation blocks on the critical path: clusters of
-  // 4 CTAs share that work (each stages 1/4 and writes it to all).  CTAs that
-  // loop over several units stage once and amortize it, so they run
-  // unclustered (no co-scheduling constraint).  The grid is rounded down to
-  // a multiple of the cluster size (persistent CTAs pick up the remaining
-  // units).
+  // CTAs stage the same activation blocks on the critical path.  If one CTA
+  // would stage more than STAGE_TARGET_BLOCKS of them, clusters of 2 or 4 CTAs
+  // share the work (each stages 1/c and writes it to all, then a cluster
+  // barrier); otherwise each CTA stages everything itself, which is cheaper
+  // than the barrier.  CTAs that loop over several units stage once and
+  // amortize it, so they run unclustered (no co-scheduling constraint).  The
+  // grid is rounded down to a multiple of the cluster size (persistent CTAs
+  // pick up the remaining units).
   q.cluster = 1;
   if (q.S == 1 && units <= dev.sm_count) {
-    for (int c = 4; c >= 2; c >>= 1) {
+    const int64_t blocks = (int64_t)Mp * q.NB;
+#if defined(Q8_MAX_CLUSTER)
+    const int cmax = Q8_MAX_CLUSTER;
+#else
+    const int cmax = 4;
+#endif
+    int want = 1;
+    while (want < cmax && (blocks + want - 1) / want > STAGE_TARGET_BLOCKS) want <<= 1;
+    for (int c = want; c >= 2; c >>= 1) {
       if (q.grid >= c && cluster_fits(q.R, q.MT, fused, c)) {
         q.cluster = c;
         q.grid = q.grid / c * c;

@@ -56,6 +56,12 @@ constexpr int SPLIT_LEVELS = 8;  // binary counter levels for S <= 128
 constexpr int MAX_SPLIT_TILES = 4096;
 constexpr size_t TICKET_BYTES = (size_t)MAX_SPLIT_TILES * 4;
 constexpr int MAX_ROUNDS_PER_UNIT = 64;
+// Blocks one CTA stages by itself before the planner shares the staging
+// among the CTAs of a cluster.
+#ifndef Q8_STAGE_TARGET
+#define Q8_STAGE_TARGET 64
+#endif
+constexpr int STAGE_TARGET_BLOCKS = Q8_STAGE_TARGET;
 
 
 enum : unsigned { ERR_PRODUCER_WAIT = 1u, ERR_CONSUMER_WAIT = 2u, ERR_DRAIN_WAIT = 4u };
@@ -71,15 +77,27 @@ struct MCfg {
   static constexpr int NCW = 4;                       // consumer warps: 128 threads
   static constexpr int THREADS = (NCW + 1) * 32;      // + the producer warp
   static constexpr int STAGES = MT <= 2 ? 3 : 2;
+  // activation staging: passes of 16 blocks (8 lanes per block), STAGE_BATCH
+  // passes with their loads in flight together (larger batches measured
+  // slower for every row count)
+  static constexpr int STAGE_BATCH = 4;
   // bytes of staged activations; for MT <= 2 the whole shared-memory use
   // stays below half an SM's, so two CTAs (of consecutive kernels) fit
   static constexpr int ACT_BUDGET = MT == 1 ? 9216 : MT == 2 ? 9088 : 40960;
 };
 
+// Activation rows at or above this use the tensor-core path.
+constexpr int TC_MIN_MT = 8;
+
 // activation bytes of one unit (RU rounds of P chunks) in shared memory,
-// laid out for MT rows: quants [MT][blocks][32], then scales [MT][blocks]
+// laid out for MT rows: quants [MT][blocks][32] (on the tensor path with 16
+// bytes of padding per row, so its loads of 8 rows hit distinct banks), then
+// scales [MT][blocks]
+__host__ __device__ constexpr int act_row_bytes(int MT, int UB) {
+  return UB * 32 + (MT >= TC_MIN_MT ? 16 : 0);
+}
 __host__ __device__ constexpr int act_bytes(int MT, int P, int RU) {
-  return MT * P * RU * CHUNK_BLOCKS * 36;
+  return MT * act_row_bytes(MT, P * RU * CHUNK_BLOCKS) + MT * P * RU * CHUNK_BLOCKS * 4;
 }
 
 template <int R, int MT>
@@ -90,11 +108,19 @@ __host__ __device__ constexpr int ru_max() {
 }
 __host__ __device__ constexpr int log2_floor(int v) { return v <= 1 ? 0 : 1 + log2_floor(v >> 1); }
 
-// per-round exchange of chunk values between the parts of a row:
-// [2 buffers][P parts][R rows][MT]
+// row stride (floats) of the exchange buffer: odd on the tensor path, where
+// a thread's MT values would otherwise share banks with its neighbours'
+template <int MT>
+constexpr int red_stride() {
+  return MT >= TC_MIN_MT ? MT + 1 : MT;
+}
+
+// per-round exchange of chunk values between the parts of a row (and, on
+// the tensor path, from the MMA fragment layout to one thread per row):
+// [2 buffers][P parts][R rows][red_stride]
 template <int R, int MT>
 constexpr int red_bytes() {
-  return RCfg<R>::P > 1 ? 2 * 128 * MT * 4 : 0;
+  return (RCfg<R>::P > 1 || MT >= TC_MIN_MT) ? 2 * 128 * red_stride<MT>() * 4 : 0;
 }
 
 template <int R, int MT>
@@ -178,108 +204,113 @@ __device__ __forceinline__ void produce(const GemvArgs& a, uint8_t* stage_buf, u
 }
 
 // Staged activation blocks of a unit, in block order: quants of row m,
-// block blk at q + (m*UB + blk)*32, its scale (as float) at d[m*UB + blk],
-// UB = blocks per unit.
+// block blk at q + m*mq + blk*32 (mq = act_row_bytes), its scale (as float) at
+// d[m*UB + blk], UB = blocks per unit.
 struct ActLayout {
   uint8_t* q;
   float* d;
-  int UB;
+  int UB, mq;
 };
 
 __device__ __forceinline__ ActLayout act_layout(uint8_t* base, int MT, int UB) {
   ActLayout L;
   L.UB = UB;
+  L.mq = act_row_bytes(MT, UB);
   L.q = base;
-  L.d = reinterpret_cast<float*>(base + (size_t)MT * UB * 32);
+  L.d = reinterpret_cast<float*>(base + (size_t)MT * L.mq);
   return L;
 }
 
-// Stage the activation blocks [b0, b0 + nblk) of rows < M, one thread per
-// block.  With a cluster of CL CTAs that all need the same blocks, CTA c
-// stages every CL-th block (c, c+CL, ...) and writes it into the staging
-// area of every CTA of the cluster (distributed shared memory); the caller
-// then waits on the cluster barrier.  Loads of two blocks per thread are
-// issued before either is used.
-__device__ __forceinline__ void put_block(const ActLayout& L, int m, int blk, const uint32_t (&w)[8],
-                                          float d, uint32_t CL) {
-  uint8_t* dst = L.q + (m * L.UB + blk) * 32;
+// Stage the activation blocks [b0, b0 + nblk) of rows < M.  Eight
+// consecutive lanes take one block: lane s = threadIdx.x % 8 loads (and, on
+// the fused path, quantizes with its 7 neighbours) values 4s..4s+3 and stores
+// their 4 quants; lane 0 of the group stores the scale.  The blocks of all
+// rows form one sequence (row-major); with a cluster of CL CTAs that all need
+// the same blocks, CTA c takes every CL-th of them (c, c+CL, ...) and writes
+// each into the staging area of every CTA of the cluster (distributed shared
+// memory); the caller then waits on the cluster barrier.  A pass covers 16
+// blocks; BATCH passes have their loads in flight together.
+template <bool CLUSTER>
+__device__ __forceinline__ void put_word(const ActLayout& L, int m, int blk, int sub, uint32_t w,
+                                         float d, uint32_t CL) {
+  uint32_t* dst = reinterpret_cast<uint32_t*>(L.q + m * L.mq + blk * 32) + sub;
   float* dd = L.d + m * L.UB + blk;
-  if (CL == 1) {
-    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
-    *reinterpret_cast<uint4*>(dst + 16) = make_uint4(w[4], w[5], w[6], w[7]);
-    *dd = d;
+  if constexpr (!CLUSTER) {
+    *dst = w;
+    if (sub == 0) *dd = d;
   } else {
     const uint32_t q0 = smem_u32(dst), d0 = smem_u32(dd);
     for (uint32_t c = 0; c < CL; ++c) {
-      const uint32_t q = mapa_shared(q0, c);
-      st_cluster_v4(q, w[0], w[1], w[2], w[3]);
-      st_cluster_v4(q + 16, w[4], w[5], w[6], w[7]);
-      st_cluster_f32(mapa_shared(d0, c), d);
+      st_cluster_u32(mapa_shared(q0, c), w);
+      if (sub == 0) st_cluster_f32(mapa_shared(d0, c), d);
     }
   }
 }
 
-template <bool FUSED>
-__device__ __forceinline__ void stage_one(const GemvArgs& a, const ActLayout& L, int b0, int nblk,
-                                          int idx0, int idx1, bool h0, bool h1, uint32_t CL) {
-  const int64_t K = (int64_t)a.NB * QK;
-  const int m0 = h0 ? idx0 / nblk : 0, k0 = h0 ? idx0 - m0 * nblk : 0;
-  const int m1 = h1 ? idx1 / nblk : 0, k1 = h1 ? idx1 - m1 * nblk : 0;
-  if constexpr (FUSED) {
-    const float4* s0 = reinterpret_cast<const float4*>(a.x + (int64_t)m0 * K + (int64_t)(b0 + k0) * QK);
-    const float4* s1 = reinterpret_cast<const float4*>(a.x + (int64_t)m1 * K + (int64_t)(b0 + k1) * QK);
-    float4 v0[8], v1[8];
-    uint32_t w0[8], w1[8];
-    float d0, d1;
-    if (h1) {  // two blocks: both loads in flight, then both quantizations
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        v0[k] = __ldcg(s0 + k);
-        v1[k] = __ldcg(s1 + k);
-      }
-      quantize_block_thread(v0, w0, d0);
-      quantize_block_thread(v1, w1, d1);
-      put_block(L, m0, k0, w0, d0, CL);
-      put_block(L, m1, k1, w1, d1, CL);
-    } else if (h0) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) v0[k] = __ldcg(s0 + k);
-      quantize_block_thread(v0, w0, d0);
-      put_block(L, m0, k0, w0, d0, CL);
-    }
-  } else {
-    uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0, r0 = q0, r1 = q0;
-    uint16_t d0 = 0, d1 = 0;
-    const uint8_t* s0 = a.A + ((int64_t)m0 * a.NB + b0 + k0) * BLOCK_BYTES;
-    const uint8_t* s1 = a.A + ((int64_t)m1 * a.NB + b0 + k1) * BLOCK_BYTES;
-    if (h0) {
-      load_block_quants_u16(s0, q0, q1);
-      d0 = load_block_scale_bits(s0);
-    }
-    if (h1) {
-      load_block_quants_u16(s1, r0, r1);
-      d1 = load_block_scale_bits(s1);
-    }
-    if (h0) {
-      const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-      put_block(L, m0, k0, w, __half2float(__ushort_as_half(d0)), CL);
-    }
-    if (h1) {
-      const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-      put_block(L, m1, k1, w, __half2float(__ushort_as_half(d1)), CL);
-    }
-  }
-}
-
-template <bool FUSED, int NT>
+template <bool FUSED, bool CLUSTER, int NT, int BATCH>
 __device__ __forceinline__ void stage_activations(const GemvArgs& a, const ActLayout& L, int b0,
                                                   int nblk, uint32_t rank, uint32_t CL) {
+  constexpr int BPP = NT / 8;  // blocks per pass
+  const int64_t K = (int64_t)a.NB * QK;
   const int total = a.M * nblk;
   const int mine = (total - (int)rank + (int)CL - 1) / (int)CL;  // blocks rank, rank+CL, ...
-  for (int base = 0; base < mine; base += 2 * NT) {
-    const int j0 = base + threadIdx.x, j1 = j0 + NT;
-    stage_one<FUSED>(a, L, b0, nblk, j0 * (int)CL + (int)rank, j1 * (int)CL + (int)rank, j0 < mine,
-                     j1 < mine, CL);
+  const int sub = threadIdx.x & 7, slot = threadIdx.x >> 3;
+  const int step = BPP * (int)CL;  // sequence distance between passes
+  // trip counts are uniform across the CTA: the shuffles inside see full warps
+  for (int base = 0; base < mine; base += BPP * BATCH) {
+    // row and block of this thread's first block of the batch (one division
+    // per batch), then stepped forward pass by pass
+    int k = (base + slot) * (int)CL + (int)rank, m = 0;
+    if (a.M > 1) {
+      m = k / nblk;
+      k -= m * nblk;
+    }
+    int mm[BATCH], kk[BATCH];
+    bool on[BATCH];
+#pragma unroll
+    for (int q = 0; q < BATCH; ++q) {
+      on[q] = base + q * BPP + slot < mine;
+      mm[q] = m;
+      kk[q] = k;
+      k += step;
+      while (k >= nblk && m < a.M) {  // once per step when nblk >= step
+        k -= nblk;
+        ++m;
+      }
+    }
+    if constexpr (FUSED) {
+      float4 v[BATCH];
+#pragma unroll
+      for (int q = 0; q < BATCH; ++q)
+        v[q] = on[q] ? __ldcg(reinterpret_cast<const float4*>(a.x + (int64_t)mm[q] * K +
+                                                               (int64_t)(b0 + kk[q]) * QK) +
+                              sub)
+                     : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      uint32_t w[BATCH];
+      float d[BATCH];
+      quantize_group8<BATCH>(v, w, d);
+#pragma unroll
+      for (int q = 0; q < BATCH; ++q)
+        if (on[q]) put_word<CLUSTER>(L, mm[q], kk[q], sub, w[q], d[q], CL);
+    } else {
+      // a block is 34 bytes (2-byte aligned): the scale, then 32 quants
+      uint32_t w[BATCH];
+      unsigned short dbits[BATCH];
+#pragma unroll
+      for (int q = 0; q < BATCH; ++q) {
+        w[q] = 0u;
+        dbits[q] = 0;
+        if (on[q]) {
+          const unsigned short* blk = reinterpret_cast<const unsigned short*>(
+              a.A + ((int64_t)mm[q] * a.NB + b0 + kk[q]) * BLOCK_BYTES);
+          w[q] = (uint32_t)__ldcg(blk + 1 + 2 * sub) | ((uint32_t)__ldcg(blk + 2 + 2 * sub) << 16);
+          if (sub == 0) dbits[q] = __ldcg(blk);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < BATCH; ++q)
+        if (on[q]) put_word<CLUSTER>(L, mm[q], kk[q], sub, w[q], __half2float(__ushort_as_half(dbits[q])), CL);
+    }
   }
 }
 
@@ -294,7 +325,7 @@ __device__ __forceinline__ void write_act_blocks(const GemvArgs& a, const ActLay
     uint8_t* ob = a.A_out + ((int64_t)m * a.NB + b0 + blk) * BLOCK_BYTES;
     const float d = L.d[m * L.UB + blk];
     const uint16_t d16 = __half_as_ushort(__float2half_rn(d));  // exact: d came from binary16
-    const uint8_t* q = L.q + (m * L.UB + blk) * 32;
+    const uint8_t* q = L.q + m * L.mq + blk * 32;
     unsigned short* o16 = reinterpret_cast<unsigned short*>(ob);
     o16[0] = d16;
 #pragma unroll
@@ -369,6 +400,102 @@ __device__ __forceinline__ void chunk_value(const uint8_t* cq, int r, int kb, in
   for (int m = 0; m < MT; ++m) v[m] = tadd(q[0][m], q[1][m]);
 }
 
+// Tensor-core path: one warp computes a 16-row slice of one chunk against
+// MT activation rows.  Per block and 16-wide half of it, the int8 weights
+// and activations are converted exactly to fp16 and multiplied with
+// mma.sync m16n8k16 (fp32 accumulate; every partial sum is an integer below
+// 2^24, so the accumulator holds the exact int32 block dot).  Inside each
+// half the 16 k positions are permuted identically for A and B (thread tig
+// takes bytes 4tig..4tig+3 for its k pairs 2tig, 2tig+1 and 2tig+8,
+// 2tig+9), which leaves the dot unchanged and makes every fragment one
+// 32-bit shared-memory load.  Each block term is then rounded exactly as on
+// the DP4A path and the 8 terms are summed in the same pairwise tree.
+// out[nt][e]: rows row0 + g (e = 0, 1) and row0 + g + 8 (e = 2, 3), activation
+// rows 8nt + 2tig + (e & 1); g = lane / 4, tig = lane % 4.
+template <int MT>
+__device__ __forceinline__ void block_terms_mma(const uint8_t* cq, const uint8_t* sc, int r, int row0,
+                                                int j, const uint8_t* aq, const float* ad, int mq,
+                                                int md, float (&t)[MT / 8][4]) {
+  constexpr int NTL = MT / 8;
+  const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+  float acc[NTL][4];
+#pragma unroll
+  for (int nt = 0; nt < NTL; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t a[4];
+    i8x4_to_h2x2(lds32(cq + ((2 * j + h) * r + row0 + g) * 16 + 4 * tig), a[0], a[2]);
+    i8x4_to_h2x2(lds32(cq + ((2 * j + h) * r + row0 + g + 8) * 16 + 4 * tig), a[1], a[3]);
+#pragma unroll
+    for (int nt = 0; nt < NTL; ++nt) {
+      uint32_t b0, b1;
+      i8x4_to_h2x2(lds32(aq + (8 * nt + g) * mq + j * 32 + 16 * h + 4 * tig), b0, b1);
+      mma_16816(acc[nt], a, b0, b1);
+    }
+  }
+  const float dw0 =
+      __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(sc + (j * r + row0 + g) * 2)));
+  const float dw1 = __half2float(
+      __ushort_as_half(*reinterpret_cast<const unsigned short*>(sc + (j * r + row0 + g + 8) * 2)));
+#pragma unroll
+  for (int nt = 0; nt < NTL; ++nt) {
+    const float da0 = ad[(8 * nt + 2 * tig) * md + j], da1 = ad[(8 * nt + 2 * tig + 1) * md + j];
+    t[nt][0] = __fmul_rn(acc[nt][0], __fmul_rn(dw0, da0));
+    t[nt][1] = __fmul_rn(acc[nt][1], __fmul_rn(dw0, da1));
+    t[nt][2] = __fmul_rn(acc[nt][2], __fmul_rn(dw1, da0));
+    t[nt][3] = __fmul_rn(acc[nt][3], __fmul_rn(dw1, da1));
+  }
+}
+
+template <int MT>
+__device__ __forceinline__ void chunk_value_mma(const uint8_t* cq, int r, int kb, int row0,
+                                                const uint8_t* aq, const float* ad, int mq, int md,
+                                                float (&v)[MT / 8][4]) {
+  constexpr int NTL = MT / 8;
+  const uint8_t* sc = cq + kb * r * 32;
+  const bool full = (kb == CHUNK_BLOCKS);
+  float q[2][NTL][4];
+#pragma unroll
+  for (int h4 = 0; h4 < 2; ++h4) {
+    float p2[2][NTL][4];
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      float ta[NTL][4], tb[NTL][4];
+      const int j = 4 * h4 + 2 * h2;
+      if (full || j < kb) {
+        block_terms_mma<MT>(cq, sc, r, row0, j, aq, ad, mq, md, ta);
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < NTL; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) ta[nt][e] = 0.0f;
+      }
+      if (full || j + 1 < kb) {
+        block_terms_mma<MT>(cq, sc, r, row0, j + 1, aq, ad, mq, md, tb);
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < NTL; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) tb[nt][e] = 0.0f;
+      }
+#pragma unroll
+      for (int nt = 0; nt < NTL; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) p2[h2][nt][e] = tadd(ta[nt][e], tb[nt][e]);
+    }
+#pragma unroll
+    for (int nt = 0; nt < NTL; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) q[h4][nt][e] = tadd(p2[0][nt][e], p2[1][nt][e]);
+  }
+#pragma unroll
+  for (int nt = 0; nt < NTL; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[nt][e] = tadd(q[0][nt][e], q[1][nt][e]);
+}
+
 // pairwise tree of the P chunk values of a round (P a power of two)
 template <int P>
 __device__ __forceinline__ float tree_of(const float* w, int stride) {
@@ -386,11 +513,14 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
   constexpr int NT = NCW * 32;  // consumer threads
   constexpr int STAGES = MCfg<MT>::STAGES;
   constexpr int LV = log2_floor(ru_max<R, MT>()) + 1;
+  constexpr bool TC = MT >= TC_MIN_MT;  // tensor-core path
+  constexpr bool EXCHANGE = (P > 1) || TC;
+  constexpr int RS = red_stride<MT>();
   constexpr int BAR_CONSUMERS = 1;  // named barrier of the consumer warps
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stage_buf = smem;
   uint8_t* act_base = smem + (size_t)STAGES * RCfg<R>::STAGE_BYTES;
-  float* red = reinterpret_cast<float*>(act_base + MCfg<MT>::ACT_BUDGET);  // [2][P][R][MT]
+  float* red = reinterpret_cast<float*>(act_base + MCfg<MT>::ACT_BUDGET);  // [2][P][R][RS]
   uint64_t* full = reinterpret_cast<uint64_t*>(act_base + MCfg<MT>::ACT_BUDGET + red_bytes<R, MT>());
   uint64_t* empty = full + STAGES;
   volatile int* misc = reinterpret_cast<volatile int*>(empty + STAGES);
@@ -463,13 +593,13 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
     }
     if (s != staged_s) {  // units with the same K range reuse the staged blocks
       if (CL > 1) {        // once per CTA: the planner clusters only when S == 1
-        stage_activations<FUSED, NT>(a, L, b0, nblk, crank, CL);
+        stage_activations<FUSED, true, NT, MCfg<MT>::STAGE_BATCH>(a, L, b0, nblk, crank, CL);
         __syncwarp();
         cluster_arrive_aligned();
         cluster_wait_aligned();
       } else {
         named_bar_sync(BAR_CONSUMERS, NT);
-        stage_activations<FUSED, NT>(a, L, b0, nblk, 0u, 1u);
+        stage_activations<FUSED, false, NT, MCfg<MT>::STAGE_BATCH>(a, L, b0, nblk, 0u, 1u);
         named_bar_sync(BAR_CONSUMERS, NT);
       }
       staged_s = s;
@@ -492,30 +622,58 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
         atomicOr(a.err, ERR_CONSUMER_WAIT);
         misc[0] = 1;
       }
-      const int c = c0 + rho * P + p;
       float v[MT];
 #pragma unroll
       for (int m = 0; m < MT; ++m) v[m] = 0.0f;
-      if (got && c < a.nch) {
-        const int blk = (rho * P + p) * CHUNK_BLOCKS;  // first block of the chunk in the unit
-        chunk_value<MT>(stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES + p * (r * CHUNK_BLOCKS * BLOCK_BYTES),
-                        r, chunk_blocks(c, a.NB), i, L.q + blk * 32, L.d + blk, UB * 32, UB, v);
+      const int xpar = consumed & 1;
+      float* rb = red + (size_t)xpar * P * R * RS;  // [P][R][RS]
+      if constexpr (TC) {
+        // 8 slices (16 rows x one chunk) per round, two per warp
+        const int g = lane >> 2, tig = lane & 3;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int sl = warp + k * NCW;
+          const int ps = sl / (R / 16), row0 = (sl % (R / 16)) * 16;
+          const int c = c0 + rho * P + ps;
+          float cv[MT / 8][4];
+#pragma unroll
+          for (int nt = 0; nt < MT / 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) cv[nt][e] = 0.0f;
+          if (got && c < a.nch) {
+            const int blk = (rho * P + ps) * CHUNK_BLOCKS;
+            chunk_value_mma<MT>(stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES + ps * (r * CHUNK_BLOCKS * BLOCK_BYTES),
+                                r, chunk_blocks(c, a.NB), row0, L.q + blk * 32, L.d + blk, L.mq, UB, cv);
+          }
+#pragma unroll
+          for (int nt = 0; nt < MT / 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              rb[(ps * R + row0 + g + (e >> 1) * 8) * RS + 8 * nt + 2 * tig + (e & 1)] = cv[nt][e];
+        }
+      } else {
+        const int c = c0 + rho * P + p;
+        if (got && c < a.nch) {
+          const int blk = (rho * P + p) * CHUNK_BLOCKS;  // first block of the chunk in the unit
+          chunk_value<MT>(stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES + p * (r * CHUNK_BLOCKS * BLOCK_BYTES),
+                          r, chunk_blocks(c, a.NB), i, L.q + blk * 32, L.d + blk, L.mq, UB, v);
+        }
+        if constexpr (EXCHANGE) {
+#pragma unroll
+          for (int m = 0; m < MT; ++m) rb[(p * R + i) * RS + m] = v[m];
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[stage]);
-      const int xpar = consumed & 1;
       ++consumed;
       if (++stage == STAGES) {
         stage = 0;
         phase ^= 1u;
       }
-      if constexpr (P > 1) {
+      if constexpr (EXCHANGE) {
         // the P chunk values of row i meet in shared memory; the buffer
         // written in round k was last read in round k-2, before the barrier
         // of round k-1 that every writer has passed
-        float* rb = red + (size_t)xpar * P * R * MT;
-#pragma unroll
-        for (int m = 0; m < MT; ++m) rb[(p * R + i) * MT + m] = v[m];
         named_bar_sync(BAR_CONSUMERS, NT);
         if (misc[0]) {
           ok = false;
@@ -523,7 +681,7 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
         }
         if (p != 0) continue;
 #pragma unroll
-        for (int m = 0; m < MT; ++m) v[m] = tree_of<P>(rb + i * MT + m, R * MT);
+        for (int m = 0; m < MT; ++m) v[m] = tree_of<P>(rb + i * RS + m, R * RS);
       } else {
         if (!got || misc[0]) {
           ok = false;
