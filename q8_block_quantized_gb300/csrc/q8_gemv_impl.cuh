@@ -364,12 +364,13 @@ __device__ __forceinline__ void block_terms(const uint8_t* cq, const uint8_t* sc
 // chunk's first activation block; mq/md are the strides between activation
 // rows.  Rows m >= M are computed on whatever the staging area holds and
 // never stored.
-template <int MT>
+template <int MT, bool FULL>
 __device__ __forceinline__ void chunk_value(const uint8_t* cq, int r, int kb, int i,
                                             const uint8_t* aq, const float* ad, int mq, int md,
                                             float (&v)[MT]) {
+  if constexpr (FULL) kb = CHUNK_BLOCKS;
   const uint8_t* sc = cq + kb * r * 32;
-  const bool full = (kb == CHUNK_BLOCKS);
+  constexpr bool full = FULL;
   float q[2][MT];
 #pragma unroll
   for (int h4 = 0; h4 < 2; ++h4) {
@@ -449,13 +450,14 @@ __device__ __forceinline__ void block_terms_mma(const uint8_t* cq, const uint8_t
   }
 }
 
-template <int MT>
+template <int MT, bool FULL>
 __device__ __forceinline__ void chunk_value_mma(const uint8_t* cq, int r, int kb, int row0,
                                                 const uint8_t* aq, const float* ad, int mq, int md,
                                                 float (&v)[MT / 8][4]) {
   constexpr int NTL = MT / 8;
+  if constexpr (FULL) kb = CHUNK_BLOCKS;
   const uint8_t* sc = cq + kb * r * 32;
-  const bool full = (kb == CHUNK_BLOCKS);
+  constexpr bool full = FULL;
   float q[2][NTL][4];
 #pragma unroll
   for (int h4 = 0; h4 < 2; ++h4) {
@@ -642,8 +644,13 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
             for (int e = 0; e < 4; ++e) cv[nt][e] = 0.0f;
           if (got && c < a.nch) {
             const int blk = (rho * P + ps) * CHUNK_BLOCKS;
-            chunk_value_mma<MT>(stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES + ps * (r * CHUNK_BLOCKS * BLOCK_BYTES),
-                                r, chunk_blocks(c, a.NB), row0, L.q + blk * 32, L.d + blk, L.mq, UB, cv);
+            const uint8_t* cq = stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES + ps * (r * CHUNK_BLOCKS * BLOCK_BYTES);
+            const int kb = chunk_blocks(c, a.NB);
+            // full chunks take straight-line code (no per-block guards)
+            if (kb == CHUNK_BLOCKS)
+              chunk_value_mma<MT, true>(cq, r, kb, row0, L.q + blk * 32, L.d + blk, L.mq, UB, cv);
+            else
+              chunk_value_mma<MT, false>(cq, r, kb, row0, L.q + blk * 32, L.d + blk, L.mq, UB, cv);
           }
 #pragma unroll
           for (int nt = 0; nt < MT / 8; ++nt)
@@ -655,8 +662,13 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
         const int c = c0 + rho * P + p;
         if (got && c < a.nch) {
           const int blk = (rho * P + p) * CHUNK_BLOCKS;  // first block of the chunk in the unit
-          chunk_value<MT>(stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES + p * (r * CHUNK_BLOCKS * BLOCK_BYTES),
-                          r, chunk_blocks(c, a.NB), i, L.q + blk * 32, L.d + blk, L.mq, UB, v);
+          const uint8_t* cq = stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES + p * (r * CHUNK_BLOCKS * BLOCK_BYTES);
+          const int kb = chunk_blocks(c, a.NB);
+          // full chunks take straight-line code (no per-block guards)
+          if (kb == CHUNK_BLOCKS)
+            chunk_value<MT, true>(cq, r, kb, i, L.q + blk * 32, L.d + blk, L.mq, UB, v);
+          else
+            chunk_value<MT, false>(cq, r, kb, i, L.q + blk * 32, L.d + blk, L.mq, UB, v);
         }
         if constexpr (EXCHANGE) {
 #pragma unroll
