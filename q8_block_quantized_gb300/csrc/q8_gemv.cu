@@ -71,7 +71,13 @@ bool cluster_fits(int R, int MT, bool fused, int c) {
 
 int mt_of(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
 int budget_of(int MT) {
-  return MT == 1 ? MCfg<1>::ACT_BUDGET : MT == 2 ? MCfg<2>::ACT_BUDGET : MCfg<16>::ACT_BUDGET;
+  switch (MT) {
+    case 1: return MCfg<1>::ACT_BUDGET;
+    case 2: return MCfg<2>::ACT_BUDGET;
+    case 4: return MCfg<4>::ACT_BUDGET;
+    case 8: return MCfg<8>::ACT_BUDGET;
+    default: return MCfg<16>::ACT_BUDGET;
+  }
 }
 
 }  // namespace
@@ -176,9 +182,9 @@ cudaError_t launch_gemv(const GemvPlan& p, const uint8_t* W, const uint8_t* A, c
     args.RU = p.RU;
     args.S = p.S;
     args.units = p.units;
-    // A last pass with fewer rows (M > 16) may use a smaller MT.  MT 4 and 8
-    // have the same activation budget as 16, so the plan's unit fits them;
-    // MT 1 and 2 have a smaller budget, so such a pass runs with MT 4.
+    // A last pass with fewer rows (M > 16) may use a smaller MT.  A unit
+    // sized for 16 rows fits MT 4 and 8 (fewer rows, no smaller budget per
+    // row); MT 1 and 2 have a smaller budget, so such a pass runs with MT 4.
     int MT = p.MT;
     if (Mp < 16 && p.MT == 16) {
       MT = mt_of(Mp);

@@ -76,14 +76,15 @@ template <int MT>
 struct MCfg {
   static constexpr int NCW = 4;                       // consumer warps: 128 threads
   static constexpr int THREADS = (NCW + 1) * 32;      // + the producer warp
-  static constexpr int STAGES = MT <= 2 ? 3 : 2;
+  static constexpr int STAGES = MT == 1 ? 3 : 2;
   // activation staging: passes of 16 blocks (8 lanes per block), STAGE_BATCH
   // passes with their loads in flight together (larger batches measured
   // slower for every row count)
   static constexpr int STAGE_BATCH = 4;
-  // bytes of staged activations; for MT <= 2 the whole shared-memory use
-  // stays below half an SM's, so two CTAs (of consecutive kernels) fit
-  static constexpr int ACT_BUDGET = MT == 1 ? 9216 : MT == 2 ? 9088 : 40960;
+  // bytes of staged activations: 256 blocks (K = 8192 in one unit) for
+  // MT <= 4, and for those the whole shared-memory use stays below half an
+  // SM's, so two CTAs (of consecutive kernels) fit
+  static constexpr int ACT_BUDGET = MT == 1 ? 9216 : MT == 2 ? 18432 : MT == 4 ? 36864 : 40960;
 };
 
 // Activation rows at or above this use the tensor-core path.
