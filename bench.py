@@ -273,6 +273,49 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemv_traffic_llama1b_m1.json")
+
+
+def kernel_sources_sha256():
+    """Hash of the GEMV library's sources (kernels, host code, header): DRAM
+    traffic measured by ncu is reported only for the sources it was measured
+    on."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "q8_block_quantized_gb300", "csrc")
+    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc)
+                   if f.endswith((".cu", ".cuh", ".h")))
+    files.append(os.path.join(ROOT, "include", "q8.h"))
+    for fn in files:
+        h.update(os.path.basename(fn).encode())
+        with open(fn, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(key, calls, M, fused):
+    """Mean dram__bytes_read + dram__bytes_write per launch of the dominant
+    class's calls, from the committed ncu capture; None if that capture was
+    taken on other sources, another configuration, or lacks one of the
+    shapes."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("sources_sha256") != kernel_sources_sha256() or d.get("M") != M or \
+            d.get("fused") != fused:
+        return None
+    per = d.get("dram_bytes_per_launch", {})
+    vals = []
+    for c in calls:
+        v = per.get("%s|%dx%d" % (key, c.N, c.K))
+        if v is None:
+            return None
+        vals.append(float(v))
+    return int(sum(vals) / len(vals)) if vals else None
+
+
 def kernel_class(q8, c, M):
     """The GEMV kernel instantiation a call runs: packed tile height, rows per
     pass, fused or not (the names ncu shows as gemv_kernel<R, MT, fused>)."""
@@ -329,18 +372,19 @@ def roofline(st, q8, reps=3):
             best = ms if best is None else min(best, ms)
         nbytes = sum(c.W.numel() + 4 * c.x.numel() + 4 * c.y.numel() if c.kind == "fused"
                      else c.W.numel() + c.A.numel() + 4 * c.y.numel() for c in calls)
-        rows.append((best, key, nbytes, len(calls)))
+        rows.append((best, key, nbytes, len(calls), calls))
         del g
-    rows.sort(reverse=True)
-    ms, key, nbytes, n = rows[0]
+    rows.sort(key=lambda r: r[0], reverse=True)
+    ms, key, nbytes, n, dom_calls = rows[0]
+    traffic = measured_traffic(key, dom_calls, st.M, st.mode == "fused")
     peak, kind = _peaks()
     achieved = nbytes / (ms * 1e-3) / 1e9
     return {"bound": "hbm", "kernel": key, "achieved": round(achieved, 1), "peak": peak,
             "peak_kind": kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "traffic": None, "launches_per_step": n,
+            "traffic": traffic, "launches_per_step": n,
             "bytes_per_launch_avg": int(nbytes / n), "us_per_launch_avg": round(ms * 1e3 / n, 3),
             "classes": {k: {"launches": nn, "us": round(t * 1e3, 2), "GB/s": round(b / (t * 1e-3) / 1e9, 1)}
-                        for t, k, b, nn in rows}}
+                        for t, k, b, nn, _ in rows}}
 
 
 # ---------------------------------------------------------------------------
