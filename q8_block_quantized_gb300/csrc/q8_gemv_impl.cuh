@@ -363,15 +363,16 @@ __device__ __forceinline__ void block_terms(const uint8_t* cq, const uint8_t* sc
 // One chunk (kb <= 8 blocks; blocks at or past kb count as zero) of row i:
 // the pairwise tree of its blocks, per activation row.  aq/ad point at the
 // chunk's first activation block; mq/md are the strides between activation
-// rows.  Rows m >= M are computed on whatever the staging area holds and
-// never stored.
-template <int MT, bool FULL>
+// rows.  All 8 blocks are computed in straight-line code and the terms of
+// blocks past kb are replaced by zero (their reads stay inside the stage and
+// staging buffers, whatever they hold), so partial chunks need no second copy
+// of the code.  Rows m >= M are computed on whatever the staging area holds
+// and never stored.
+template <int MT>
 __device__ __forceinline__ void chunk_value(const uint8_t* cq, int r, int kb, int i,
                                             const uint8_t* aq, const float* ad, int mq, int md,
                                             float (&v)[MT]) {
-  if constexpr (FULL) kb = CHUNK_BLOCKS;
   const uint8_t* sc = cq + kb * r * 32;
-  constexpr bool full = FULL;
   float q[2][MT];
 #pragma unroll
   for (int h4 = 0; h4 < 2; ++h4) {
@@ -380,20 +381,14 @@ __device__ __forceinline__ void chunk_value(const uint8_t* cq, int r, int kb, in
     for (int h2 = 0; h2 < 2; ++h2) {
       float ta[MT], tb[MT];
       const int j = 4 * h4 + 2 * h2;
-      if (full || j < kb) {
-        block_terms<MT>(cq, sc, r, i, j, aq, ad, mq, md, ta);
-      } else {
+      block_terms<MT>(cq, sc, r, i, j, aq, ad, mq, md, ta);
+      block_terms<MT>(cq, sc, r, i, j + 1, aq, ad, mq, md, tb);
 #pragma unroll
-        for (int m = 0; m < MT; ++m) ta[m] = 0.0f;
+      for (int m = 0; m < MT; ++m) {
+        ta[m] = (j < kb) ? ta[m] : 0.0f;
+        tb[m] = (j + 1 < kb) ? tb[m] : 0.0f;
+        (h2 ? p1 : p0)[m] = tadd(ta[m], tb[m]);
       }
-      if (full || j + 1 < kb) {
-        block_terms<MT>(cq, sc, r, i, j + 1, aq, ad, mq, md, tb);
-      } else {
-#pragma unroll
-        for (int m = 0; m < MT; ++m) tb[m] = 0.0f;
-      }
-#pragma unroll
-      for (int m = 0; m < MT; ++m) (h2 ? p1 : p0)[m] = tadd(ta[m], tb[m]);
     }
 #pragma unroll
     for (int m = 0; m < MT; ++m) q[h4][m] = tadd(p0[m], p1[m]);
@@ -451,14 +446,12 @@ __device__ __forceinline__ void block_terms_mma(const uint8_t* cq, const uint8_t
   }
 }
 
-template <int MT, bool FULL>
+template <int MT>
 __device__ __forceinline__ void chunk_value_mma(const uint8_t* cq, int r, int kb, int row0,
                                                 const uint8_t* aq, const float* ad, int mq, int md,
                                                 float (&v)[MT / 8][4]) {
   constexpr int NTL = MT / 8;
-  if constexpr (FULL) kb = CHUNK_BLOCKS;
   const uint8_t* sc = cq + kb * r * 32;
-  constexpr bool full = FULL;
   float q[2][NTL][4];
 #pragma unroll
   for (int h4 = 0; h4 < 2; ++h4) {
@@ -467,26 +460,17 @@ __device__ __forceinline__ void chunk_value_mma(const uint8_t* cq, int r, int kb
     for (int h2 = 0; h2 < 2; ++h2) {
       float ta[NTL][4], tb[NTL][4];
       const int j = 4 * h4 + 2 * h2;
-      if (full || j < kb) {
-        block_terms_mma<MT>(cq, sc, r, row0, j, aq, ad, mq, md, ta);
-      } else {
-#pragma unroll
-        for (int nt = 0; nt < NTL; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) ta[nt][e] = 0.0f;
-      }
-      if (full || j + 1 < kb) {
-        block_terms_mma<MT>(cq, sc, r, row0, j + 1, aq, ad, mq, md, tb);
-      } else {
-#pragma unroll
-        for (int nt = 0; nt < NTL; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) tb[nt][e] = 0.0f;
-      }
+      // straight-line over all 8 blocks; blocks past kb count as zero
+      block_terms_mma<MT>(cq, sc, r, row0, j, aq, ad, mq, md, ta);
+      block_terms_mma<MT>(cq, sc, r, row0, j + 1, aq, ad, mq, md, tb);
 #pragma unroll
       for (int nt = 0; nt < NTL; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) p2[h2][nt][e] = tadd(ta[nt][e], tb[nt][e]);
+        for (int e = 0; e < 4; ++e) {
+          ta[nt][e] = (j < kb) ? ta[nt][e] : 0.0f;
+          tb[nt][e] = (j + 1 < kb) ? tb[nt][e] : 0.0f;
+          p2[h2][nt][e] = tadd(ta[nt][e], tb[nt][e]);
+        }
     }
 #pragma unroll
     for (int nt = 0; nt < NTL; ++nt)
@@ -631,9 +615,10 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
       const int xpar = consumed & 1;
       float* rb = red + (size_t)xpar * P * R * RS;  // [P][R][RS]
       if constexpr (TC) {
-        // 8 slices (16 rows x one chunk) per round, two per warp
+        // 8 slices (16 rows x one chunk) per round, two per warp (a loop, not
+        // unrolled: one copy of the slice code keeps the instruction cache warm)
         const int g = lane >> 2, tig = lane & 3;
-#pragma unroll
+#pragma unroll 1
         for (int k = 0; k < 2; ++k) {
           const int sl = warp + k * NCW;
           const int ps = sl / (R / 16), row0 = (sl % (R / 16)) * 16;
@@ -646,12 +631,7 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
           if (got && c < a.nch) {
             const int blk = (rho * P + ps) * CHUNK_BLOCKS;
             const uint8_t* cq = stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES + ps * (r * CHUNK_BLOCKS * BLOCK_BYTES);
-            const int kb = chunk_blocks(c, a.NB);
-            // full chunks take straight-line code (no per-block guards)
-            if (kb == CHUNK_BLOCKS)
-              chunk_value_mma<MT, true>(cq, r, kb, row0, L.q + blk * 32, L.d + blk, L.mq, UB, cv);
-            else
-              chunk_value_mma<MT, false>(cq, r, kb, row0, L.q + blk * 32, L.d + blk, L.mq, UB, cv);
+            chunk_value_mma<MT>(cq, r, chunk_blocks(c, a.NB), row0, L.q + blk * 32, L.d + blk, L.mq, UB, cv);
           }
 #pragma unroll
           for (int nt = 0; nt < MT / 8; ++nt)
@@ -664,12 +644,7 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
         if (got && c < a.nch) {
           const int blk = (rho * P + p) * CHUNK_BLOCKS;  // first block of the chunk in the unit
           const uint8_t* cq = stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES + p * (r * CHUNK_BLOCKS * BLOCK_BYTES);
-          const int kb = chunk_blocks(c, a.NB);
-          // full chunks take straight-line code (no per-block guards)
-          if (kb == CHUNK_BLOCKS)
-            chunk_value<MT, true>(cq, r, kb, i, L.q + blk * 32, L.d + blk, L.mq, UB, v);
-          else
-            chunk_value<MT, false>(cq, r, kb, i, L.q + blk * 32, L.d + blk, L.mq, UB, v);
+          chunk_value<MT>(cq, r, chunk_blocks(c, a.NB), i, L.q + blk * 32, L.d + blk, L.mq, UB, v);
         }
         if constexpr (EXCHANGE) {
 #pragma unroll
