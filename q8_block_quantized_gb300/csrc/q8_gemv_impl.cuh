@@ -8,7 +8,10 @@
 // 128 consumer threads of a CTA are P = 128/R parts x R rows: thread t owns
 // row i = t % R and part p = t / R.  A pipeline round is P consecutive chunks
 // of one tile (one contiguous bulk copy of up to 34,816 bytes); part p
-// computes chunk p of the round for its row.  A work unit is one tile times
+// computes chunk p of the round for its row.  For one activation row the CTA
+// has 256 consumer threads and each (row, part) pair is split in two halves
+// of 4 blocks (t / 128 picks the half), which halves a round's latency; the
+// halves' values meet in the exchange like the parts'.  A work unit is one tile times
 // RU consecutive rounds; usually a unit covers all of K and a tile is one
 // unit.
 //
@@ -74,9 +77,15 @@ struct RCfg {
 
 template <int MT>
 struct MCfg {
-  static constexpr int NCW = 4;                       // consumer warps: 128 threads
+  // consumer warps: 8 for one activation row (each thread then takes half a
+  // chunk, 4 blocks, which halves the latency of a round), else 4
+  static constexpr int NCW = MT == 1 ? 8 : 4;
+  static constexpr int HALVES = NCW * 32 / 128;       // threads per (row, chunk)
   static constexpr int THREADS = (NCW + 1) * 32;      // + the producer warp
   static constexpr int STAGES = MT == 1 ? 3 : 2;
+  // CTAs per SM the kernel is compiled for: the 288-thread kernel for one
+  // row must keep two CTAs per SM (registers included)
+  static constexpr int MIN_CTAS = MT == 1 ? 2 : 1;
   // activation staging: passes of 16 blocks (8 lanes per block), STAGE_BATCH
   // passes with their loads in flight together (larger batches measured
   // slower for every row count)
@@ -84,7 +93,7 @@ struct MCfg {
   // bytes of staged activations: 256 blocks (K = 8192 in one unit) for
   // MT <= 4, and for those the whole shared-memory use stays below half an
   // SM's, so two CTAs (of consecutive kernels) fit
-  static constexpr int ACT_BUDGET = MT == 1 ? 9216 : MT == 2 ? 18432 : MT == 4 ? 36864 : 40960;
+  static constexpr int ACT_BUDGET = MT == 1 ? 8704 : MT == 2 ? 17408 : MT == 4 ? 34816 : 40960;
 };
 
 // Activation rows at or above this use the tensor-core path.
@@ -98,7 +107,7 @@ __host__ __device__ constexpr int act_row_bytes(int MT, int UB) {
   return UB * 32 + (MT >= TC_MIN_MT ? 16 : 0);
 }
 __host__ __device__ constexpr int act_bytes(int MT, int P, int RU) {
-  return MT * act_row_bytes(MT, P * RU * CHUNK_BLOCKS) + MT * P * RU * CHUNK_BLOCKS * 4;
+  return MT * act_row_bytes(MT, P * RU * CHUNK_BLOCKS) + MT * P * RU * CHUNK_BLOCKS * 2;
 }
 
 template <int R, int MT>
@@ -121,7 +130,9 @@ constexpr int red_stride() {
 // [2 buffers][P parts][R rows][red_stride]
 template <int R, int MT>
 constexpr int red_bytes() {
-  return (RCfg<R>::P > 1 || MT >= TC_MIN_MT) ? 2 * 128 * red_stride<MT>() * 4 : 0;
+  return (RCfg<R>::P > 1 || MT >= TC_MIN_MT || MCfg<MT>::HALVES > 1)
+             ? 2 * MCfg<MT>::HALVES * 128 * red_stride<MT>() * 4
+             : 0;
 }
 
 template <int R, int MT>
@@ -205,11 +216,11 @@ __device__ __forceinline__ void produce(const GemvArgs& a, uint8_t* stage_buf, u
 }
 
 // Staged activation blocks of a unit, in block order: quants of row m,
-// block blk at q + m*mq + blk*32 (mq = act_row_bytes), its scale (as float) at
+// block blk at q + m*mq + blk*32 (mq = act_row_bytes), its binary16 scale at
 // d[m*UB + blk], UB = blocks per unit.
 struct ActLayout {
   uint8_t* q;
-  float* d;
+  __half* d;
   int UB, mq;
 };
 
@@ -218,7 +229,7 @@ __device__ __forceinline__ ActLayout act_layout(uint8_t* base, int MT, int UB) {
   L.UB = UB;
   L.mq = act_row_bytes(MT, UB);
   L.q = base;
-  L.d = reinterpret_cast<float*>(base + (size_t)MT * L.mq);
+  L.d = reinterpret_cast<__half*>(base + (size_t)MT * L.mq);
   return L;
 }
 
@@ -233,9 +244,9 @@ __device__ __forceinline__ ActLayout act_layout(uint8_t* base, int MT, int UB) {
 // blocks; BATCH passes have their loads in flight together.
 template <bool CLUSTER>
 __device__ __forceinline__ void put_word(const ActLayout& L, int m, int blk, int sub, uint32_t w,
-                                         float d, uint32_t CL) {
+                                         __half d, uint32_t CL) {
   uint32_t* dst = reinterpret_cast<uint32_t*>(L.q + m * L.mq + blk * 32) + sub;
-  float* dd = L.d + m * L.UB + blk;
+  __half* dd = L.d + m * L.UB + blk;
   if constexpr (!CLUSTER) {
     *dst = w;
     if (sub == 0) *dd = d;
@@ -243,7 +254,7 @@ __device__ __forceinline__ void put_word(const ActLayout& L, int m, int blk, int
     const uint32_t q0 = smem_u32(dst), d0 = smem_u32(dd);
     for (uint32_t c = 0; c < CL; ++c) {
       st_cluster_u32(mapa_shared(q0, c), w);
-      if (sub == 0) st_cluster_f32(mapa_shared(d0, c), d);
+      if (sub == 0) st_cluster_u16(mapa_shared(d0, c), __half_as_ushort(d));
     }
   }
 }
@@ -292,7 +303,7 @@ __device__ __forceinline__ void stage_activations(const GemvArgs& a, const ActLa
       quantize_group8<BATCH>(v, w, d);
 #pragma unroll
       for (int q = 0; q < BATCH; ++q)
-        if (on[q]) put_word<CLUSTER>(L, mm[q], kk[q], sub, w[q], d[q], CL);
+        if (on[q]) put_word<CLUSTER>(L, mm[q], kk[q], sub, w[q], __float2half_rn(d[q]), CL);  // exact
     } else {
       // a block is 34 bytes (2-byte aligned): the scale, then 32 quants
       uint32_t w[BATCH];
@@ -310,7 +321,7 @@ __device__ __forceinline__ void stage_activations(const GemvArgs& a, const ActLa
       }
 #pragma unroll
       for (int q = 0; q < BATCH; ++q)
-        if (on[q]) put_word<CLUSTER>(L, mm[q], kk[q], sub, w[q], __half2float(__ushort_as_half(dbits[q])), CL);
+        if (on[q]) put_word<CLUSTER>(L, mm[q], kk[q], sub, w[q], __ushort_as_half(dbits[q]), CL);
     }
   }
 }
@@ -324,8 +335,7 @@ __device__ __forceinline__ void write_act_blocks(const GemvArgs& a, const ActLay
   for (int idx = threadIdx.x; idx < total; idx += NT) {
     const int m = idx / nblk, blk = idx - m * nblk;
     uint8_t* ob = a.A_out + ((int64_t)m * a.NB + b0 + blk) * BLOCK_BYTES;
-    const float d = L.d[m * L.UB + blk];
-    const uint16_t d16 = __half_as_ushort(__float2half_rn(d));  // exact: d came from binary16
+    const uint16_t d16 = __half_as_ushort(L.d[m * L.UB + blk]);
     const uint8_t* q = L.q + m * L.mq + blk * 32;
     unsigned short* o16 = reinterpret_cast<unsigned short*>(ob);
     o16[0] = d16;
@@ -338,7 +348,7 @@ __device__ __forceinline__ void write_act_blocks(const GemvArgs& a, const ActLay
 // Two independent dp4a chains per block keep the dependent latency short.
 template <int MT>
 __device__ __forceinline__ void block_terms(const uint8_t* cq, const uint8_t* sc, int r, int i,
-                                            int j, const uint8_t* aq, const float* ad, int mq,
+                                            int j, const uint8_t* aq, const __half* ad, int mq,
                                             int md, float (&out)[MT]) {
   const uint4 w0 = lds128(cq + ((2 * j) * r + i) * 16);
   const uint4 w1 = lds128(cq + ((2 * j + 1) * r + i) * 16);
@@ -356,7 +366,7 @@ __device__ __forceinline__ void block_terms(const uint8_t* cq, const uint8_t* sc
     s1 = __dp4a((int)w1.z, (int)a1.z, s1);
     s0 = __dp4a((int)w0.w, (int)a0.w, s0);
     s1 = __dp4a((int)w1.w, (int)a1.w, s1);
-    out[m] = block_term(s0 + s1, dw, ad[m * md + j]);  // integer sum: exact
+    out[m] = block_term(s0 + s1, dw, __half2float(ad[m * md + j]));  // integer sum: exact
   }
 }
 
@@ -370,7 +380,7 @@ __device__ __forceinline__ void block_terms(const uint8_t* cq, const uint8_t* sc
 // and never stored.
 template <int MT>
 __device__ __forceinline__ void chunk_value(const uint8_t* cq, int r, int kb, int i,
-                                            const uint8_t* aq, const float* ad, int mq, int md,
+                                            const uint8_t* aq, const __half* ad, int mq, int md,
                                             float (&v)[MT]) {
   const uint8_t* sc = cq + kb * r * 32;
   float q[2][MT];
@@ -397,6 +407,32 @@ __device__ __forceinline__ void chunk_value(const uint8_t* cq, int r, int kb, in
   for (int m = 0; m < MT; ++m) v[m] = tadd(q[0][m], q[1][m]);
 }
 
+// Half a chunk: the 4-block subtree of blocks j0..j0+3 (j0 = 0 or 4), the
+// same straight-line code and masking as chunk_value; the two halves' values
+// merge into the chunk value (the top node of the 8-block tree).
+template <int MT>
+__device__ __forceinline__ void chunk_value_half(const uint8_t* cq, int r, int kb, int i, int j0,
+                                                 const uint8_t* aq, const __half* ad, int mq, int md,
+                                                 float (&v)[MT]) {
+  const uint8_t* sc = cq + kb * r * 32;
+  float pp[2][MT];
+#pragma unroll
+  for (int h2 = 0; h2 < 2; ++h2) {
+    float ta[MT], tb[MT];
+    const int j = j0 + 2 * h2;
+    block_terms<MT>(cq, sc, r, i, j, aq, ad, mq, md, ta);
+    block_terms<MT>(cq, sc, r, i, j + 1, aq, ad, mq, md, tb);
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+      ta[m] = (j < kb) ? ta[m] : 0.0f;
+      tb[m] = (j + 1 < kb) ? tb[m] : 0.0f;
+      pp[h2][m] = tadd(ta[m], tb[m]);
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < MT; ++m) v[m] = tadd(pp[0][m], pp[1][m]);
+}
+
 // Tensor-core path: one warp computes a 16-row slice of one chunk against
 // MT activation rows.  Per block and 16-wide half of it, the int8 weights
 // and activations are converted exactly to fp16 and multiplied with
@@ -411,7 +447,7 @@ __device__ __forceinline__ void chunk_value(const uint8_t* cq, int r, int kb, in
 // rows 8nt + 2tig + (e & 1); g = lane / 4, tig = lane % 4.
 template <int MT>
 __device__ __forceinline__ void block_terms_mma(const uint8_t* cq, const uint8_t* sc, int r, int row0,
-                                                int j, const uint8_t* aq, const float* ad, int mq,
+                                                int j, const uint8_t* aq, const __half* ad, int mq,
                                                 int md, float (&t)[MT / 8][4]) {
   constexpr int NTL = MT / 8;
   const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
@@ -438,7 +474,8 @@ __device__ __forceinline__ void block_terms_mma(const uint8_t* cq, const uint8_t
       __ushort_as_half(*reinterpret_cast<const unsigned short*>(sc + (j * r + row0 + g + 8) * 2)));
 #pragma unroll
   for (int nt = 0; nt < NTL; ++nt) {
-    const float da0 = ad[(8 * nt + 2 * tig) * md + j], da1 = ad[(8 * nt + 2 * tig + 1) * md + j];
+    const float da0 = __half2float(ad[(8 * nt + 2 * tig) * md + j]);
+    const float da1 = __half2float(ad[(8 * nt + 2 * tig + 1) * md + j]);
     t[nt][0] = __fmul_rn(acc[nt][0], __fmul_rn(dw0, da0));
     t[nt][1] = __fmul_rn(acc[nt][1], __fmul_rn(dw0, da1));
     t[nt][2] = __fmul_rn(acc[nt][2], __fmul_rn(dw1, da0));
@@ -448,7 +485,7 @@ __device__ __forceinline__ void block_terms_mma(const uint8_t* cq, const uint8_t
 
 template <int MT>
 __device__ __forceinline__ void chunk_value_mma(const uint8_t* cq, int r, int kb, int row0,
-                                                const uint8_t* aq, const float* ad, int mq, int md,
+                                                const uint8_t* aq, const __half* ad, int mq, int md,
                                                 float (&v)[MT / 8][4]) {
   constexpr int NTL = MT / 8;
   const uint8_t* sc = cq + kb * r * 32;
@@ -483,31 +520,35 @@ __device__ __forceinline__ void chunk_value_mma(const uint8_t* cq, int r, int kb
     for (int e = 0; e < 4; ++e) v[nt][e] = tadd(q[0][nt][e], q[1][nt][e]);
 }
 
-// pairwise tree of the P chunk values of a round (P a power of two)
-template <int P>
-__device__ __forceinline__ float tree_of(const float* w, int stride) {
+// pairwise tree of the P chunk values of a round (P a power of two); with
+// H = 2 halves per chunk, a chunk's value is first the sum of its halves'
+// (stored hstride apart)
+template <int P, int H>
+__device__ __forceinline__ float tree_of(const float* w, int stride, int hstride) {
   if constexpr (P == 1) {
-    return w[0];
+    return H == 2 ? tadd(w[0], w[hstride]) : w[0];
   } else {
-    return tadd(tree_of<P / 2>(w, stride), tree_of<P / 2>(w + (P / 2) * stride, stride));
+    return tadd(tree_of<P / 2, H>(w, stride, hstride),
+                tree_of<P / 2, H>(w + (P / 2) * stride, stride, hstride));
   }
 }
 
 template <int R, int MT, bool FUSED>
-__global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_kernel(const GemvArgs a) {
   constexpr int P = RCfg<R>::P;
   constexpr int NCW = MCfg<MT>::NCW;
   constexpr int NT = NCW * 32;  // consumer threads
   constexpr int STAGES = MCfg<MT>::STAGES;
   constexpr int LV = log2_floor(ru_max<R, MT>()) + 1;
   constexpr bool TC = MT >= TC_MIN_MT;  // tensor-core path
-  constexpr bool EXCHANGE = (P > 1) || TC;
+  constexpr int HALVES = MCfg<MT>::HALVES;
+  constexpr bool EXCHANGE = (P > 1) || TC || (HALVES > 1);
   constexpr int RS = red_stride<MT>();
   constexpr int BAR_CONSUMERS = 1;  // named barrier of the consumer warps
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stage_buf = smem;
   uint8_t* act_base = smem + (size_t)STAGES * RCfg<R>::STAGE_BYTES;
-  float* red = reinterpret_cast<float*>(act_base + MCfg<MT>::ACT_BUDGET);  // [2][P][R][RS]
+  float* red = reinterpret_cast<float*>(act_base + MCfg<MT>::ACT_BUDGET);  // [2][HALVES][P][R][RS]
   uint64_t* full = reinterpret_cast<uint64_t*>(act_base + MCfg<MT>::ACT_BUDGET + red_bytes<R, MT>());
   uint64_t* empty = full + STAGES;
   volatile int* misc = reinterpret_cast<volatile int*>(empty + STAGES);
@@ -552,8 +593,10 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
     cluster_wait_aligned();
   }
 
-  const int i = threadIdx.x % R;  // row inside the tile
-  const int p = threadIdx.x / R;  // part: chunk p of each round
+  const int i = threadIdx.x % R;        // row inside the tile
+  const int p = (threadIdx.x / R) % P;  // part: chunk p of each round
+  const int hb = threadIdx.x / 128;     // half of the chunk (blocks 4hb..) when HALVES == 2
+  const bool merger = (int)threadIdx.x < R;  // merges, counts and stores row i
   const int UB = a.RU * P * CHUNK_BLOCKS;  // activation blocks per unit
   // laid out for MT rows (the planner sized the unit for MT), so rows
   // M <= m < MT read inside the staging area
@@ -613,7 +656,7 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
 #pragma unroll
       for (int m = 0; m < MT; ++m) v[m] = 0.0f;
       const int xpar = consumed & 1;
-      float* rb = red + (size_t)xpar * P * R * RS;  // [P][R][RS]
+      float* rb = red + (size_t)xpar * HALVES * P * R * RS;  // [HALVES][P][R][RS]
       if constexpr (TC) {
         // 8 slices (16 rows x one chunk) per round, two per warp (a loop, not
         // unrolled: one copy of the slice code keeps the instruction cache warm)
@@ -644,11 +687,15 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
         if (got && c < a.nch) {
           const int blk = (rho * P + p) * CHUNK_BLOCKS;  // first block of the chunk in the unit
           const uint8_t* cq = stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES + p * (r * CHUNK_BLOCKS * BLOCK_BYTES);
-          chunk_value<MT>(cq, r, chunk_blocks(c, a.NB), i, L.q + blk * 32, L.d + blk, L.mq, UB, v);
+          if constexpr (HALVES == 1)
+            chunk_value<MT>(cq, r, chunk_blocks(c, a.NB), i, L.q + blk * 32, L.d + blk, L.mq, UB, v);
+          else
+            chunk_value_half<MT>(cq, r, chunk_blocks(c, a.NB), i, 4 * hb, L.q + blk * 32, L.d + blk, L.mq,
+                                 UB, v);
         }
         if constexpr (EXCHANGE) {
 #pragma unroll
-          for (int m = 0; m < MT; ++m) rb[(p * R + i) * RS + m] = v[m];
+          for (int m = 0; m < MT; ++m) rb[((hb * P + p) * R + i) * RS + m] = v[m];
         }
       }
       __syncwarp();
@@ -667,9 +714,9 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
           ok = false;
           break;
         }
-        if (p != 0) continue;
+        if (!merger) continue;
 #pragma unroll
-        for (int m = 0; m < MT; ++m) v[m] = tree_of<P>(rb + i * RS + m, R * RS);
+        for (int m = 0; m < MT; ++m) v[m] = tree_of<P, HALVES>(rb + i * RS + m, R * RS, P * R * RS);
       } else {
         if (!got || misc[0]) {
           ok = false;
@@ -708,7 +755,7 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
     }
 
     if (a.S == 1) {
-      if (ok && p == 0 && i < r) {
+      if (ok && merger && i < r) {
 #pragma unroll
         for (int m = 0; m < MT; ++m)
           if (m < a.M) a.y[(int64_t)m * a.N + n] = pv[m];
@@ -717,7 +764,7 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
     }
 
     // split along K: publish the unit value, take a ticket, last one combines
-    if (ok && p == 0 && i < r) {
+    if (ok && merger && i < r) {
 #pragma unroll
       for (int m = 0; m < MT; ++m)
         if (m < a.M) a.ws_part[((int64_t)s * a.M + m) * a.N + n] = pv[m];
@@ -733,7 +780,7 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, 1) gemv_kernel(const GemvAr
     if (misc[1]) {
       __threadfence();
       if (i < r) {
-        for (int m = p; m < a.M; m += P) {  // every part thread of the row takes some m
+        for (int m = p + hb * P; m < a.M; m += P * HALVES) {  // every thread of the row takes some m
           float sl[SPLIT_LEVELS];
 #pragma unroll
           for (int l = 0; l < SPLIT_LEVELS; ++l) sl[l] = 0.0f;
