@@ -70,6 +70,15 @@ bool cluster_fits(int R, int MT, bool fused, int c) {
 }
 
 int mt_of(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
+int stage_target_of(int MT) {
+  switch (MT) {
+    case 1: return MCfg<1>::STAGE_TARGET;
+    case 2: return MCfg<2>::STAGE_TARGET;
+    case 4: return MCfg<4>::STAGE_TARGET;
+    case 8: return MCfg<8>::STAGE_TARGET;
+    default: return MCfg<16>::STAGE_TARGET;
+  }
+}
 int budget_of(int MT) {
   switch (MT) {
     case 1: return MCfg<1>::ACT_BUDGET;
@@ -124,9 +133,9 @@ bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, G
   q.grid = (int)(units < dev.sm_count ? units : dev.sm_count);
   // When every unit covers all of K and every CTA has exactly one unit, the
   // CTAs stage the same activation blocks on the critical path.  If one CTA
-  // would stage more than STAGE_TARGET_BLOCKS of them, clusters of 2 or 4 CTAs
-  // share the work (each stages 1/c and writes it to all, then a cluster
-  // barrier); otherwise each CTA stages everything itself, which is cheaper
+  // would stage more than one batch of them (MCfg::STAGE_TARGET), clusters
+  // of 2 or 4 CTAs share the work (each stages 1/c and writes it to all,
+  // then a cluster barrier); otherwise each CTA stages everything itself, which is cheaper
   // than the barrier.  CTAs that loop over several units stage once and
   // amortize it, so they run unclustered (no co-scheduling constraint).  The
   // grid is rounded down to a multiple of the cluster size (persistent CTAs
@@ -140,7 +149,8 @@ bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, G
     const int cmax = 4;
 #endif
     int want = 1;
-    while (want < cmax && (blocks + want - 1) / want > STAGE_TARGET_BLOCKS) want <<= 1;
+    const int target = stage_target_of(q.MT);
+    while (want < cmax && (blocks + want - 1) / want > target) want <<= 1;
     for (int c = want; c >= 2; c >>= 1) {
       if (q.grid >= c && cluster_fits(q.R, q.MT, fused, c)) {
         q.cluster = c;

@@ -59,12 +59,6 @@ constexpr int SPLIT_LEVELS = 8;  // binary counter levels for S <= 128
 constexpr int MAX_SPLIT_TILES = 4096;
 constexpr size_t TICKET_BYTES = (size_t)MAX_SPLIT_TILES * 4;
 constexpr int MAX_ROUNDS_PER_UNIT = 64;
-// Blocks one CTA stages by itself before the planner shares the staging
-// among the CTAs of a cluster.
-#ifndef Q8_STAGE_TARGET
-#define Q8_STAGE_TARGET 64
-#endif
-constexpr int STAGE_TARGET_BLOCKS = Q8_STAGE_TARGET;
 
 
 enum : unsigned { ERR_PRODUCER_WAIT = 1u, ERR_CONSUMER_WAIT = 2u, ERR_DRAIN_WAIT = 4u };
@@ -86,10 +80,13 @@ struct MCfg {
   // CTAs per SM the kernel is compiled for: the 288-thread kernel for one
   // row must keep two CTAs per SM (registers included)
   static constexpr int MIN_CTAS = MT == 1 ? 2 : 1;
-  // activation staging: passes of 16 blocks (8 lanes per block), STAGE_BATCH
+  // activation staging: passes of NCW*4 blocks (8 lanes per block), STAGE_BATCH
   // passes with their loads in flight together (larger batches measured
   // slower for every row count)
   static constexpr int STAGE_BATCH = 4;
+  // blocks one CTA stages by itself (one batch: passes of NCW*4 blocks)
+  // before the planner shares the staging among the CTAs of a cluster
+  static constexpr int STAGE_TARGET = NCW * 4 * STAGE_BATCH;
   // bytes of staged activations: 256 blocks (K = 8192 in one unit) for
   // MT <= 4, and for those the whole shared-memory use stays below half an
   // SM's, so two CTAs (of consecutive kernels) fit
