@@ -200,6 +200,9 @@ cudaError_t launch_gemv(const GemvPlan& p, const uint8_t* W, const uint8_t* A, c
       MT = mt_of(Mp);
       if (MT <= 2) MT = 4;
     }
+    // shared memory for the unit's staged activations only (a launch with a
+    // short K range does not reserve the whole budget)
+    args.act_smem = (act_bytes(MT, 128 / p.R, p.RU) + 15) / 16 * 16;
     switch (p.R) {
       case 16: e = launch_gemv_r<16>(args, MT, fused, p.grid, p.cluster, pdl, s); break;
       case 32: e = launch_gemv_r<32>(args, MT, fused, p.grid, p.cluster, pdl, s); break;

@@ -91,7 +91,11 @@ struct MCfg {
   // bytes of staged activations: 256 blocks (K = 8192 in one unit) for
   // MT <= 4, and for those the whole shared-memory use stays below half an
   // SM's, so two CTAs (of consecutive kernels) fit
-  static constexpr int ACT_BUDGET = MT == 1 ? 8704 : MT == 2 ? 17408 : MT == 4 ? 34816 : 40960;
+  // 8-16 rows: one CTA per SM anyway; the budget holds K = 8192 (256 blocks
+  // of MT rows, padded rows, binary16 scales) so such matrices need no split
+  // along K (a split restages the activations for every unit)
+  static constexpr int ACT_BUDGET = MT == 1 ? 8704 : MT == 2 ? 17408 : MT == 4 ? 34816
+                                  : MT * (256 * 32 + 16) + MT * 256 * 2;
 };
 
 // Activation rows at or above this use the tensor-core path.
@@ -134,8 +138,8 @@ constexpr int red_bytes() {
 }
 
 template <int R, int MT>
-constexpr size_t gemv_smem_bytes() {
-  return (size_t)MCfg<MT>::STAGES * RCfg<R>::STAGE_BYTES + MCfg<MT>::ACT_BUDGET + red_bytes<R, MT>() +
+constexpr size_t gemv_smem_bytes(int act = MCfg<MT>::ACT_BUDGET) {
+  return (size_t)MCfg<MT>::STAGES * RCfg<R>::STAGE_BYTES + act + red_bytes<R, MT>() +
          2 * MCfg<MT>::STAGES * sizeof(uint64_t) + 4 * sizeof(int);
 }
 
@@ -150,6 +154,7 @@ struct GemvArgs {
   unsigned* err;         // device error word
   int64_t N;
   int NB, nch, T, M, RU, S, units;
+  int act_smem;          // bytes of the activation staging area of this launch (<= ACT_BUDGET, 16 | x)
 };
 
 // ---- producer: one lane streams the rounds of every unit of this CTA ----
@@ -546,8 +551,9 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stage_buf = smem;
   uint8_t* act_base = smem + (size_t)STAGES * RCfg<R>::STAGE_BYTES;
-  float* red = reinterpret_cast<float*>(act_base + MCfg<MT>::ACT_BUDGET);  // [2][HALVES][P][R][RS]
-  uint64_t* full = reinterpret_cast<uint64_t*>(act_base + MCfg<MT>::ACT_BUDGET + red_bytes<R, MT>());
+  // the activation area is sized per launch (the unit's blocks), the rest follows it
+  float* red = reinterpret_cast<float*>(act_base + a.act_smem);  // [2][HALVES][P][R][RS]
+  uint64_t* full = reinterpret_cast<uint64_t*>(act_base + a.act_smem + red_bytes<R, MT>());
   uint64_t* empty = full + STAGES;
   volatile int* misc = reinterpret_cast<volatile int*>(empty + STAGES);
   // misc[0]: abort flag, misc[1]: "this CTA combines the tile", misc[2]: rounds issued
@@ -858,7 +864,7 @@ cudaError_t launch_gemv_t(const GemvArgs& args, int grid, int cluster, bool pdl,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(MCfg<MT>::THREADS);
-  cfg.dynamicSmemBytes = gemv_smem_bytes<R, MT>();
+  cfg.dynamicSmemBytes = gemv_smem_bytes<R, MT>(args.act_smem);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   int na = 0;
