@@ -128,8 +128,8 @@ bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, G
   const int64_t units = T * S;
   if (units > ((int64_t)1 << 31) - 1) return false;
   q.units = (int)units;
-  // one CTA per SM: the second slot of each SM stays free for the next
-  // kernel in the stream, which starts streaming its weights early (PDL)
+  // one persistent CTA per SM; SMs this kernel leaves free take the next
+  // kernel's CTAs early (PDL), which stream their first weights at once
   q.grid = (int)(units < dev.sm_count ? units : dev.sm_count);
   // When every unit covers all of K and every CTA has exactly one unit, the
   // CTAs stage the same activation blocks on the critical path.  If one CTA

@@ -77,9 +77,13 @@ struct MCfg {
   static constexpr int HALVES = NCW * 32 / 128;       // threads per (row, chunk)
   static constexpr int THREADS = (NCW + 1) * 32;      // + the producer warp
   static constexpr int STAGES = MT == 1 ? 3 : 2;
-  // CTAs per SM the kernel is compiled for: the 288-thread kernel for one
-  // row must keep two CTAs per SM (registers included)
-  static constexpr int MIN_CTAS = MT == 1 ? 2 : 1;
+  // CTAs per SM the kernel is compiled for: one.  Registers are not capped
+  // for a second CTA: a co-resident CTA of the next kernel (started early by
+  // PDL) prefetches while the current kernel, which is on the critical path,
+  // still streams and computes, and measured slower (the 288-thread kernel
+  // at 96 registers and two CTAs per SM: 0.373 ms per M = 1 step; uncapped,
+  // one CTA per SM: 0.326 ms)
+  static constexpr int MIN_CTAS = 1;
   // activation staging: passes of NCW*4 blocks (8 lanes per block), STAGE_BATCH
   // passes with their loads in flight together (larger batches measured
   // slower for every row count; every pass of a batch is quantized, so the
@@ -88,12 +92,9 @@ struct MCfg {
   // blocks one CTA stages by itself (one batch: passes of NCW*4 blocks)
   // before the planner shares the staging among the CTAs of a cluster
   static constexpr int STAGE_TARGET = NCW * 4 * STAGE_BATCH;
-  // bytes of staged activations: 256 blocks (K = 8192 in one unit) for
-  // MT <= 4, and for those the whole shared-memory use stays below half an
-  // SM's, so two CTAs (of consecutive kernels) fit
-  // 8-16 rows: one CTA per SM anyway; the budget holds K = 8192 (256 blocks
-  // of MT rows, padded rows, binary16 scales) so such matrices need no split
-  // along K (a split restages the activations for every unit)
+  // bytes of staged activations: 256 blocks of MT rows (padded rows on the
+  // tensor path, binary16 scales), so K = 8192 fits one unit and needs no
+  // split along K (a split restages the activations for every unit)
   static constexpr int ACT_BUDGET = MT == 1 ? 8704 : MT == 2 ? 17408 : MT == 4 ? 34816
                                   : MT * (256 * 32 + 16) + MT * 256 * 2;
 };
@@ -843,9 +844,8 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
   }
 }
 
-// Every libq8 kernel asks for the largest shared-memory carveout, so CTAs of
-// consecutive kernels can share an SM (a programmatic dependent starts while
-// its predecessor still runs); kernels with different carveouts cannot.
+// Every libq8 kernel asks for the largest shared-memory carveout (the same
+// for all, so an SM switching between kernels needs no reconfiguration).
 template <int R, int MT, bool FUSED>
 cudaError_t set_attributes() {
   cudaError_t e = cudaFuncSetAttribute(gemv_kernel<R, MT, FUSED>,
