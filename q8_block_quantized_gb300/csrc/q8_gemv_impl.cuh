@@ -71,9 +71,10 @@ struct RCfg {
 
 template <int MT>
 struct MCfg {
-  // consumer warps: 8 for one activation row (each thread then takes half a
-  // chunk, 4 blocks, which halves the latency of a round), else 4
-  static constexpr int NCW = MT == 1 ? 8 : 4;
+  // consumer warps: 8 on the DP4A path (1-4 activation rows: each thread then
+  // takes half a chunk, 4 blocks, which halves the latency of a round; the
+  // 288-thread CTA also keeps one CTA per SM), 4 on the tensor path
+  static constexpr int NCW = MT <= 4 ? 8 : 4;
   static constexpr int HALVES = NCW * 32 / 128;       // threads per (row, chunk)
   static constexpr int THREADS = (NCW + 1) * 32;      // + the producer warp
   static constexpr int STAGES = MT == 1 ? 3 : 2;
