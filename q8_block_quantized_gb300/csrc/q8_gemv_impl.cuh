@@ -71,11 +71,14 @@ struct RCfg {
 
 template <int MT>
 struct MCfg {
-  // consumer warps: 8 on the DP4A path (1-4 activation rows: each thread then
-  // takes half a chunk, 4 blocks, which halves the latency of a round; the
-  // 288-thread CTA also keeps one CTA per SM), 4 on the tensor path
-  static constexpr int NCW = MT <= 4 ? 8 : 4;
-  static constexpr int HALVES = NCW * 32 / 128;       // threads per (row, chunk)
+  // consumer warps: 8 for 1-8 activation rows (on the DP4A path each thread
+  // then takes half a chunk, 4 blocks, which halves the latency of a round;
+  // on the tensor path each warp takes one 16-row slice of a round; the
+  // 288-thread CTA also keeps one CTA per SM), 4 for 16 rows
+  static constexpr int NCW = MT <= 8 ? 8 : 4;
+  // threads per (row, chunk) on the DP4A path; the tensor path computes a
+  // round as 8 slices of 16 rows, 8 / NCW per warp
+  static constexpr int HALVES = MT >= 8 ? 1 : NCW * 32 / 128;
   static constexpr int THREADS = (NCW + 1) * 32;      // + the producer warp
   static constexpr int STAGES = MT == 1 ? 3 : 2;
   // CTAs per SM the kernel is compiled for: one.  Registers are not capped
@@ -664,11 +667,11 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
       const int xpar = consumed & 1;
       float* rb = red + (size_t)xpar * HALVES * P * R * RS;  // [HALVES][P][R][RS]
       if constexpr (TC) {
-        // 8 slices (16 rows x one chunk) per round, two per warp (a loop, not
+        // 8 slices (16 rows x one chunk) per round, 8/NCW per warp (a loop, not
         // unrolled: one copy of the slice code keeps the instruction cache warm)
         const int g = lane >> 2, tig = lane & 3;
 #pragma unroll 1
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < 8 / NCW; ++k) {
           const int sl = warp + k * NCW;
           const int ps = sl / (R / 16), row0 = (sl % (R / 16)) * 16;
           const int c = c0 + rho * P + ps;
@@ -786,7 +789,7 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
     if (misc[1]) {
       __threadfence();
       if (i < r) {
-        for (int m = p + hb * P; m < a.M; m += P * HALVES) {  // every thread of the row takes some m
+        for (int m = p + hb * P; m < a.M; m += P * (NT / 128)) {  // every thread of the row takes some m
           float sl[SPLIT_LEVELS];
 #pragma unroll
           for (int l = 0; l < SPLIT_LEVELS; ++l) sl[l] = 0.0f;
