@@ -71,11 +71,11 @@ struct RCfg {
 
 template <int MT>
 struct MCfg {
-  // consumer warps: 8 for 1-8 activation rows (on the DP4A path each thread
-  // then takes half a chunk, 4 blocks, which halves the latency of a round;
-  // on the tensor path each warp takes one 16-row slice of a round; the
-  // 288-thread CTA also keeps one CTA per SM), 4 for 16 rows
-  static constexpr int NCW = MT <= 8 ? 8 : 4;
+  // consumer warps: 8 (on the DP4A path each thread takes half a chunk, 4
+  // blocks, which halves the latency of a round; on the tensor path each
+  // warp takes one 16-row slice of a round; the 288-thread CTA also keeps
+  // one CTA per SM)
+  static constexpr int NCW = 8;
   // threads per (row, chunk) on the DP4A path; the tensor path computes a
   // round as 8 slices of 16 rows, 8 / NCW per warp
   static constexpr int HALVES = MT >= 8 ? 1 : NCW * 32 / 128;
@@ -605,7 +605,13 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
   const int i = threadIdx.x % R;        // row inside the tile
   const int p = (threadIdx.x / R) % P;  // part: chunk p of each round
   const int hb = threadIdx.x / 128;     // half of the chunk (blocks 4hb..) when HALVES == 2
-  const bool merger = (int)threadIdx.x < R;  // merges, counts and stores row i
+  // After each round's exchange, row i is merged by CG threads (t % R = i),
+  // each owning MC of the MT output columns: the merge work and the binary
+  // counter's registers are shared out.
+  constexpr int CG = EXCHANGE ? (NT / R < MT ? NT / R : MT) : 1;
+  constexpr int MC = MT / CG;
+  const int mcg = threadIdx.x / R;
+  const bool merger = mcg < CG;  // merges, counts and stores columns [mcg*MC, +MC) of row i
   const int UB = a.RU * P * CHUNK_BLOCKS;  // activation blocks per unit
   // laid out for MT rows (the planner sized the unit for MT), so rows
   // M <= m < MT read inside the staging area
@@ -647,11 +653,11 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
       if (a.A_out != nullptr && t == 0) write_act_blocks<NT>(a, L, b0, nblk);
     }
 
-    float slot[MT][LV];
+    float slot[MC][LV];
 #pragma unroll
-    for (int m = 0; m < MT; ++m)
+    for (int c = 0; c < MC; ++c)
 #pragma unroll
-      for (int l = 0; l < LV; ++l) slot[m][l] = 0.0f;
+      for (int l = 0; l < LV; ++l) slot[c][l] = 0.0f;
 
     for (int rho = 0; rho < nrounds; ++rho) {
       // the abort decision must be the same for every consumer (they meet
@@ -664,6 +670,7 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
       float v[MT];
 #pragma unroll
       for (int m = 0; m < MT; ++m) v[m] = 0.0f;
+      float mv[MC];  // this thread's merged columns of the round
       const int xpar = consumed & 1;
       float* rb = red + (size_t)xpar * HALVES * P * R * RS;  // [HALVES][P][R][RS]
       if constexpr (TC) {
@@ -725,24 +732,26 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
         }
         if (!merger) continue;
 #pragma unroll
-        for (int m = 0; m < MT; ++m) v[m] = tree_of<P, HALVES>(rb + i * RS + m, R * RS, P * R * RS);
+        for (int c = 0; c < MC; ++c) mv[c] = tree_of<P, HALVES>(rb + i * RS + mcg * MC + c, R * RS, P * R * RS);
       } else {
         if (!got || misc[0]) {
           ok = false;
           break;
         }
+#pragma unroll
+        for (int c = 0; c < MC; ++c) mv[c] = v[c];  // CG == 1: the thread's own row
       }
-      // binary counter over the round subtrees (part-0 threads)
+      // binary counter over the round subtrees (merging threads)
       bool placed = false;
 #pragma unroll
       for (int l = 0; l < LV; ++l) {
         if (!placed) {
           if ((rho >> l) & 1) {
 #pragma unroll
-            for (int m = 0; m < MT; ++m) v[m] = tadd(slot[m][l], v[m]);
+            for (int c = 0; c < MC; ++c) mv[c] = tadd(slot[c][l], mv[c]);
           } else {
 #pragma unroll
-            for (int m = 0; m < MT; ++m) slot[m][l] = v[m];
+            for (int c = 0; c < MC; ++c) slot[c][l] = mv[c];
             placed = true;
           }
         }
@@ -750,15 +759,15 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
     }
 
     // what is left merges from the lowest level up (= zero padding)
-    float pv[MT];
+    float pv[MC];
     bool have = false;
 #pragma unroll
-    for (int m = 0; m < MT; ++m) pv[m] = 0.0f;
+    for (int c = 0; c < MC; ++c) pv[c] = 0.0f;
 #pragma unroll
     for (int l = 0; l < LV; ++l) {
       if ((nrounds >> l) & 1) {
 #pragma unroll
-        for (int m = 0; m < MT; ++m) pv[m] = have ? tadd(slot[m][l], pv[m]) : slot[m][l];
+        for (int c = 0; c < MC; ++c) pv[c] = have ? tadd(slot[c][l], pv[c]) : slot[c][l];
         have = true;
       }
     }
@@ -766,8 +775,10 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
     if (a.S == 1) {
       if (ok && merger && i < r) {
 #pragma unroll
-        for (int m = 0; m < MT; ++m)
-          if (m < a.M) a.y[(int64_t)m * a.N + n] = pv[m];
+        for (int c = 0; c < MC; ++c) {
+          const int m = mcg * MC + c;
+          if (m < a.M) a.y[(int64_t)m * a.N + n] = pv[c];
+        }
       }
       continue;
     }
@@ -775,8 +786,10 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
     // split along K: publish the unit value, take a ticket, last one combines
     if (ok && merger && i < r) {
 #pragma unroll
-      for (int m = 0; m < MT; ++m)
-        if (m < a.M) a.ws_part[((int64_t)s * a.M + m) * a.N + n] = pv[m];
+      for (int c = 0; c < MC; ++c) {
+        const int m = mcg * MC + c;
+        if (m < a.M) a.ws_part[((int64_t)s * a.M + m) * a.N + n] = pv[c];
+      }
     }
     __threadfence();
     named_bar_sync(BAR_CONSUMERS, NT);
