@@ -80,7 +80,7 @@ struct MCfg {
   // round as 8 slices of 16 rows, 8 / NCW per warp
   static constexpr int HALVES = MT >= 8 ? 1 : NCW * 32 / 128;
   static constexpr int THREADS = (NCW + 1) * 32;      // + the producer warp
-  static constexpr int STAGES = MT == 1 ? 3 : 2;
+  static constexpr int STAGES = MT <= 2 ? 3 : 2;
   // CTAs per SM the kernel is compiled for: one.  Registers are not capped
   // for a second CTA: a co-resident CTA of the next kernel (started early by
   // PDL) prefetches while the current kernel, which is on the critical path,
