@@ -1,27 +1,32 @@
-// q8_gemv_impl.cuh -- the Q8_0 decode GEMV kernel (int8 dot products on the
-// DP4A path), templated on the packed tile height R, the activation rows per
-// pass MT and whether the activation is quantized in the kernel (FUSED).
+// q8_gemv_impl.cuh -- the Q8_0 decode GEMV kernel, templated on the packed
+// tile height R, the activation rows per pass MT and whether the activation
+// is quantized in the kernel (FUSED).
 //
 // Work decomposition.  The packed layout groups rows in tiles of R rows
 // (R in {16, 32, 64, 128}, chosen from N so a matrix has about one tile per
-// SM) and blocks in chunks of 8; the chunks of a tile are contiguous.  The
-// 128 consumer threads of a CTA are P = 128/R parts x R rows: thread t owns
-// row i = t % R and part p = t / R.  A pipeline round is P consecutive chunks
-// of one tile (one contiguous bulk copy of up to 34,816 bytes); part p
-// computes chunk p of the round for its row.  For one activation row the CTA
-// has 256 consumer threads and each (row, part) pair is split in two halves
-// of 4 blocks (t / 128 picks the half), which halves a round's latency; the
-// halves' values meet in the exchange like the parts'.  A work unit is one tile times
-// RU consecutive rounds; usually a unit covers all of K and a tile is one
-// unit.
+// SM) and blocks in chunks of 8; the chunks of a tile are contiguous.  A
+// pipeline round is P = 128/R consecutive chunks of one tile (one contiguous
+// bulk copy of up to 34,816 bytes).  A work unit is one tile times RU
+// consecutive rounds; usually a unit covers all of K and a tile is one unit.
+// A CTA is 8 consumer warps and one producer warp, one CTA per SM.
 //
-// Pipeline.  Warp 4 is the producer: one lane issues one cp.async.bulk copy
-// per round into a ring of shared-memory stages, completing on mbarriers.
-// Warps 0-3 consume: for each block of its chunk, a thread computes the exact
-// int32 dot of its row with every activation row (__dp4a), the canonical
-// term t_b = float(isum) * (d_w * d_a), and the pairwise tree of the chunk.
-// Within a quarter warp the 8 lanes read 8 consecutive rows of one chunk
-// (distinct banks) and the same activation block (a broadcast).
+// DP4A path (MT <= 4).  Consumer thread t owns row i = t % R, part p =
+// (t / R) % P (chunk p of each round) and half t / 128 of that chunk (4
+// blocks), which halves a round's latency.  For each block it computes the
+// exact int32 dot of its row with every activation row (__dp4a), the
+// canonical term t_b = float(isum) * (d_w * d_a), and the pairwise tree of
+// its blocks.  Within a quarter warp the 8 lanes read 8 consecutive rows of
+// one chunk (distinct banks) and the same activation block (a broadcast).
+// Tensor path (MT >= 8).  A warp computes 16-row slices of a chunk with
+// mma.sync on int8 values converted exactly to fp16 (8 slices per round,
+// one per warp); the block terms and trees are the same as on the DP4A path.
+// Either way the values of a round meet in shared memory, and each row is
+// then merged by CG = min(256 / R, MT) threads that own MT / CG output
+// columns each.
+//
+// Pipeline.  One lane of the producer warp issues one cp.async.bulk copy per
+// round into a ring of shared-memory stages, completing on mbarriers; every
+// wait is bounded and a failed wait sets the device error word and aborts.
 //
 // Reduction order.  The sum over blocks b is the pairwise tree over b,
 // padded with zeros to a power of two.  A chunk (8 aligned blocks) is a

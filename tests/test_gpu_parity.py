@@ -111,7 +111,8 @@ def test_weight_quantize_repack_round_trip(q8):
         assert np.array_equal(np.sort(W.cpu().numpy()), np.sort(ref.ravel()))
 
 
-@pytest.mark.parametrize("N,K", [(131, 11 * 32), (3000, 5 * 32), (9000, 17 * 32), (20000, 96)])
+@pytest.mark.parametrize("N,K", [(131, 11 * 32), (3000, 5 * 32), (9000, 17 * 32), (20000, 96),
+                                 (40000, 64), (80000, 32), (160000, 32)])
 def test_packed_layout_matches_header_description(q8, N, K):
     # the byte positions stated in q8.h, for ragged tiles and chunks and
     # every tile height
