@@ -14,6 +14,8 @@ arrays to it.  Each C function cites the page passage it follows:
 * "Ember: packed Q8 decode", the row-contiguous source figure (a block is a
   scale followed by 32 quants) and the packed 16-row tile figure (544 bytes
   per 16 blocks).
+* "Ferro" README, "How the iGPU path is fast", item 3: fused producers (the
+  residual add and the norm, SwiGLU) that emit the next GEMM's int8 input.
 
 Every function is pinned by ``tests/test_oracle_pins.py``; none is
 "parity unpinned".
@@ -73,6 +75,13 @@ def _load():
         lib.q8o_gemm.argtypes = [u8p, i64, i64, u8p, i64, f64p, f64p]
         lib.q8o_quant_gemm.argtypes = [u8p, i64, i64, f32p, i64, u8p, f64p, f64p]
         lib.q8o_ember_tile_pack.argtypes = [u8p, u8p]
+        lib.q8o_pairwise_sum.argtypes = [f32p, i64]
+        lib.q8o_pairwise_sum.restype = ctypes.c_float
+        lib.q8o_exp_array.argtypes = [f32p, i64, f32p]
+        lib.q8o_silu_array.argtypes = [f32p, i64, f32p]
+        lib.q8o_residual_rmsnorm_quantize.argtypes = [f32p, f32p, f32p, ctypes.c_float, i64, i64,
+                                                      f32p, u8p]
+        lib.q8o_swiglu_quantize.argtypes = [f32p, i64, i64, u8p]
         lib.q8o_ember_tile_unpack.argtypes = [u8p, u8p]
         for name in ("q8o_qk", "q8o_block_bytes", "q8o_ember_tile_bytes"):
             getattr(lib, name).restype = ctypes.c_int
@@ -176,6 +185,62 @@ def quant_gemm(W, x, K: int):
                        _ptr(A, ctypes.c_uint8), _ptr(y, ctypes.c_double),
                        _ptr(S, ctypes.c_double))
     return y, S, A
+
+
+def pairwise_sum(v) -> float:
+    """Single-precision pairwise (tree) sum, zero-padded to a power of two."""
+    v = _f32(v).ravel()
+    return float(_load().q8o_pairwise_sum(_ptr(v, ctypes.c_float), v.size))
+
+
+def exp_f32(x) -> np.ndarray:
+    """The fixed single-precision e^x of the fused producers (elementwise)."""
+    x = _f32(x)
+    out = np.empty_like(x)
+    _load().q8o_exp_array(_ptr(x.ravel(), ctypes.c_float), x.size, _ptr(out.ravel(), ctypes.c_float))
+    return out
+
+
+def silu_f32(x) -> np.ndarray:
+    """silu(g) = g / (1 + e^-g) in single precision (elementwise)."""
+    x = _f32(x)
+    out = np.empty_like(x)
+    _load().q8o_silu_array(_ptr(x.ravel(), ctypes.c_float), x.size, _ptr(out.ravel(), ctypes.c_float))
+    return out
+
+
+def residual_rmsnorm_quantize(x, delta, gamma, eps: float):
+    """h = x + delta (delta may be None), y = RMSNorm(h) * gamma, quantized.
+    Returns (h [M][K] float32, blocks uint8 [M][K/32*34])."""
+    lib = _load()
+    x = _f32(x)
+    if x.ndim == 1:
+        x = x.reshape(1, -1)
+    M, K = x.shape
+    if K % QK:
+        raise ValueError("K must be a multiple of 32")
+    d = None if delta is None else _f32(delta).reshape(M, K)
+    g = _f32(gamma).reshape(K)
+    h = np.zeros((M, K), dtype=np.float32)
+    out = np.zeros((M, (K // QK) * BLOCK_BYTES), dtype=np.uint8)
+    lib.q8o_residual_rmsnorm_quantize(_ptr(x, ctypes.c_float),
+                                      None if d is None else _ptr(d, ctypes.c_float),
+                                      _ptr(g, ctypes.c_float), float(eps), M, K,
+                                      _ptr(h, ctypes.c_float), _ptr(out, ctypes.c_uint8))
+    return h, out
+
+
+def swiglu_quantize(gu, F: int) -> np.ndarray:
+    """gu [M][2F] (gate | up) -> blocks of silu(gate) * up, uint8 [M][F/32*34]."""
+    gu = _f32(gu)
+    if gu.ndim == 1:
+        gu = gu.reshape(1, -1)
+    M = gu.shape[0]
+    if gu.shape[1] != 2 * F or F % QK:
+        raise ValueError("gu must be [M][2F] with F a multiple of 32")
+    out = np.zeros((M, (F // QK) * BLOCK_BYTES), dtype=np.uint8)
+    _load().q8o_swiglu_quantize(_ptr(gu, ctypes.c_float), M, F, _ptr(out, ctypes.c_uint8))
+    return out
 
 
 def ember_tile_pack(blocks16) -> np.ndarray:

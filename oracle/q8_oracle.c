@@ -28,6 +28,8 @@
  *     bytes 2..33 (34 bytes per block).
  *   - output: y[m][n] = sum_b isum_b * d_w * d_a, accumulated here in fp64;
  *     every term is exact in fp64 (20 + 11 + 11 significant bits).
+ *   - fused producers (the norm and SwiGLU before quantization): see the
+ *     section at the end of this file.
  *
  * Build: any C99 compiler, -O2 -ffp-contract=off, no fast-math.  Portable C:
  * no intrinsics, no inline assembly, no reliance on the signedness of char.
@@ -38,6 +40,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define QK 32               /* values per block  [Ferro, item 1; Ember figure] */
@@ -260,4 +263,138 @@ void q8o_ember_tile_unpack(const uint8_t *tile, uint8_t *dst)
         dst[r * BLOCK_BYTES + 0] = *p++;
         dst[r * BLOCK_BYTES + 1] = *p++;
     }
+}
+
+/* ---------------------------------------------------------------------------
+ * Fused producers [Ferro, "How the iGPU path is fast", item 3: the residual
+ * add, the norm and the int8 quantization in one pass; SwiGLU emits the next
+ * GEMM's int8 input].  The pages name these fusions, not their arithmetic.
+ * Readings (each listed in the design doc), all in single precision, every
+ * operation one IEEE rounding (sqrt and division correctly rounded):
+ *   - RMSNorm as in the Llama family: h = x + delta (or x); s = sum_k h_k^2
+ *     summed as the pairwise tree over k padded with zeros to a power of
+ *     two; ms = s / K; r = 1 / sqrt(ms + eps); y_k = (h_k * r) * gamma_k.
+ *   - SwiGLU: h = silu(g) * u with silu(g) = g / (1 + e^-g), e^x being the
+ *     fixed procedure q8o_exp below; gate g and up u are the first and the
+ *     second half of each row of the gate/up product.
+ *   - then every 32-block of y (or h) is quantized by q8o_quantize_block.
+ * ------------------------------------------------------------------------- */
+
+/* Pairwise sum: the n values padded with zeros to p = 2^ceil(log2 n) leaves,
+ * then level by level each adjacent pair is added (a complete binary tree). */
+float q8o_pairwise_sum(const float *v, int64_t n)
+{
+    if (n <= 0)
+        return 0.0f;
+    int64_t p = 1;
+    while (p < n)
+        p <<= 1;
+    float *buf = (float *)malloc((size_t)p * sizeof(float));
+    if (buf == NULL)
+        return NAN;
+    for (int64_t i = 0; i < p; ++i)
+        buf[i] = i < n ? v[i] : 0.0f;
+    for (int64_t w = p; w > 1; w >>= 1)
+        for (int64_t i = 0; i < w / 2; ++i)
+            buf[i] = buf[2 * i] + buf[2 * i + 1];
+    float s = buf[0];
+    free(buf);
+    return s;
+}
+
+/* e^x by a fixed single-precision procedure: Cody and Waite's reduction
+ * x = n ln2 + r with ln2 split into 355/512 (9 significant bits, so n * 355/512
+ * is exact for |n| <= 128) plus the rest of ln2 rounded to single precision,
+ * then the Taylor polynomial of degree 7 of e^r in Horner form (|r| <= 0.35,
+ * truncation below 6e-9 relative), then the exact scaling by 2^n.  Outside
+ * [-87, 88] the result is 0 or +infinity. */
+#define Q8O_LOG2E 0x1.715476p+0f      /* 1/ln 2 rounded            */
+#define Q8O_LN2_HI 0x1.63p-1f         /* 355/512                   */
+#define Q8O_LN2_LO -0x1.bd0106p-13f   /* ln 2 - 355/512 rounded    */
+#define Q8O_C3 0x1.555556p-3f         /* 1/3! rounded              */
+#define Q8O_C4 0x1.555556p-5f         /* 1/4!                      */
+#define Q8O_C5 0x1.111112p-7f         /* 1/5!                      */
+#define Q8O_C6 0x1.6c16c2p-10f        /* 1/6!                      */
+#define Q8O_C7 0x1.a01a02p-13f        /* 1/7!                      */
+float q8o_exp(float x)
+{
+    if (x > 88.0f)
+        return INFINITY;
+    if (x < -87.0f)
+        return 0.0f;
+    float n = rintf(x * Q8O_LOG2E);
+    float r = (x - n * Q8O_LN2_HI) - n * Q8O_LN2_LO;
+    float p = Q8O_C7;
+    p = p * r + Q8O_C6;
+    p = p * r + Q8O_C5;
+    p = p * r + Q8O_C4;
+    p = p * r + Q8O_C3;
+    p = p * r + 0.5f;
+    p = p * r + 1.0f;
+    p = p * r + 1.0f;
+    return p * ldexpf(1.0f, (int)n);
+}
+
+float q8o_silu(float g)
+{
+    return g / (1.0f + q8o_exp(-g));
+}
+
+void q8o_exp_array(const float *x, int64_t n, float *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = q8o_exp(x[i]);
+}
+
+void q8o_silu_array(const float *x, int64_t n, float *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = q8o_silu(x[i]);
+}
+
+/* Residual add + RMSNorm + quantization of M rows of K values.
+ * x, delta (may be NULL): [M][K]; gamma: [K]; h_out (may be NULL): [M][K]
+ * receives h = x + delta; out: [M][K/32] blocks. */
+void q8o_residual_rmsnorm_quantize(const float *x, const float *delta, const float *gamma,
+                                   float eps, int64_t M, int64_t K, float *h_out, uint8_t *out)
+{
+    float *h = (float *)malloc((size_t)K * sizeof(float));
+    float *sq = (float *)malloc((size_t)K * sizeof(float));
+    float *y = (float *)malloc((size_t)K * sizeof(float));
+    if (h == NULL || sq == NULL || y == NULL) {
+        free(h); free(sq); free(y);
+        return;
+    }
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t k = 0; k < K; ++k) {
+            h[k] = delta != NULL ? x[m * K + k] + delta[m * K + k] : x[m * K + k];
+            sq[k] = h[k] * h[k];
+        }
+        if (h_out != NULL)
+            memcpy(h_out + m * K, h, (size_t)K * sizeof(float));
+        float s = q8o_pairwise_sum(sq, K);
+        float ms = s / (float)K;
+        float r = 1.0f / sqrtf(ms + eps);
+        for (int64_t k = 0; k < K; ++k)
+            y[k] = (h[k] * r) * gamma[k];
+        q8o_quantize_rows(y, 1, K, out + m * (K / QK) * BLOCK_BYTES);
+    }
+    free(h); free(sq); free(y);
+}
+
+/* SwiGLU + quantization: gu is [M][2F] (gate = gu[m][0..F), up =
+ * gu[m][F..2F)), out is [M][F/32] blocks of h = silu(gate) * up. */
+void q8o_swiglu_quantize(const float *gu, int64_t M, int64_t F, uint8_t *out)
+{
+    float h[QK];
+    int64_t nb = F / QK;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t b = 0; b < nb; ++b) {
+            for (int i = 0; i < QK; ++i) {
+                float g = gu[m * 2 * F + b * QK + i];
+                float u = gu[m * 2 * F + F + b * QK + i];
+                h[i] = q8o_silu(g) * u;
+            }
+            q8o_quantize_block(h, out + (m * nb + b) * BLOCK_BYTES);
+        }
 }
