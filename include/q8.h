@@ -128,6 +128,64 @@ Q8_API int q8_quantize_act(const float *x, int64_t M, int64_t K, void *out_block
                     unsigned flags, void *stream);
 
 /*
+ * Fused producers: the step before a GEMV, emitting its activation blocks
+ * directly (Ferro README, "How the iGPU path is fast", item 3: the residual
+ * add, the norm and the int8 quantization in one pass; SwiGLU emits the next
+ * GEMM's int8 input).  The pages give no arithmetic for these steps; the
+ * readings below are single-precision operations with one IEEE rounding
+ * each (sqrt and division correctly rounded), so the output is bit-exact
+ * and reproducible anywhere.  Both end in the rounding rule of
+ * q8_quantize_act.
+ */
+
+/*
+ * q8_residual_rmsnorm_quantize -- h = x + delta (or x when delta is NULL);
+ * y = RMSNorm(h) * gamma as in the Llama family; out_blocks = q8_quantize_act(y).
+ *
+ *   s  = sum over k of h_k * h_k, added as the pairwise tree over k (leaves
+ *        padded with zeros to the next power of two);
+ *   ms = s / K;  r = 1 / sqrt(ms + eps);  y_k = (h_k * r) * gamma_k.
+ *
+ *   x, delta   [M][K] fp32, 16-byte aligned (delta may be NULL).
+ *   gamma      [K] fp32, 16-byte aligned.
+ *   eps        positive and finite (else Q8_EINVAL).
+ *   M          rows, 1 <= M <= 2^31-1; K a positive multiple of 32,
+ *              K <= Q8_MAX_NORM_K.
+ *   h_out      optional [M][K] fp32 (16-byte aligned) receiving h, the new
+ *              residual stream; it may be x or delta (in-place update).
+ *   out_blocks [M][K/32] blocks, 2-byte aligned.
+ *   flags      0 or Q8_FLAG_PDL.
+ * One CTA per row.  Inputs whose squares overflow are outside the contract.
+ */
+#define Q8_MAX_NORM_K (1 << 24)
+Q8_API int q8_residual_rmsnorm_quantize(const float *x, const float *delta, const float *gamma,
+                                        float eps, int64_t M, int64_t K, float *h_out,
+                                        void *out_blocks, unsigned flags, void *stream);
+
+/*
+ * q8_swiglu_quantize -- h = silu(gate) * up, out_blocks = q8_quantize_act(h).
+ *
+ *   gate_up    [M][2F] fp32, 16-byte aligned: gate in columns [0, F), up in
+ *              [F, 2F) (the output of one GEMV over the concatenated gate
+ *              and up weights).
+ *   F          positive multiple of 32.
+ *   out_blocks [M][F/32] blocks, 2-byte aligned.
+ *   flags      0 or Q8_FLAG_PDL.
+ * silu(g) = g / (1 + e^-g).  e^x is a fixed procedure (Cody and Waite's
+ * reduction, then a Taylor polynomial), identical wherever it runs:
+ *   x > 88: +inf;  x < -87: 0;  otherwise n = rint(x * L2E),
+ *   r = (x - n * LN2_HI) - n * LN2_LO,
+ *   p = ((((((C7 r + C6) r + C5) r + C4) r + C3) r + 1/2) r + 1) r + 1,
+ *   e^x = p * 2^n,
+ * with L2E = 0x1.715476p+0 (1/ln 2), LN2_HI = 0x1.63p-1 (355/512),
+ * LN2_LO = -0x1.bd0106p-13 (ln 2 - 355/512), C3..C7 = 1/3!..1/7! rounded to
+ * single precision (0x1.555556p-3, 0x1.555556p-5, 0x1.111112p-7,
+ * 0x1.6c16c2p-10, 0x1.a01a02p-13); within 1 ulp of e^x.
+ */
+Q8_API int q8_swiglu_quantize(const float *gate_up, int64_t M, int64_t F, void *out_blocks,
+                              unsigned flags, void *stream);
+
+/*
  * q8_repack_weights -- move row-contiguous Q8_0 weight blocks into the packed
  * layout the GEMV streams.  A one-time step (Ember repacks each layer's projection
  * weights once at load time into 16-row tiles; Ferro keeps its device weights

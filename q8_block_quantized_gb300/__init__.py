@@ -40,6 +40,8 @@ SIGNATURES = {
     "q8_packed_tile_rows": (_int, [_i64]),
     "q8_workspace_bytes": (_sz, [_i64, _i64, _int]),
     "q8_quantize_act": (_int, [_vp, _i64, _i64, _vp, _u, _vp]),
+    "q8_residual_rmsnorm_quantize": (_int, [_vp, _vp, _vp, ctypes.c_float, _i64, _i64, _vp, _vp, _u, _vp]),
+    "q8_swiglu_quantize": (_int, [_vp, _i64, _i64, _vp, _u, _vp]),
     "q8_repack_weights": (_int, [_vp, _i64, _i64, _vp, _vp]),
     "q8_gemm": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _vp, _sz, _u, _vp]),
     "q8_fused_quant_gemm": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _vp, _vp, _sz, _u, _vp]),
@@ -127,6 +129,29 @@ def q8_quantize_act(x: torch.Tensor, out_blocks: torch.Tensor, flags: int = 0, s
     _check("q8_quantize_act", lib().q8_quantize_act(
         _dev(x, torch.float32, "x"), M, K, _dev(out_blocks, torch.uint8, "out_blocks"),
         flags, _stream(stream)))
+    return out_blocks
+
+
+def q8_residual_rmsnorm_quantize(x: torch.Tensor, gamma: torch.Tensor, eps: float,
+                                 out_blocks: torch.Tensor, delta: torch.Tensor | None = None,
+                                 h_out: torch.Tensor | None = None, flags: int = 0, stream=None):
+    """h = x + delta; out_blocks = quantized RMSNorm(h) * gamma (see q8.h)."""
+    M, K = x.shape
+    _check("q8_residual_rmsnorm_quantize", lib().q8_residual_rmsnorm_quantize(
+        _dev(x, torch.float32, "x"), _opt(delta, torch.float32, "delta"),
+        _dev(gamma, torch.float32, "gamma"), float(eps), M, K,
+        _opt(h_out, torch.float32, "h_out"), _dev(out_blocks, torch.uint8, "out_blocks"),
+        flags, _stream(stream)))
+    return out_blocks
+
+
+def q8_swiglu_quantize(gate_up: torch.Tensor, out_blocks: torch.Tensor, flags: int = 0,
+                       stream=None):
+    """out_blocks = quantized silu(gate) * up, gate_up = [M][2F] (see q8.h)."""
+    M, F2 = gate_up.shape
+    _check("q8_swiglu_quantize", lib().q8_swiglu_quantize(
+        _dev(gate_up, torch.float32, "gate_up"), M, F2 // 2,
+        _dev(out_blocks, torch.uint8, "out_blocks"), flags, _stream(stream)))
     return out_blocks
 
 

@@ -177,6 +177,36 @@ int q8_fused_quant_gemm(const void* W, int64_t N, int64_t K, const float* x, int
                                  (flags & Q8_FLAG_PDL) != 0, static_cast<cudaStream_t>(stream)));
 }
 
+int q8_residual_rmsnorm_quantize(const float* x, const float* delta, const float* gamma, float eps,
+                                 int64_t M, int64_t K, float* h_out, void* out_blocks, unsigned flags,
+                                 void* stream) {
+  if (x == nullptr || gamma == nullptr || out_blocks == nullptr || (flags & ~Q8_FLAG_PDL) != 0)
+    return Q8_EINVAL;
+  if (!(eps > 0.0f) || !(eps <= 3.0e38f)) return Q8_EINVAL;  // positive and finite (NaN fails)
+  if (M <= 0 || M > INT32_MAX || !k_ok(K) || K > Q8_MAX_NORM_K) return Q8_ESHAPE;
+  if (!aligned(x, 16) || !aligned(gamma, 16) || (delta != nullptr && !aligned(delta, 16)) ||
+      (h_out != nullptr && !aligned(h_out, 16)) || !aligned(out_blocks, 2))
+    return Q8_EALIGN;
+  DeviceInfo d;
+  int st = device_ok(&d);
+  if (st != Q8_OK) return st;
+  return cuda_status(launch_rmsnorm_quantize(x, delta, gamma, eps, M, K, h_out,
+                                             static_cast<uint8_t*>(out_blocks), (flags & Q8_FLAG_PDL) != 0,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+int q8_swiglu_quantize(const float* gate_up, int64_t M, int64_t F, void* out_blocks, unsigned flags,
+                       void* stream) {
+  if (gate_up == nullptr || out_blocks == nullptr || (flags & ~Q8_FLAG_PDL) != 0) return Q8_EINVAL;
+  if (M <= 0 || M > INT32_MAX || !k_ok(F) || F > ((int64_t)1 << 30)) return Q8_ESHAPE;
+  if (!aligned(gate_up, 16) || !aligned(out_blocks, 2)) return Q8_EALIGN;
+  DeviceInfo d;
+  int st = device_ok(&d);
+  if (st != Q8_OK) return st;
+  return cuda_status(launch_swiglu_quantize(gate_up, M, F, static_cast<uint8_t*>(out_blocks), d.sm_count,
+                                            (flags & Q8_FLAG_PDL) != 0, static_cast<cudaStream_t>(stream)));
+}
+
 int q8_block_dots(const void* W, int64_t N, int64_t K, const void* A_blocks, int M, int32_t* isum,
                   void* stream) {
   if (W == nullptr || A_blocks == nullptr || isum == nullptr) return Q8_EINVAL;

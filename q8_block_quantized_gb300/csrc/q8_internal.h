@@ -49,4 +49,11 @@ cudaError_t launch_gemv(const GemvPlan& p, const uint8_t* W, const uint8_t* A, c
                         uint8_t* A_out, float* y, void* workspace, bool pdl, cudaStream_t s);
 cudaError_t read_and_clear_gemv_error(unsigned* code);
 
+// Fused producers (q8_producers.cu).
+cudaError_t launch_rmsnorm_quantize(const float* x, const float* delta, const float* gamma, float eps,
+                                    int64_t M, int64_t K, float* h_out, uint8_t* out, bool pdl,
+                                    cudaStream_t s);
+cudaError_t launch_swiglu_quantize(const float* gu, int64_t M, int64_t F, uint8_t* out, int sm_count,
+                                   bool pdl, cudaStream_t s);
+
 }  // namespace q8

@@ -1,0 +1,260 @@
+// q8_producers.cu -- fused producers of the next GEMM's int8 input ("Ferro"
+// README, "How the iGPU path is fast", item 3: the residual add, the norm
+// and the int8 quantization in one pass; SwiGLU emitting the next GEMM's
+// int8 input directly).
+//
+// Both kernels end in the activation quantization of q8_quantize_act (the
+// same bits) and write row-contiguous Q8_0 blocks [M][K/32].  Their
+// floating-point steps are single-precision operations with one IEEE
+// rounding each (explicit _rn intrinsics, so no contraction into fma):
+//   RMSNorm: h = x + delta; s = sum_k h_k^2 as the pairwise tree over k,
+//            padded with zeros to a power of two; ms = s / K;
+//            r = 1 / sqrt(ms + eps); y_k = (h_k * r) * gamma_k.
+//   SwiGLU:  h = silu(g) * u, silu(g) = g / (1 + e^-g), e^x by the fixed
+//            procedure exp_cw below.
+#include <cuda_runtime.h>
+
+#include "q8_device.cuh"
+#include "q8_internal.h"
+
+namespace q8 {
+namespace {
+
+constexpr int NORM_THREADS = 256;    // 8 warps per row
+constexpr int SWIGLU_THREADS = 256;  // 32 blocks per pass, 8 lanes each
+constexpr int NORM_LEVELS = 20;      // binary counter over chunks: up to 2^19 chunks of 8
+
+// The 8 lanes of a group store one block: lane s the quants of values
+// 4s..4s+3 (bytes 2+4s..5+4s, 2-byte aligned), lane 0 also the scale.
+__device__ __forceinline__ void store_block_lane(uint8_t* ob, int sub, uint32_t w, float d) {
+  uint16_t* o16 = reinterpret_cast<uint16_t*>(ob);
+  o16[1 + 2 * sub] = (uint16_t)(w & 0xffffu);
+  o16[2 + 2 * sub] = (uint16_t)(w >> 16);
+  if (sub == 0) o16[0] = __half_as_ushort(__float2half_rn(d));  // d is a binary16 value: exact
+}
+
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
+}
+
+// ---- residual add + RMSNorm + quantization: one CTA per row ----
+// The sum of squares is the pairwise tree over k with P = 2^ceil(log2 K)
+// leaves (zeros past K).  Thread t sums the aligned leaf segment
+// [tL, (t+1)L), L = P / 256 (one leaf for threads t < P when P < 256), in
+// chunks of 8 leaves merged by a binary counter (what is left merges from the
+// lowest level up, which is what the zero leaves give); then a butterfly
+// inside each warp and a pairwise tree over the 8 warps.  Each step adds two
+// adjacent subtrees of equal size, so the result is the tree sum.
+__global__ void __launch_bounds__(NORM_THREADS)
+    rmsnorm_quant_kernel(const float* x, const float* delta, const float* __restrict__ gamma, float eps,
+                         int64_t K, float* h_out, uint8_t* __restrict__ out) {
+  // h_out may be x or delta (an in-place residual update): no restrict on them
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ float wsum[NORM_THREADS / 32];
+  __shared__ float rs;
+  const int64_t m = blockIdx.x;
+  const float* xr = x + m * K;
+  const float* dr = delta != nullptr ? delta + m * K : nullptr;
+  float* hr = h_out != nullptr ? h_out + m * K : nullptr;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  int64_t P = 1;
+  while (P < K) P <<= 1;
+  const int64_t L = P >= NORM_THREADS ? P / NORM_THREADS : 1;
+  const int64_t k0 = (int64_t)threadIdx.x * L;
+  float seg = 0.0f;
+  if (L < 8) {
+    // 1, 2 or 4 leaves (K <= 512): scalar loads
+    float sq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t k = k0 + j;
+      if (j < L && k < K) {
+        const float h = dr != nullptr ? __fadd_rn(__ldcg(xr + k), __ldcg(dr + k)) : __ldcg(xr + k);
+        if (hr != nullptr) hr[k] = h;
+        sq[j] = __fmul_rn(h, h);
+      }
+    }
+    seg = L == 1 ? sq[0] : L == 2 ? __fadd_rn(sq[0], sq[1])
+                                  : __fadd_rn(__fadd_rn(sq[0], sq[1]), __fadd_rn(sq[2], sq[3]));
+  } else {
+    float slot[NORM_LEVELS];
+    int64_t c = 0;
+    // chunks of 8 leaves; K is a multiple of 32, so a chunk is all data or all padding
+    for (; c < L / 8 && k0 + 8 * c < K; ++c) {
+      const int64_t k = k0 + 8 * c;
+      float4 a = __ldcg(reinterpret_cast<const float4*>(xr + k));
+      float4 b = __ldcg(reinterpret_cast<const float4*>(xr + k + 4));
+      if (dr != nullptr) {
+        a = add4(a, __ldcg(reinterpret_cast<const float4*>(dr + k)));
+        b = add4(b, __ldcg(reinterpret_cast<const float4*>(dr + k + 4)));
+      }
+      if (hr != nullptr) {
+        *reinterpret_cast<float4*>(hr + k) = a;
+        *reinterpret_cast<float4*>(hr + k + 4) = b;
+      }
+      float v = __fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(a.x, a.x), __fmul_rn(a.y, a.y)),
+                                    __fadd_rn(__fmul_rn(a.z, a.z), __fmul_rn(a.w, a.w))),
+                          __fadd_rn(__fadd_rn(__fmul_rn(b.x, b.x), __fmul_rn(b.y, b.y)),
+                                    __fadd_rn(__fmul_rn(b.z, b.z), __fmul_rn(b.w, b.w))));
+      bool placed = false;
+#pragma unroll
+      for (int l = 0; l < NORM_LEVELS; ++l) {
+        if (!placed) {
+          if ((c >> l) & 1) {
+            v = __fadd_rn(slot[l], v);
+          } else {
+            slot[l] = v;
+            placed = true;
+          }
+        }
+      }
+    }
+    bool have = false;
+#pragma unroll
+    for (int l = 0; l < NORM_LEVELS; ++l) {
+      if ((c >> l) & 1) {
+        seg = have ? __fadd_rn(slot[l], seg) : slot[l];
+        have = true;
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) seg = __fadd_rn(seg, __shfl_xor_sync(0xffffffffu, seg, o));
+  if (lane == 0) wsum[warp] = seg;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const float s = __fadd_rn(__fadd_rn(__fadd_rn(wsum[0], wsum[1]), __fadd_rn(wsum[2], wsum[3])),
+                              __fadd_rn(__fadd_rn(wsum[4], wsum[5]), __fadd_rn(wsum[6], wsum[7])));
+    const float ms = __fdiv_rn(s, (float)K);
+    rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+  }
+  __syncthreads();  // also makes this CTA's h stores visible to its pass 2
+  const float r = rs;
+
+  // pass 2: y = (h * r) * gamma, quantized; 8 lanes per block
+  const int sub = threadIdx.x & 7, grp = threadIdx.x >> 3;
+  const int64_t nb = K / QK;
+  for (int64_t b0 = 0; b0 < nb; b0 += NORM_THREADS / 8) {  // same trip count in every thread
+    const int64_t b = b0 + grp;
+    float4 v[1] = {make_float4(0.0f, 0.0f, 0.0f, 0.0f)};
+    if (b < nb) {
+      const int64_t k = b * QK + 4 * sub;
+      float4 h;
+      if (hr != nullptr) {
+        h = __ldcg(reinterpret_cast<const float4*>(hr + k));
+      } else {
+        h = __ldcg(reinterpret_cast<const float4*>(xr + k));
+        if (dr != nullptr) h = add4(h, __ldcg(reinterpret_cast<const float4*>(dr + k)));
+      }
+      const float4 g = __ldcg(reinterpret_cast<const float4*>(gamma + k));
+      v[0] = make_float4(__fmul_rn(__fmul_rn(h.x, r), g.x), __fmul_rn(__fmul_rn(h.y, r), g.y),
+                         __fmul_rn(__fmul_rn(h.z, r), g.z), __fmul_rn(__fmul_rn(h.w, r), g.w));
+    }
+    uint32_t w[1];
+    float d[1];
+    quantize_group8<1>(v, w, d);
+    if (b < nb) store_block_lane(out + (m * nb + b) * BLOCK_BYTES, sub, w[0], d[0]);
+  }
+}
+
+// ---- SwiGLU + quantization ----
+// e^x by a fixed single-precision procedure: Cody and Waite's reduction
+// x = n ln2 + r, ln2 split into 355/512 (9 significant bits: n * 355/512 is
+// exact for |n| <= 128) and the rest of ln2 rounded to single precision;
+// the Taylor polynomial of degree 7 of e^r in Horner form (|r| <= 0.35);
+// scaling by 2^n (exact).  Outside [-87, 88] the result is 0 or +infinity.
+constexpr float EXP_LOG2E = 0x1.715476p+0f;    // 1/ln 2, rounded
+constexpr float EXP_LN2_HI = 0x1.63p-1f;       // 355/512
+constexpr float EXP_LN2_LO = -0x1.bd0106p-13f; // ln 2 - 355/512, rounded
+constexpr float EXP_C3 = 0x1.555556p-3f;       // 1/3!
+constexpr float EXP_C4 = 0x1.555556p-5f;       // 1/4!
+constexpr float EXP_C5 = 0x1.111112p-7f;       // 1/5!
+constexpr float EXP_C6 = 0x1.6c16c2p-10f;      // 1/6!
+constexpr float EXP_C7 = 0x1.a01a02p-13f;      // 1/7!
+
+__device__ __forceinline__ float exp_cw(float x) {
+  if (x > 88.0f) return __int_as_float(0x7f800000);
+  if (x < -87.0f) return 0.0f;
+  const float n = rintf(__fmul_rn(x, EXP_LOG2E));
+  const float r = __fsub_rn(__fsub_rn(x, __fmul_rn(n, EXP_LN2_HI)), __fmul_rn(n, EXP_LN2_LO));
+  float p = EXP_C7;
+  p = __fadd_rn(__fmul_rn(p, r), EXP_C6);
+  p = __fadd_rn(__fmul_rn(p, r), EXP_C5);
+  p = __fadd_rn(__fmul_rn(p, r), EXP_C4);
+  p = __fadd_rn(__fmul_rn(p, r), EXP_C3);
+  p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));  // 2^n, -126 <= n <= 127
+}
+
+__device__ __forceinline__ float swiglu_one(float g, float u) {
+  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, exp_cw(-g))), u);
+}
+
+// gu is [M][2F] (gate = columns [0, F), up = [F, 2F)); block b of the output
+// (row b / nbr, block b % nbr) reads 32 gate and 32 up values.
+__global__ void __launch_bounds__(SWIGLU_THREADS)
+    swiglu_quant_kernel(const float* __restrict__ gu, int64_t F, int64_t nbr, int64_t total,
+                        uint8_t* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int sub = threadIdx.x & 7;
+  const int64_t grp = ((int64_t)blockIdx.x * SWIGLU_THREADS + threadIdx.x) >> 3;
+  const int64_t ngrp = ((int64_t)gridDim.x * SWIGLU_THREADS) >> 3;
+  for (int64_t b0 = 0; b0 < total; b0 += ngrp) {  // same trip count in every thread
+    const int64_t b = b0 + grp;
+    float4 v[1] = {make_float4(0.0f, 0.0f, 0.0f, 0.0f)};
+    if (b < total) {
+      const int64_t m = b / nbr, j = b - (b / nbr) * nbr;
+      const float* row = gu + m * 2 * F + j * QK + 4 * sub;
+      const float4 g = __ldcg(reinterpret_cast<const float4*>(row));
+      const float4 u = __ldcg(reinterpret_cast<const float4*>(row + F));
+      v[0] = make_float4(swiglu_one(g.x, u.x), swiglu_one(g.y, u.y), swiglu_one(g.z, u.z),
+                         swiglu_one(g.w, u.w));
+    }
+    uint32_t w[1];
+    float d[1];
+    quantize_group8<1>(v, w, d);
+    if (b < total) store_block_lane(out + b * BLOCK_BYTES, sub, w[0], d[0]);
+  }
+}
+
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, int threads, bool pdl, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+}  // namespace
+
+cudaError_t launch_rmsnorm_quantize(const float* x, const float* delta, const float* gamma, float eps,
+                                    int64_t M, int64_t K, float* h_out, uint8_t* out, bool pdl,
+                                    cudaStream_t s) {
+  return launch_pdl(rmsnorm_quant_kernel, dim3((unsigned)M), NORM_THREADS, pdl, s, x, delta, gamma, eps,
+                    K, h_out, out);
+}
+
+cudaError_t launch_swiglu_quantize(const float* gu, int64_t M, int64_t F, uint8_t* out, int sm_count,
+                                   bool pdl, cudaStream_t s) {
+  const int64_t nbr = F / QK;
+  const int64_t total = M * nbr;
+  const int64_t per_cta = SWIGLU_THREADS / 8;
+  int64_t grid = (total + per_cta - 1) / per_cta;
+  const int64_t cap = (int64_t)sm_count * 16;
+  if (grid > cap) grid = cap;
+  return launch_pdl(swiglu_quant_kernel, dim3((unsigned)grid), SWIGLU_THREADS, pdl, s, gu, F, nbr, total,
+                    out);
+}
+
+}  // namespace q8

@@ -88,6 +88,27 @@ def test_host_argument_checks_reject_before_any_device_work(lib):
     assert r(fake, 8, 40, fake, None) == -2
     assert lib.q8_block_dots(fake, 8, 64, fake, 1, odd, None) == -3
     assert lib.q8_unpack_weights(fake, 8, 64, None, None) == -1
+    n = lib.q8_residual_rmsnorm_quantize
+    assert n(None, None, fake, 1e-5, 1, 64, None, fake, 0, None) == -1          # null x
+    assert n(fake, None, None, 1e-5, 1, 64, None, fake, 0, None) == -1          # null gamma
+    assert n(fake, None, fake, 0.0, 1, 64, None, fake, 0, None) == -1           # eps = 0
+    assert n(fake, None, fake, float("nan"), 1, 64, None, fake, 0, None) == -1  # eps NaN
+    assert n(fake, None, fake, float("inf"), 1, 64, None, fake, 0, None) == -1  # eps inf
+    assert n(fake, None, fake, 1e-5, 1, 48, None, fake, 0, None) == -2          # K % 32
+    assert n(fake, None, fake, 1e-5, 0, 64, None, fake, 0, None) == -2          # M = 0
+    assert n(fake, None, fake, 1e-5, 1, (1 << 24) + 32, None, fake, 0, None) == -2  # K too large
+    eight = ctypes.c_void_p(0x10008)
+    assert n(eight, None, fake, 1e-5, 1, 64, None, fake, 0, None) == -3         # x 8-aligned only
+    assert n(fake, eight, fake, 1e-5, 1, 64, None, fake, 0, None) == -3         # delta
+    assert n(fake, None, fake, 1e-5, 1, 64, eight, fake, 0, None) == -3         # h_out
+    assert n(fake, None, fake, 1e-5, 1, 64, None, odd, 0, None) == -3           # out odd
+    s = lib.q8_swiglu_quantize
+    assert s(None, 1, 64, fake, 0, None) == -1
+    assert s(fake, 1, 64, fake, 2, None) == -1                                  # unknown flag
+    assert s(fake, 1, 48, fake, 0, None) == -2
+    assert s(fake, 0, 64, fake, 0, None) == -2
+    assert s(eight, 1, 64, fake, 0, None) == -3
+    assert s(fake, 1, 64, odd, 0, None) == -3
 
 
 def test_no_device_means_an_error_not_a_fallback(lib):
