@@ -240,6 +240,7 @@ def run_ours(args):
     e2e_value = aggregate_gbs(bytes_step, world, ms_e2e)
 
     roof = roofline(st, q8) if rank == 0 else None
+    prod = producers(q8, shape) if (rank == 0 and not args.no_producers) else None
     peak, peak_kind = _peaks()
     if rank == 0:
         cpu = cpu_baseline(shape, args.M) if (world == 1 and not args.no_cpu) else None
@@ -259,6 +260,7 @@ def run_ours(args):
             "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
             "hbm_peak_gbs": peak, "hbm_peak_kind": peak_kind,
             "roofline": roof,
+            "producers": prod,
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
                     "h2d_bytes_per_step": st.x_all.numel() * 4,
@@ -387,6 +389,94 @@ def roofline(st, q8, reps=3):
                         for t, k, b, nn, _ in rows}}
 
 
+def producers(q8, shape, launches=20):
+    """The fused producers that emit a GEMV's activation blocks (residual add
+    + RMSNorm + quantization, SwiGLU + quantization), measured beside the
+    step: at the step's decode shape (one token: K = hidden, F = ffn; a graph
+    of `launches` launches chained with PDL, time per launch) and at a row
+    count whose data is several times L2 (plain launches; achieved =
+    algorithmic bytes / time against the measured HBM peak).  The oracle's
+    single-thread time for the decode shape is reported beside them."""
+    import numpy as np
+    import torch
+
+    import oracle
+    import q8_synth
+    peak, kind = _peaks()
+    K, F = shape.hidden, shape.ffn
+    dev = "cuda"
+
+    def timed(fn, pdl):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn(0)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(launches):
+                fn(q8.FLAG_PDL if pdl else 0)
+        g.replay()
+        torch.cuda.synchronize()
+        cur = torch.cuda.current_stream()
+        best = None
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(cur)
+            g.replay()
+            b.record(cur)
+            b.synchronize()
+            best = a.elapsed_time(b) if best is None else min(best, a.elapsed_time(b))
+        del g
+        return best * 1e3 / launches  # us per launch
+
+    def oracle_us(fn):
+        n, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < 0.3:
+            fn()
+            n += 1
+        return (time.perf_counter() - t0) * 1e6 / n
+
+    out = {}
+    # residual add + RMSNorm + quantization, in place on the residual stream
+    gamma = q8_synth.normal_torch((K,), 0.1, 1, dev) + 1.0
+    rows = {}
+    for label, M in (("decode", 1), ("bulk", 16384)):
+        x = q8_synth.normal_torch((M, K), 1.0, 2, dev)
+        d = q8_synth.normal_torch((M, K), 0.01, 3, dev)
+        blocks = q8.empty_blocks(M, K)
+        us = timed(lambda f: q8.q8_residual_rmsnorm_quantize(x, gamma, 1e-5, blocks, delta=d,
+                                                              h_out=x, flags=f), label == "decode")
+        nbytes = M * K * 4 * 3 + K * 4 + blocks.numel()  # x, delta, h in place, gamma, blocks
+        gbs = nbytes / (us * 1e-6) / 1e9
+        rows[label] = {"M": M, "K": K, "us": round(us, 3), "bytes": nbytes, "GB/s": round(gbs, 1)}
+        if label == "bulk":
+            rows[label].update({"peak": peak, "peak_kind": kind, "frac": round(gbs / peak, 4)})
+        del x, d, blocks
+    xo = q8_synth.normal_np((1, K), 1.0, 4)
+    do = q8_synth.normal_np((1, K), 0.01, 5)
+    go = (1.0 + q8_synth.normal_np((K,), 0.1, 6)).astype(np.float32)
+    rows["oracle_us_decode"] = round(oracle_us(lambda: oracle.residual_rmsnorm_quantize(xo, do, go, 1e-5)), 2)
+    out["residual_rmsnorm_quantize"] = rows
+    # SwiGLU + quantization
+    rows = {}
+    for label, M in (("decode", 1), ("bulk", 8192)):
+        gu = q8_synth.normal_torch((M, 2 * F), 1.0, 7, dev)
+        blocks = q8.empty_blocks(M, F)
+        us = timed(lambda f: q8.q8_swiglu_quantize(gu, blocks, flags=f), label == "decode")
+        nbytes = M * 2 * F * 4 + blocks.numel()
+        gbs = nbytes / (us * 1e-6) / 1e9
+        rows[label] = {"M": M, "F": F, "us": round(us, 3), "bytes": nbytes, "GB/s": round(gbs, 1)}
+        if label == "bulk":
+            rows[label].update({"peak": peak, "peak_kind": kind, "frac": round(gbs / peak, 4)})
+        del gu, blocks
+    guo = q8_synth.normal_np((1, 2 * F), 1.0, 8)
+    rows["oracle_us_decode"] = round(oracle_us(lambda: oracle.swiglu_quantize(guo, F)), 2)
+    out["swiglu_quantize"] = rows
+    torch.cuda.empty_cache()
+    return out
+
+
 # ---------------------------------------------------------------------------
 # reference arm: the oracle on the host cores
 # ---------------------------------------------------------------------------
@@ -457,6 +547,7 @@ def main():
     ap.add_argument("--mode", choices=["shared", "fused", "unfused"], default="fused")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--no-producers", action="store_true", help="skip the fused-producer measurements")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -159,6 +159,86 @@ __global__ void __launch_bounds__(NORM_THREADS)
   }
 }
 
+// Rows of K <= 8192 (P <= 8192 leaves): the same tree with coalesced loads
+// and h kept in registers.  Thread t holds the float4 groups f = t + 256 j,
+// j < J = max(1, P / 1024): a group's 4 leaves are a subtree, a warp's 32
+// consecutive groups (butterfly) one of 128 leaves, the CTA's 256 groups of
+// index j (tree over the 8 warps) one of 1024 leaves, and the J of those
+// meet in a pairwise tree.  In pass 2 the 8 lanes that hold a block's
+// 8 groups are the 8 consecutive lanes of a quantization group.
+template <int J>
+__global__ void __launch_bounds__(NORM_THREADS)
+    rmsnorm_quant_reg_kernel(const float* x, const float* delta, const float* __restrict__ gamma, float eps,
+                             int64_t K, float* h_out, uint8_t* __restrict__ out) {
+  // h_out may be x or delta (an in-place residual update): no restrict on them
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ float wsum[J][NORM_THREADS / 32];
+  __shared__ float rs;
+  const int64_t m = blockIdx.x;
+  const float* xr = x + m * K;
+  const float* dr = delta != nullptr ? delta + m * K : nullptr;
+  float* hr = h_out != nullptr ? h_out + m * K : nullptr;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float4 v[J];
+  float part[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int64_t k = 4 * ((int64_t)threadIdx.x + NORM_THREADS * j);
+    v[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (k < K) {
+      v[j] = __ldcg(reinterpret_cast<const float4*>(xr + k));
+      if (dr != nullptr) v[j] = add4(v[j], __ldcg(reinterpret_cast<const float4*>(dr + k)));
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int64_t k = 4 * ((int64_t)threadIdx.x + NORM_THREADS * j);
+    if (hr != nullptr && k < K) *reinterpret_cast<float4*>(hr + k) = v[j];
+    part[j] = __fadd_rn(__fadd_rn(__fmul_rn(v[j].x, v[j].x), __fmul_rn(v[j].y, v[j].y)),
+                        __fadd_rn(__fmul_rn(v[j].z, v[j].z), __fmul_rn(v[j].w, v[j].w)));
+  }
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1)
+#pragma unroll
+    for (int j = 0; j < J; ++j) part[j] = __fadd_rn(part[j], __shfl_xor_sync(0xffffffffu, part[j], o));
+  if (lane == 0)
+#pragma unroll
+    for (int j = 0; j < J; ++j) wsum[j][warp] = part[j];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+      t[j] = __fadd_rn(__fadd_rn(__fadd_rn(wsum[j][0], wsum[j][1]), __fadd_rn(wsum[j][2], wsum[j][3])),
+                       __fadd_rn(__fadd_rn(wsum[j][4], wsum[j][5]), __fadd_rn(wsum[j][6], wsum[j][7])));
+#pragma unroll
+    for (int w = J; w > 1; w >>= 1)
+#pragma unroll
+      for (int j = 0; j < w / 2; ++j) t[j] = __fadd_rn(t[2 * j], t[2 * j + 1]);
+    const float ms = __fdiv_rn(t[0], (float)K);
+    rs = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(ms, eps)));
+  }
+  __syncthreads();
+  const float r = rs;
+  const int sub = threadIdx.x & 7;
+  const int64_t nb = K / QK;
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int64_t f = (int64_t)threadIdx.x + NORM_THREADS * j;  // block f / 8, lane f % 8 = sub
+    float4 y[1] = {make_float4(0.0f, 0.0f, 0.0f, 0.0f)};
+    if (4 * f < K) {
+      const float4 g = __ldcg(reinterpret_cast<const float4*>(gamma + 4 * f));
+      y[0] = make_float4(__fmul_rn(__fmul_rn(v[j].x, r), g.x), __fmul_rn(__fmul_rn(v[j].y, r), g.y),
+                         __fmul_rn(__fmul_rn(v[j].z, r), g.z), __fmul_rn(__fmul_rn(v[j].w, r), g.w));
+    }
+    uint32_t w[1];
+    float d[1];
+    quantize_group8<1>(y, w, d);
+    if (4 * f < K) store_block_lane(out + (m * nb + f / 8) * BLOCK_BYTES, sub, w[0], d[0]);
+  }
+}
+
 // ---- SwiGLU + quantization ----
 // e^x by a fixed single-precision procedure: Cody and Waite's reduction
 // x = n ln2 + r, ln2 split into 355/512 (9 significant bits: n * 355/512 is
@@ -195,7 +275,10 @@ __device__ __forceinline__ float swiglu_one(float g, float u) {
 }
 
 // gu is [M][2F] (gate = columns [0, F), up = [F, 2F)); block b of the output
-// (row b / nbr, block b % nbr) reads 32 gate and 32 up values.
+// (row b / nbr, block b % nbr) reads 32 gate and 32 up values.  A group of 8
+// lanes takes SWIGLU_B blocks per pass (two measured slower: the kernel is
+// bound by the arithmetic of the exact e^x and division, not by latency).
+constexpr int SWIGLU_B = 1;
 __global__ void __launch_bounds__(SWIGLU_THREADS)
     swiglu_quant_kernel(const float* __restrict__ gu, int64_t F, int64_t nbr, int64_t total,
                         uint8_t* __restrict__ out) {
@@ -204,21 +287,31 @@ __global__ void __launch_bounds__(SWIGLU_THREADS)
   const int sub = threadIdx.x & 7;
   const int64_t grp = ((int64_t)blockIdx.x * SWIGLU_THREADS + threadIdx.x) >> 3;
   const int64_t ngrp = ((int64_t)gridDim.x * SWIGLU_THREADS) >> 3;
-  for (int64_t b0 = 0; b0 < total; b0 += ngrp) {  // same trip count in every thread
-    const int64_t b = b0 + grp;
-    float4 v[1] = {make_float4(0.0f, 0.0f, 0.0f, 0.0f)};
-    if (b < total) {
-      const int64_t m = b / nbr, j = b - (b / nbr) * nbr;
-      const float* row = gu + m * 2 * F + j * QK + 4 * sub;
-      const float4 g = __ldcg(reinterpret_cast<const float4*>(row));
-      const float4 u = __ldcg(reinterpret_cast<const float4*>(row + F));
-      v[0] = make_float4(swiglu_one(g.x, u.x), swiglu_one(g.y, u.y), swiglu_one(g.z, u.z),
-                         swiglu_one(g.w, u.w));
+  for (int64_t b0 = 0; b0 < total; b0 += ngrp * SWIGLU_B) {  // same trip count in every thread
+    float4 g[SWIGLU_B], u[SWIGLU_B], v[SWIGLU_B];
+#pragma unroll
+    for (int q = 0; q < SWIGLU_B; ++q) {
+      const int64_t b = b0 + grp + q * ngrp;
+      g[q] = u[q] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      if (b < total) {
+        const int64_t m = b / nbr, j = b - (b / nbr) * nbr;
+        const float* row = gu + m * 2 * F + j * QK + 4 * sub;
+        g[q] = __ldcg(reinterpret_cast<const float4*>(row));
+        u[q] = __ldcg(reinterpret_cast<const float4*>(row + F));
+      }
     }
-    uint32_t w[1];
-    float d[1];
-    quantize_group8<1>(v, w, d);
-    if (b < total) store_block_lane(out + b * BLOCK_BYTES, sub, w[0], d[0]);
+#pragma unroll
+    for (int q = 0; q < SWIGLU_B; ++q)
+      v[q] = make_float4(swiglu_one(g[q].x, u[q].x), swiglu_one(g[q].y, u[q].y), swiglu_one(g[q].z, u[q].z),
+                         swiglu_one(g[q].w, u[q].w));
+    uint32_t w[SWIGLU_B];
+    float d[SWIGLU_B];
+    quantize_group8<SWIGLU_B>(v, w, d);
+#pragma unroll
+    for (int q = 0; q < SWIGLU_B; ++q) {
+      const int64_t b = b0 + grp + q * ngrp;
+      if (b < total) store_block_lane(out + b * BLOCK_BYTES, sub, w[q], d[q]);
+    }
   }
 }
 
@@ -241,15 +334,24 @@ cudaError_t launch_pdl(Kern kern, dim3 grid, int threads, bool pdl, cudaStream_t
 cudaError_t launch_rmsnorm_quantize(const float* x, const float* delta, const float* gamma, float eps,
                                     int64_t M, int64_t K, float* h_out, uint8_t* out, bool pdl,
                                     cudaStream_t s) {
-  return launch_pdl(rmsnorm_quant_kernel, dim3((unsigned)M), NORM_THREADS, pdl, s, x, delta, gamma, eps,
-                    K, h_out, out);
+  int64_t P = 1;
+  while (P < K) P <<= 1;
+  const dim3 grid((unsigned)M);
+  switch (P <= 1024 ? 1 : P / 1024) {
+    case 1: return launch_pdl(rmsnorm_quant_reg_kernel<1>, grid, NORM_THREADS, pdl, s, x, delta, gamma, eps, K, h_out, out);
+    case 2: return launch_pdl(rmsnorm_quant_reg_kernel<2>, grid, NORM_THREADS, pdl, s, x, delta, gamma, eps, K, h_out, out);
+    case 4: return launch_pdl(rmsnorm_quant_reg_kernel<4>, grid, NORM_THREADS, pdl, s, x, delta, gamma, eps, K, h_out, out);
+    case 8: return launch_pdl(rmsnorm_quant_reg_kernel<8>, grid, NORM_THREADS, pdl, s, x, delta, gamma, eps, K, h_out, out);
+    default:  // K > 8192: thread segments, h read again in pass 2
+      return launch_pdl(rmsnorm_quant_kernel, grid, NORM_THREADS, pdl, s, x, delta, gamma, eps, K, h_out, out);
+  }
 }
 
 cudaError_t launch_swiglu_quantize(const float* gu, int64_t M, int64_t F, uint8_t* out, int sm_count,
                                    bool pdl, cudaStream_t s) {
   const int64_t nbr = F / QK;
   const int64_t total = M * nbr;
-  const int64_t per_cta = SWIGLU_THREADS / 8;
+  const int64_t per_cta = SWIGLU_THREADS / 8 * SWIGLU_B;
   int64_t grid = (total + per_cta - 1) / per_cta;
   const int64_t cap = (int64_t)sm_count * 16;
   if (grid > cap) grid = cap;
