@@ -190,7 +190,7 @@ def run_ours(args):
     from q8_block_quantized_gb300.stack import Q8Stack
 
     shape = q8_synth.LLAMA_3B if args.model == "3b" else q8_synth.LLAMA_1B
-    st = Q8Stack(shape, M=args.M, mode=args.mode, layers=args.layers, seed=rank)
+    st = Q8Stack(shape, M=args.M, mode=args.mode, layers=args.layers, seed=rank, tcgen05=args.tcgen05)
     graph = st.capture()
     stream = torch.cuda.current_stream()
     bytes_step = st.bytes_per_step()
@@ -241,6 +241,7 @@ def run_ours(args):
 
     roof = roofline(st, q8) if rank == 0 else None
     prod = producers(q8, shape) if (rank == 0 and not args.no_producers) else None
+    tc5 = tcgen05_vs_default(q8, st) if (rank == 0 and world == 1 and not args.no_producers) else None
     peak, peak_kind = _peaks()
     if rank == 0:
         cpu = cpu_baseline(shape, args.M) if (world == 1 and not args.no_cpu) else None
@@ -255,12 +256,14 @@ def run_ours(args):
                 "weight_bytes_per_step": st.weight_bytes(),
                 "l2": "no flush: each step streams %.2f GB > 129 MB L2" % (bytes_step / 1e9),
                 "graph": True, "pdl": True, "parallelism": "replicas" if world > 1 else "single",
+                "tcgen05": bool(args.tcgen05),
             },
             "tok_s": round(args.M * world / (ms_max * 1e-3), 1),
             "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
             "hbm_peak_gbs": peak, "hbm_peak_kind": peak_kind,
             "roofline": roof,
             "producers": prod,
+            "tcgen05_vs_default": tc5,
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
                     "h2d_bytes_per_step": st.x_all.numel() * 4,
@@ -477,6 +480,40 @@ def producers(q8, shape, launches=20):
     return out
 
 
+def tcgen05_vs_default(q8, st, M=16, steps=100):
+    """The step at 16 activation rows with the default kernels and with
+    Q8_FLAG_TCGEN05 (tcgen05 block dots on the 128-row tiles: gate/up and the
+    LM head), same weights and inputs: time per step of each (CUDA events over
+    graph replays) and whether the outputs are bitwise equal."""
+    import torch
+
+    from q8_block_quantized_gb300.stack import Q8Stack
+    res = {"M": M}
+    outs = {}
+    for label, flag in (("default", False), ("tcgen05", True)):
+        s2 = Q8Stack(st.shape, M=M, mode="fused", layers=st.n_layers, shared_weights=st.weights,
+                     tcgen05=flag)
+        g = s2.capture()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        cur = torch.cuda.current_stream()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        for _ in range(steps):
+            g.replay()
+        b.record(cur)
+        b.synchronize()
+        ms = a.elapsed_time(b) / steps
+        res[label] = {"ms_per_step": round(ms, 5),
+                      "GB/s": round(s2.bytes_per_step() / (ms * 1e-3) / 1e9, 1)}
+        outs[label] = s2.y_all.clone()
+        del g, s2
+    res["bitwise_equal"] = bool(torch.equal(outs["default"], outs["tcgen05"]))
+    torch.cuda.empty_cache()
+    return res
+
+
 # ---------------------------------------------------------------------------
 # reference arm: the oracle on the host cores
 # ---------------------------------------------------------------------------
@@ -547,7 +584,10 @@ def main():
     ap.add_argument("--mode", choices=["shared", "fused", "unfused"], default="fused")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
-    ap.add_argument("--no-producers", action="store_true", help="skip the fused-producer measurements")
+    ap.add_argument("--no-producers", action="store_true",
+                    help="skip the fused-producer and tcgen05-variant measurements")
+    ap.add_argument("--tcgen05", action="store_true",
+                    help="GEMV calls with Q8_FLAG_TCGEN05 (tcgen05 block dots where they apply)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -74,6 +74,8 @@ extern "C" {
 /* Flags for the compute calls. */
 #define Q8_FLAG_PDL 1u      /* launch as a programmatic dependent of the
                                previous work on the stream (see q8_gemm)     */
+#define Q8_FLAG_TCGEN05 2u  /* q8_gemm / q8_fused_quant_gemm: block dots on
+                               the tcgen05 tensor cores (see q8_gemm)        */
 
 typedef enum q8_status {
     Q8_OK = 0,
@@ -235,6 +237,15 @@ Q8_API int q8_repack_weights(const void *src_blocks, int64_t N, int64_t K, void 
  *             starts streaming W before that work has finished; it waits for
  *             it before reading A_blocks or writing y/workspace.  The caller
  *             promises that no unfinished earlier work on the stream writes W.
+ *             Q8_FLAG_TCGEN05 (alone or with Q8_FLAG_PDL): on matrices packed
+ *             in 128-row tiles, passes of 9-16 activation rows compute their
+ *             block dots with tcgen05 MMAs (int8 converted exactly to fp16,
+ *             fp32 accumulators in tensor memory, one per block) instead of
+ *             the default mma.sync tensor path; other shapes ignore it.  The
+ *             result is bitwise the same.  It is measured slower on GB300
+ *             (each round converts the weights to fp16 in shared memory and
+ *             reads every block's accumulator back from tensor memory, one
+ *             step after the other) and kept for comparison.
  */
 Q8_API int q8_gemm(const void *W, int64_t N, int64_t K, const void *A_blocks, int M,
             float *y, void *workspace, size_t workspace_bytes, unsigned flags,

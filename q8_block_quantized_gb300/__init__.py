@@ -25,6 +25,7 @@ MAX_M = 64
 MAX_TILE_ROWS = 128
 CHUNK_BLOCKS = 8
 FLAG_PDL = 1
+FLAG_TCGEN05 = 2
 
 STATUS = {0: "Q8_OK", -1: "Q8_EINVAL", -2: "Q8_ESHAPE", -3: "Q8_EALIGN", -4: "Q8_EDEVICE",
           -5: "Q8_ECUDA", -6: "Q8_EWORKSPACE", -7: "Q8_ETIMEOUT", -8: "Q8_ESCRATCH"}

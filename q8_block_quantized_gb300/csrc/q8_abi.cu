@@ -58,7 +58,7 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? Q8_OK : Q8_ECUDA; }
 
 int check_gemm_common(const void* W, int64_t N, int64_t K, int M, const float* y, unsigned flags) {
   if (W == nullptr || y == nullptr) return Q8_EINVAL;
-  if ((flags & ~Q8_FLAG_PDL) != 0) return Q8_EINVAL;
+  if ((flags & ~(Q8_FLAG_PDL | Q8_FLAG_TCGEN05)) != 0) return Q8_EINVAL;
   if (N <= 0 || N > INT32_MAX || !k_ok(K) || M < 1 || M > Q8_MAX_M) return Q8_ESHAPE;
   if (!aligned(W, 16) || !aligned(y, 4)) return Q8_EALIGN;
   return Q8_OK;
@@ -105,9 +105,14 @@ size_t q8_workspace_bytes(int64_t N, int64_t K, int M) {
   if (N <= 0 || N > INT32_MAX || !k_ok(K) || M < 1 || M > Q8_MAX_M) return 0;
   DeviceInfo d;
   if (device_ok(&d) != Q8_OK) return 0;
-  GemvPlan p, pf;
-  if (!plan_gemv(d, N, K, M, false, &p) || !plan_gemv(d, N, K, M, true, &pf)) return 0;
-  return p.ws_bytes > pf.ws_bytes ? p.ws_bytes : pf.ws_bytes;
+  // the largest need over the kernel variants a call may pick
+  size_t most = 0;
+  for (int v = 0; v < 4; ++v) {
+    GemvPlan p;
+    if (!plan_gemv(d, N, K, M, (v & 1) != 0, (v & 2) != 0, &p)) return 0;
+    if (p.ws_bytes > most) most = p.ws_bytes;
+  }
+  return most;
 }
 
 int q8_quantize_act(const float* x, int64_t M, int64_t K, void* out_blocks, unsigned flags,
@@ -153,7 +158,7 @@ int q8_gemm(const void* W, int64_t N, int64_t K, const void* A_blocks, int M, fl
   DeviceInfo d;
   if ((st = device_ok(&d)) != Q8_OK) return st;
   GemvPlan p;
-  if (!plan_gemv(d, N, K, M, false, &p)) return Q8_ESHAPE;
+  if (!plan_gemv(d, N, K, M, false, (flags & Q8_FLAG_TCGEN05) != 0, &p)) return Q8_ESHAPE;
   if ((st = check_workspace(p, workspace, workspace_bytes)) != Q8_OK) return st;
   return cuda_status(launch_gemv(p, static_cast<const uint8_t*>(W), static_cast<const uint8_t*>(A_blocks),
                                  nullptr, nullptr, y, workspace, (flags & Q8_FLAG_PDL) != 0,
@@ -170,7 +175,7 @@ int q8_fused_quant_gemm(const void* W, int64_t N, int64_t K, const float* x, int
   DeviceInfo d;
   if ((st = device_ok(&d)) != Q8_OK) return st;
   GemvPlan p;
-  if (!plan_gemv(d, N, K, M, true, &p)) return Q8_ESHAPE;
+  if (!plan_gemv(d, N, K, M, true, (flags & Q8_FLAG_TCGEN05) != 0, &p)) return Q8_ESHAPE;
   if ((st = check_workspace(p, workspace, workspace_bytes)) != Q8_OK) return st;
   return cuda_status(launch_gemv(p, static_cast<const uint8_t*>(W), nullptr, x,
                                  static_cast<uint8_t*>(A_blocks_out), y, workspace,

@@ -11,12 +11,12 @@
 namespace q8 {
 
 template <int R>
-cudaError_t launch_gemv_r(const GemvArgs& args, int MT, bool fused, int grid, int cluster, bool pdl,
+cudaError_t launch_gemv_r(const GemvArgs& args, int MT, bool fused, bool u5, int grid, int cluster, bool pdl,
                          cudaStream_t s);
 template <int R>
-int occupancy_r(int MT, bool fused);
+int occupancy_r(int MT, bool fused, bool u5);
 template <int R>
-bool cluster_fits_r(int MT, bool fused, int cluster);
+bool cluster_fits_r(int MT, bool fused, bool u5, int cluster);
 
 namespace {
 
@@ -38,31 +38,31 @@ cudaError_t error_word(int dev, unsigned** out) {
   return cudaSuccess;
 }
 
-int occupancy(int R, int MT, bool fused) {
+int occupancy(int R, int MT, bool fused, bool u5) {
   switch (R) {
-    case 16: return occupancy_r<16>(MT, fused);
-    case 32: return occupancy_r<32>(MT, fused);
-    case 64: return occupancy_r<64>(MT, fused);
-    default: return occupancy_r<128>(MT, fused);
+    case 16: return occupancy_r<16>(MT, fused, u5);
+    case 32: return occupancy_r<32>(MT, fused, u5);
+    case 64: return occupancy_r<64>(MT, fused, u5);
+    default: return occupancy_r<128>(MT, fused, u5);
   }
 }
 
 // cluster feasibility per (R, MT, fused, size), cached
 std::mutex g_cl_mu;
-signed char g_cl_cache[4][5][2][4];  // 0 unknown, 1 fits, -1 does not
-bool cluster_fits(int R, int MT, bool fused, int c) {
+signed char g_cl_cache[4][5][2][2][4];  // 0 unknown, 1 fits, -1 does not
+bool cluster_fits(int R, int MT, bool fused, bool u5, int c) {
   const int ri = R == 16 ? 0 : R == 32 ? 1 : R == 64 ? 2 : 3;
   const int mi = MT == 1 ? 0 : MT == 2 ? 1 : MT == 4 ? 2 : MT == 8 ? 3 : 4;
   const int ci = c == 2 ? 0 : c == 4 ? 1 : c == 8 ? 2 : 3;
   std::lock_guard<std::mutex> lk(g_cl_mu);
-  signed char& v = g_cl_cache[ri][mi][fused ? 1 : 0][ci];
+  signed char& v = g_cl_cache[ri][mi][fused ? 1 : 0][u5 ? 1 : 0][ci];
   if (v == 0) {
     bool ok;
     switch (R) {
-      case 16: ok = cluster_fits_r<16>(MT, fused, c); break;
-      case 32: ok = cluster_fits_r<32>(MT, fused, c); break;
-      case 64: ok = cluster_fits_r<64>(MT, fused, c); break;
-      default: ok = cluster_fits_r<128>(MT, fused, c); break;
+      case 16: ok = cluster_fits_r<16>(MT, fused, u5, c); break;
+      case 32: ok = cluster_fits_r<32>(MT, fused, u5, c); break;
+      case 64: ok = cluster_fits_r<64>(MT, fused, u5, c); break;
+      default: ok = cluster_fits_r<128>(MT, fused, u5, c); break;
     }
     v = ok ? 1 : -1;
   }
@@ -79,7 +79,8 @@ int stage_target_of(int MT) {
     default: return MCfg<16>::STAGE_TARGET;
   }
 }
-int budget_of(int MT) {
+int budget_of(int R, int MT, bool u5) {
+  if (u5 && R == 128 && MT == 16) return act_budget<128, 16, true>();  // the tcgen05 path's smaller area
   switch (MT) {
     case 1: return MCfg<1>::ACT_BUDGET;
     case 2: return MCfg<2>::ACT_BUDGET;
@@ -91,7 +92,7 @@ int budget_of(int MT) {
 
 }  // namespace
 
-bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, GemvPlan* out) {
+bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, bool tcgen05, GemvPlan* out) {
   GemvPlan q;
   q.N = N;
   q.K = K;
@@ -106,13 +107,15 @@ bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, G
   if (T > ((int64_t)1 << 30) || nch > ((int64_t)1 << 24)) return false;
   q.T = (int)T;
   q.nch = (int)nch;
-  if (occupancy(q.R, q.MT, fused) < 1) return false;  // also sets the smem attribute
+  // the tcgen05 kernel serves 128-row tiles with 16 rows per pass
+  q.u5 = tcgen05 && q.R == 128 && q.MT == 16;
+  if (occupancy(q.R, q.MT, fused, q.u5) < 1) return false;  // also sets the smem attribute
   // rounds of P chunks; a unit is RU rounds (a power of two)
   const int64_t nrounds_all = (nch + P - 1) / P;
   int64_t ru = 1;
   while (ru < nrounds_all && ru < MAX_ROUNDS_PER_UNIT) ru <<= 1;
   // sized for MT rows: the kernel's reduction depth is fixed by MT, not M
-  const int budget = budget_of(q.MT);
+  const int budget = budget_of(q.R, q.MT, q.u5);
   while (ru > 1 && act_bytes(q.MT, P, (int)ru) > budget) ru >>= 1;
   if (act_bytes(q.MT, P, (int)ru) > budget) return false;
   int64_t S = (nrounds_all + ru - 1) / ru;
@@ -152,7 +155,7 @@ bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, G
     const int target = stage_target_of(q.MT);
     while (want < cmax && (blocks + want - 1) / want > target) want <<= 1;
     for (int c = want; c >= 2; c >>= 1) {
-      if (q.grid >= c && cluster_fits(q.R, q.MT, fused, c)) {
+      if (q.grid >= c && cluster_fits(q.R, q.MT, fused, q.u5, c)) {
         q.cluster = c;
         q.grid = q.grid / c * c;
         break;
@@ -204,10 +207,10 @@ cudaError_t launch_gemv(const GemvPlan& p, const uint8_t* W, const uint8_t* A, c
     // short K range does not reserve the whole budget)
     args.act_smem = (act_bytes(MT, 128 / p.R, p.RU) + 15) / 16 * 16;
     switch (p.R) {
-      case 16: e = launch_gemv_r<16>(args, MT, fused, p.grid, p.cluster, pdl, s); break;
-      case 32: e = launch_gemv_r<32>(args, MT, fused, p.grid, p.cluster, pdl, s); break;
-      case 64: e = launch_gemv_r<64>(args, MT, fused, p.grid, p.cluster, pdl, s); break;
-      default: e = launch_gemv_r<128>(args, MT, fused, p.grid, p.cluster, pdl, s); break;
+      case 16: e = launch_gemv_r<16>(args, MT, fused, p.u5 && MT == 16, p.grid, p.cluster, pdl, s); break;
+      case 32: e = launch_gemv_r<32>(args, MT, fused, p.u5 && MT == 16, p.grid, p.cluster, pdl, s); break;
+      case 64: e = launch_gemv_r<64>(args, MT, fused, p.u5 && MT == 16, p.grid, p.cluster, pdl, s); break;
+      default: e = launch_gemv_r<128>(args, MT, fused, p.u5 && MT == 16, p.grid, p.cluster, pdl, s); break;
     }
     if (e != cudaSuccess) return e;
   }

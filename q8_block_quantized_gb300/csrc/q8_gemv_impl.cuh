@@ -111,6 +111,28 @@ struct MCfg {
 // Activation rows at or above this use the tensor-core path.
 constexpr int TC_MIN_MT = 8;
 
+// 5th-generation tensor-core path (tcgen05), selected per call (U5): tiles
+// of 128 rows (one chunk per round) with 16 activation rows.  Each round the consumer warps convert
+// the chunk's int8 weights and the round's activation blocks exactly to fp16
+// in the MMA's canonical layout (no swizzle, K-major: core matrices of 8 rows
+// x 16 bytes, 128 bytes apart along k, 256 bytes apart along rows), one
+// thread issues two 128 x 16 x 16 MMAs per block into tensor memory (a fresh
+// fp32 accumulator per block: every partial sum is an integer below 2^24, so
+// it holds the exact block dot), and the consumers read the block dots back
+// for the canonical terms and trees.
+template <int R, int MT, bool U5>
+struct UCfg {
+  static constexpr bool ON = U5 && R == 128 && MT == 16;
+  static constexpr int SLICE_A = 128 * 16 * 2;  // one 16-wide k slice of the 128 weight rows, fp16
+  static constexpr int SLICE_B = MT * 16 * 2;   // the same slice of the activation rows
+  static constexpr int A_BYTES = ON ? 2 * CHUNK_BLOCKS * SLICE_A : 0;
+  static constexpr int B_BYTES = ON ? 2 * CHUNK_BLOCKS * SLICE_B : 0;
+  static constexpr int TMEM_COLS = CHUNK_BLOCKS * MT;  // block j's dots in columns [MT j, MT j + MT)
+  static constexpr int MISC_INTS = ON ? 8 : 4;         // + the MMA mbarrier and the TMEM base
+};
+// dynamic shared memory a CTA may use on sm_103 (227 KB)
+constexpr int SMEM_LIMIT = 232448;
+
 // activation bytes of one unit (RU rounds of P chunks) in shared memory,
 // laid out for MT rows: quants [MT][blocks][32] (on the tensor path with 16
 // bytes of padding per row, so its loads of 8 rows hit distinct banks), then
@@ -122,10 +144,20 @@ __host__ __device__ constexpr int act_bytes(int MT, int P, int RU) {
   return MT * act_row_bytes(MT, P * RU * CHUNK_BLOCKS) + MT * P * RU * CHUNK_BLOCKS * 2;
 }
 
-template <int R, int MT>
+// bytes of staged activations a unit may use: MCfg's budget, or on the
+// tcgen05 path what the stages and the fp16 operands leave of SMEM_LIMIT
+template <int R, int MT, bool U5>
+__host__ __device__ constexpr int act_budget() {
+  return UCfg<R, MT, U5>::ON
+             ? (SMEM_LIMIT - MCfg<MT>::STAGES * RCfg<R>::STAGE_BYTES - UCfg<R, MT, U5>::A_BYTES -
+                UCfg<R, MT, U5>::B_BYTES - 2 * MCfg<MT>::STAGES * 8 - UCfg<R, MT, U5>::MISC_INTS * 4) / 16 * 16
+             : MCfg<MT>::ACT_BUDGET;
+}
+
+template <int R, int MT, bool U5>
 __host__ __device__ constexpr int ru_max() {
   int c = MAX_ROUNDS_PER_UNIT;
-  while (c > 1 && act_bytes(MT, RCfg<R>::P, c) > MCfg<MT>::ACT_BUDGET) c >>= 1;
+  while (c > 1 && act_bytes(MT, RCfg<R>::P, c) > act_budget<R, MT, U5>()) c >>= 1;
   return c;
 }
 __host__ __device__ constexpr int log2_floor(int v) { return v <= 1 ? 0 : 1 + log2_floor(v >> 1); }
@@ -140,17 +172,17 @@ constexpr int red_stride() {
 // per-round exchange of chunk values between the parts of a row (and, on
 // the tensor path, from the MMA fragment layout to one thread per row):
 // [2 buffers][P parts][R rows][red_stride]
-template <int R, int MT>
+template <int R, int MT, bool U5>
 constexpr int red_bytes() {
-  return (RCfg<R>::P > 1 || MT >= TC_MIN_MT || MCfg<MT>::HALVES > 1)
+  return !UCfg<R, MT, U5>::ON && (RCfg<R>::P > 1 || MT >= TC_MIN_MT || MCfg<MT>::HALVES > 1)
              ? 2 * MCfg<MT>::HALVES * 128 * red_stride<MT>() * 4
              : 0;
 }
 
-template <int R, int MT>
-constexpr size_t gemv_smem_bytes(int act = MCfg<MT>::ACT_BUDGET) {
-  return (size_t)MCfg<MT>::STAGES * RCfg<R>::STAGE_BYTES + act + red_bytes<R, MT>() +
-         2 * MCfg<MT>::STAGES * sizeof(uint64_t) + 4 * sizeof(int);
+template <int R, int MT, bool U5>
+constexpr size_t gemv_smem_bytes(int act = act_budget<R, MT, U5>()) {
+  return (size_t)MCfg<MT>::STAGES * RCfg<R>::STAGE_BYTES + UCfg<R, MT, U5>::A_BYTES + UCfg<R, MT, U5>::B_BYTES + act +
+         red_bytes<R, MT, U5>() + 2 * MCfg<MT>::STAGES * sizeof(uint64_t) + UCfg<R, MT, U5>::MISC_INTS * sizeof(int);
 }
 
 struct GemvArgs {
@@ -533,6 +565,21 @@ __device__ __forceinline__ void chunk_value_mma(const uint8_t* cq, int r, int kb
     for (int e = 0; e < 4; ++e) v[nt][e] = tadd(q[0][nt][e], q[1][nt][e]);
 }
 
+// tcgen05 path: 16 int8 values (one row's half block) to 16 fp16, written as
+// the two core-matrix rows of a canonical K-major slice (k 0..7 at dst, k
+// 8..15 at dst + 128).  The weights and the activations go through the same
+// conversion, so their k order is permuted identically and every dot is
+// unchanged.
+__device__ __forceinline__ void store_f16_slice(uint8_t* dst, uint4 q) {
+  uint32_t o[8];
+  i8x4_to_h2x2(q.x, o[0], o[1]);
+  i8x4_to_h2x2(q.y, o[2], o[3]);
+  i8x4_to_h2x2(q.z, o[4], o[5]);
+  i8x4_to_h2x2(q.w, o[6], o[7]);
+  *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+  *reinterpret_cast<uint4*>(dst + 128) = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 // pairwise tree of the P chunk values of a round (P a power of two); with
 // H = 2 halves per chunk, a chunk's value is first the sum of its halves'
 // (stored hstride apart)
@@ -546,27 +593,33 @@ __device__ __forceinline__ float tree_of(const float* w, int stride, int hstride
   }
 }
 
-template <int R, int MT, bool FUSED>
+template <int R, int MT, bool FUSED, bool U5>
 __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_kernel(const GemvArgs a) {
   constexpr int P = RCfg<R>::P;
   constexpr int NCW = MCfg<MT>::NCW;
   constexpr int NT = NCW * 32;  // consumer threads
   constexpr int STAGES = MCfg<MT>::STAGES;
-  constexpr int LV = log2_floor(ru_max<R, MT>()) + 1;
+  constexpr int LV = log2_floor(ru_max<R, MT, U5>()) + 1;
   constexpr bool TC = MT >= TC_MIN_MT;  // tensor-core path
   constexpr int HALVES = MCfg<MT>::HALVES;
   constexpr bool EXCHANGE = (P > 1) || TC || (HALVES > 1);
   constexpr int RS = red_stride<MT>();
   constexpr int BAR_CONSUMERS = 1;  // named barrier of the consumer warps
+  constexpr bool UM = UCfg<R, MT, U5>::ON;  // tcgen05 path
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stage_buf = smem;
-  uint8_t* act_base = smem + (size_t)STAGES * RCfg<R>::STAGE_BYTES;
+  uint8_t* umA = smem + (size_t)STAGES * RCfg<R>::STAGE_BYTES;  // fp16 operands (tcgen05 path)
+  uint8_t* umB = umA + UCfg<R, MT, U5>::A_BYTES;
+  uint8_t* act_base = umB + UCfg<R, MT, U5>::B_BYTES;
   // the activation area is sized per launch (the unit's blocks), the rest follows it
   float* red = reinterpret_cast<float*>(act_base + a.act_smem);  // [2][HALVES][P][R][RS]
-  uint64_t* full = reinterpret_cast<uint64_t*>(act_base + a.act_smem + red_bytes<R, MT>());
+  uint64_t* full = reinterpret_cast<uint64_t*>(act_base + a.act_smem + red_bytes<R, MT, U5>());
   uint64_t* empty = full + STAGES;
   volatile int* misc = reinterpret_cast<volatile int*>(empty + STAGES);
-  // misc[0]: abort flag, misc[1]: "this CTA combines the tile", misc[2]: rounds issued
+  // misc[0]: abort flag, misc[1]: "this CTA combines the tile", misc[2]: rounds issued;
+  // tcgen05 path: misc[4..5] the MMA mbarrier, misc[6] the tensor-memory base
+  uint64_t* mma_bar = reinterpret_cast<uint64_t*>(const_cast<int*>(misc) + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(misc) + 6);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -577,6 +630,7 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
     misc[0] = 0;
     misc[1] = 0;
     misc[2] = 0;
+    if constexpr (UM) mbar_init(mma_bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -605,6 +659,15 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
   if (CL > 1) {  // phase 1: every CTA of the cluster is running
     cluster_arrive_aligned();
     cluster_wait_aligned();
+  }
+  uint32_t tmem = 0;     // tensor memory of the block dots (tcgen05 path)
+  uint32_t mphase = 0;   // parity of the MMA mbarrier's next completion
+  if constexpr (UM) {
+    if (warp == 0) tmem_alloc(tmem_slot, UCfg<R, MT, U5>::TMEM_COLS);
+    tc_fence_before_sync();
+    named_bar_sync(BAR_CONSUMERS, NT);
+    tc_fence_after_sync();
+    tmem = *tmem_slot;
   }
 
   const int i = threadIdx.x % R;        // row inside the tile
@@ -672,79 +735,172 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
         atomicOr(a.err, ERR_CONSUMER_WAIT);
         misc[0] = 1;
       }
-      float v[MT];
-#pragma unroll
-      for (int m = 0; m < MT; ++m) v[m] = 0.0f;
       float mv[MC];  // this thread's merged columns of the round
-      const int xpar = consumed & 1;
-      float* rb = red + (size_t)xpar * HALVES * P * R * RS;  // [HALVES][P][R][RS]
-      if constexpr (TC) {
-        // 8 slices (16 rows x one chunk) per round, 8/NCW per warp (a loop, not
-        // unrolled: one copy of the slice code keeps the instruction cache warm)
-        const int g = lane >> 2, tig = lane & 3;
+      if constexpr (UM) {
+        // the round is one chunk of the tile (P == 1); rows past r are zero,
+        // blocks past kb are not multiplied and count as zero
+        const int c = c0 + rho;
+        const int kb = chunk_blocks(c, a.NB);
+        const uint8_t* cq = stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES;
+        if (got) {
 #pragma unroll 1
-        for (int k = 0; k < 8 / NCW; ++k) {
-          const int sl = warp + k * NCW;
-          const int ps = sl / (R / 16), row0 = (sl % (R / 16)) * 16;
-          const int c = c0 + rho * P + ps;
-          float cv[MT / 8][4];
-#pragma unroll
-          for (int nt = 0; nt < MT / 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) cv[nt][e] = 0.0f;
-          if (got && c < a.nch) {
-            const int blk = (rho * P + ps) * CHUNK_BLOCKS;
-            const uint8_t* cq = stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES + ps * (r * CHUNK_BLOCKS * BLOCK_BYTES);
-            chunk_value_mma<MT>(cq, r, chunk_blocks(c, a.NB), row0, L.q + blk * 32, L.d + blk, L.mq, UB, cv);
+          for (int task = threadIdx.x; task < kb * 2 * 128; task += NT) {
+            const int row = task & 127, jh = task >> 7;  // jh = 2 * block + half
+            const uint4 q = row < r ? lds128(cq + chunk_quant_off(jh >> 1, jh & 1, row, r)) : make_uint4(0u, 0u, 0u, 0u);
+            store_f16_slice(umA + jh * UCfg<R, MT, U5>::SLICE_A + (row >> 3) * 256 + (row & 7) * 16, q);
           }
-#pragma unroll
-          for (int nt = 0; nt < MT / 8; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              rb[(ps * R + row0 + g + (e >> 1) * 8) * RS + 8 * nt + 2 * tig + (e & 1)] = cv[nt][e];
+#pragma unroll 1
+          for (int task = threadIdx.x; task < kb * 2 * MT; task += NT) {
+            const int m = task % MT, jh = task / MT;
+            const uint4 q = lds128(L.q + m * L.mq + (rho * CHUNK_BLOCKS + (jh >> 1)) * 32 + (jh & 1) * 16);
+            store_f16_slice(umB + jh * UCfg<R, MT, U5>::SLICE_B + (m >> 3) * 256 + (m & 7) * 16, q);
+          }
         }
-      } else {
-        const int c = c0 + rho * P + p;
-        if (got && c < a.nch) {
-          const int blk = (rho * P + p) * CHUNK_BLOCKS;  // first block of the chunk in the unit
-          const uint8_t* cq = stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES + p * (r * CHUNK_BLOCKS * BLOCK_BYTES);
-          if constexpr (HALVES == 1)
-            chunk_value<MT>(cq, r, chunk_blocks(c, a.NB), i, L.q + blk * 32, L.d + blk, L.mq, UB, v);
-          else
-            chunk_value_half<MT>(cq, r, chunk_blocks(c, a.NB), i, 4 * hb, L.q + blk * 32, L.d + blk, L.mq,
-                                 UB, v);
-        }
-        if constexpr (EXCHANGE) {
-#pragma unroll
-          for (int m = 0; m < MT; ++m) rb[((hb * P + p) * R + i) * RS + m] = v[m];
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
-      ++consumed;
-      if (++stage == STAGES) {
-        stage = 0;
-        phase ^= 1u;
-      }
-      if constexpr (EXCHANGE) {
-        // the P chunk values of row i meet in shared memory; the buffer
-        // written in round k was last read in round k-2, before the barrier
-        // of round k-1 that every writer has passed
+        fence_proxy_async_smem();
         named_bar_sync(BAR_CONSUMERS, NT);
+        const bool go = misc[0] == 0;  // read after the barrier: the same in every consumer
+        if (go && threadIdx.x == 0) {
+          tc_fence_after_sync();
+          constexpr uint32_t IDESC = umma_idesc_f16(128, MT);
+          for (int jh = 0; jh < 2 * kb; ++jh)
+            umma_f16(tmem + (uint32_t)(MT * (jh >> 1)),
+                     umma_smem_desc(smem_u32(umA + jh * UCfg<R, MT, U5>::SLICE_A), 128, 256),
+                     umma_smem_desc(smem_u32(umB + jh * UCfg<R, MT, U5>::SLICE_B), 128, 256), IDESC, (jh & 1) != 0);
+          umma_commit(mma_bar);
+        }
+        bool done = false;
+        if (go) {
+          done = mbar_wait_bounded(mma_bar, mphase, WAIT_LIMIT_NS);
+          if (!done) {
+            atomicOr(a.err, ERR_CONSUMER_WAIT);
+            misc[0] = 1;
+          }
+          done = __all_sync(0xffffffffu, done);  // tcgen05.ld is warp-collective
+          if (done) mphase ^= 1u;
+          tc_fence_after_sync();
+        }
+        // thread (row i, column group mcg) reads its row's dots of tokens
+        // [MC mcg, MC mcg + MC): warp w reaches lanes 32 (w % 4) .. + 31.  The
+        // two 4-block halves of the chunk are read and summed one after the
+        // other (fewer live registers); the tree is that of the other paths.
+        float half_sum[2][MC];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t u[4][MC];
+          if (done) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (4 * hf + j < kb)
+                tmem_ld8(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(MT * (4 * hf + j) + MC * mcg), u[j]);
+            tmem_ld_wait();
+          }
+          float dw[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dw[j] = (4 * hf + j < kb && i < r)
+                        ? __half2float(*reinterpret_cast<const __half*>(cq + chunk_scale_off(4 * hf + j, i, r, kb)))
+                        : 0.0f;
+#pragma unroll
+          for (int cc = 0; cc < MC; ++cc) {
+            const __half* da = L.d + (mcg * MC + cc) * UB + rho * CHUNK_BLOCKS + 4 * hf;
+            float t[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              t[j] = (done && 4 * hf + j < kb)
+                         ? __fmul_rn(__uint_as_float(u[j][cc]), __fmul_rn(dw[j], __half2float(da[j])))
+                         : 0.0f;
+            half_sum[hf][cc] = tadd(tadd(t[0], t[1]), tadd(t[2], t[3]));
+          }
+        }
+#pragma unroll
+        for (int cc = 0; cc < MC; ++cc) mv[cc] = tadd(half_sum[0][cc], half_sum[1][cc]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+        ++consumed;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        tc_fence_before_sync();
+        named_bar_sync(BAR_CONSUMERS, NT);  // operands and tensor memory free for the next round
         if (misc[0]) {
           ok = false;
           break;
         }
-        if (!merger) continue;
-#pragma unroll
-        for (int c = 0; c < MC; ++c) mv[c] = tree_of<P, HALVES>(rb + i * RS + mcg * MC + c, R * RS, P * R * RS);
       } else {
-        if (!got || misc[0]) {
-          ok = false;
-          break;
+        float v[MT];
+  #pragma unroll
+        for (int m = 0; m < MT; ++m) v[m] = 0.0f;
+        const int xpar = consumed & 1;
+        float* rb = red + (size_t)xpar * HALVES * P * R * RS;  // [HALVES][P][R][RS]
+        if constexpr (TC) {
+          // 8 slices (16 rows x one chunk) per round, 8/NCW per warp (a loop, not
+          // unrolled: one copy of the slice code keeps the instruction cache warm)
+          const int g = lane >> 2, tig = lane & 3;
+  #pragma unroll 1
+          for (int k = 0; k < 8 / NCW; ++k) {
+            const int sl = warp + k * NCW;
+            const int ps = sl / (R / 16), row0 = (sl % (R / 16)) * 16;
+            const int c = c0 + rho * P + ps;
+            float cv[MT / 8][4];
+  #pragma unroll
+            for (int nt = 0; nt < MT / 8; ++nt)
+  #pragma unroll
+              for (int e = 0; e < 4; ++e) cv[nt][e] = 0.0f;
+            if (got && c < a.nch) {
+              const int blk = (rho * P + ps) * CHUNK_BLOCKS;
+              const uint8_t* cq = stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES + ps * (r * CHUNK_BLOCKS * BLOCK_BYTES);
+              chunk_value_mma<MT>(cq, r, chunk_blocks(c, a.NB), row0, L.q + blk * 32, L.d + blk, L.mq, UB, cv);
+            }
+  #pragma unroll
+            for (int nt = 0; nt < MT / 8; ++nt)
+  #pragma unroll
+              for (int e = 0; e < 4; ++e)
+                rb[(ps * R + row0 + g + (e >> 1) * 8) * RS + 8 * nt + 2 * tig + (e & 1)] = cv[nt][e];
+          }
+        } else {
+          const int c = c0 + rho * P + p;
+          if (got && c < a.nch) {
+            const int blk = (rho * P + p) * CHUNK_BLOCKS;  // first block of the chunk in the unit
+            const uint8_t* cq = stage_buf + (size_t)stage * RCfg<R>::STAGE_BYTES + p * (r * CHUNK_BLOCKS * BLOCK_BYTES);
+            if constexpr (HALVES == 1)
+              chunk_value<MT>(cq, r, chunk_blocks(c, a.NB), i, L.q + blk * 32, L.d + blk, L.mq, UB, v);
+            else
+              chunk_value_half<MT>(cq, r, chunk_blocks(c, a.NB), i, 4 * hb, L.q + blk * 32, L.d + blk, L.mq,
+                                   UB, v);
+          }
+          if constexpr (EXCHANGE) {
+  #pragma unroll
+            for (int m = 0; m < MT; ++m) rb[((hb * P + p) * R + i) * RS + m] = v[m];
+          }
         }
-#pragma unroll
-        for (int c = 0; c < MC; ++c) mv[c] = v[c];  // CG == 1: the thread's own row
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+        ++consumed;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if constexpr (EXCHANGE) {
+          // the P chunk values of row i meet in shared memory; the buffer
+          // written in round k was last read in round k-2, before the barrier
+          // of round k-1 that every writer has passed
+          named_bar_sync(BAR_CONSUMERS, NT);
+          if (misc[0]) {
+            ok = false;
+            break;
+          }
+          if (!merger) continue;
+  #pragma unroll
+          for (int c = 0; c < MC; ++c) mv[c] = tree_of<P, HALVES>(rb + i * RS + mcg * MC + c, R * RS, P * R * RS);
+        } else {
+          if (!got || misc[0]) {
+            ok = false;
+            break;
+          }
+  #pragma unroll
+          for (int c = 0; c < MC; ++c) mv[c] = v[c];  // CG == 1: the thread's own row
+        }
       }
       // binary counter over the round subtrees (merging threads)
       bool placed = false;
@@ -864,29 +1020,41 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
       }
     }
   }
+  if constexpr (UM) {
+    // the warp that allocated the tensor memory frees it once every consumer
+    // is done with it; after an abort an MMA may still be in flight, which
+    // lands first (bounded)
+    tc_fence_before_sync();
+    named_bar_sync(BAR_CONSUMERS, NT);
+    if (warp == 0) {
+      if (lane == 0 && misc[0]) (void)mbar_wait_bounded(mma_bar, mphase, WAIT_LIMIT_NS / 4);
+      __syncwarp();
+      tmem_dealloc(tmem, UCfg<R, MT, U5>::TMEM_COLS);
+    }
+  }
 }
 
 // Every libq8 kernel asks for the largest shared-memory carveout (the same
 // for all, so an SM switching between kernels needs no reconfiguration).
-template <int R, int MT, bool FUSED>
+template <int R, int MT, bool FUSED, bool U5>
 cudaError_t set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<R, MT, FUSED>,
+  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<R, MT, FUSED, U5>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)gemv_smem_bytes<R, MT>());
+                                       (int)gemv_smem_bytes<R, MT, U5>());
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gemv_kernel<R, MT, FUSED>,
+  return cudaFuncSetAttribute(gemv_kernel<R, MT, FUSED, U5>,
                               cudaFuncAttributePreferredSharedMemoryCarveout,
                               (int)cudaSharedmemCarveoutMaxShared);
 }
 
-template <int R, int MT, bool FUSED>
+template <int R, int MT, bool FUSED, bool U5>
 cudaError_t launch_gemv_t(const GemvArgs& args, int grid, int cluster, bool pdl, cudaStream_t s) {
-  cudaError_t e = set_attributes<R, MT, FUSED>();
+  cudaError_t e = set_attributes<R, MT, FUSED, U5>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(MCfg<MT>::THREADS);
-  cfg.dynamicSmemBytes = gemv_smem_bytes<R, MT>(args.act_smem);
+  cfg.dynamicSmemBytes = gemv_smem_bytes<R, MT, U5>(args.act_smem);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   int na = 0;
@@ -904,27 +1072,27 @@ cudaError_t launch_gemv_t(const GemvArgs& args, int grid, int cluster, bool pdl,
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<R, MT, FUSED>, args);
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<R, MT, FUSED, U5>, args);
 }
 
-template <int R, int MT, bool FUSED>
+template <int R, int MT, bool FUSED, bool U5>
 int occupancy_t() {
-  if (set_attributes<R, MT, FUSED>() != cudaSuccess) return 0;
+  if (set_attributes<R, MT, FUSED, U5>() != cudaSuccess) return 0;
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_kernel<R, MT, FUSED>, MCfg<MT>::THREADS,
-                                                    gemv_smem_bytes<R, MT>()) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_kernel<R, MT, FUSED, U5>, MCfg<MT>::THREADS,
+                                                    gemv_smem_bytes<R, MT, U5>()) != cudaSuccess)
     return 0;
   return occ;
 }
 
 // Whether clusters of `cluster` CTAs of this kernel can be resident at all.
-template <int R, int MT, bool FUSED>
+template <int R, int MT, bool FUSED, bool U5>
 bool cluster_fits_t(int cluster) {
-  if (set_attributes<R, MT, FUSED>() != cudaSuccess) return false;
+  if (set_attributes<R, MT, FUSED, U5>() != cudaSuccess) return false;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster);
   cfg.blockDim = dim3(MCfg<MT>::THREADS);
-  cfg.dynamicSmemBytes = gemv_smem_bytes<R, MT>();
+  cfg.dynamicSmemBytes = gemv_smem_bytes<R, MT, U5>();
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cluster;
@@ -933,57 +1101,81 @@ bool cluster_fits_t(int cluster) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemv_kernel<R, MT, FUSED>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, gemv_kernel<R, MT, FUSED, U5>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
   return n > 0;
 }
 
+// 16 activation rows: the tcgen05 kernel exists for 128-row tiles only
+// (u5 selects it there and is ignored elsewhere).
+template <int R, bool FUSED>
+cudaError_t launch_gemv_16(const GemvArgs& args, bool u5, int grid, int cluster, bool pdl, cudaStream_t s) {
+  if constexpr (R == 128) {
+    if (u5) return launch_gemv_t<R, 16, FUSED, true>(args, grid, cluster, pdl, s);
+  }
+  return launch_gemv_t<R, 16, FUSED, false>(args, grid, cluster, pdl, s);
+}
+template <int R, bool FUSED>
+int occupancy_16(bool u5) {
+  if constexpr (R == 128) {
+    if (u5) return occupancy_t<R, 16, FUSED, true>();
+  }
+  return occupancy_t<R, 16, FUSED, false>();
+}
+template <int R, bool FUSED>
+bool cluster_fits_16(bool u5, int c) {
+  if constexpr (R == 128) {
+    if (u5) return cluster_fits_t<R, 16, FUSED, true>(c);
+  }
+  return cluster_fits_t<R, 16, FUSED, false>(c);
+}
+
 // Per-R translation units instantiate these for every MT and FUSED.
 template <int R>
-cudaError_t launch_gemv_r(const GemvArgs& args, int MT, bool fused, int grid, int cluster, bool pdl,
+cudaError_t launch_gemv_r(const GemvArgs& args, int MT, bool fused, bool u5, int grid, int cluster, bool pdl,
                          cudaStream_t s);
 template <int R>
-int occupancy_r(int MT, bool fused);
+int occupancy_r(int MT, bool fused, bool u5);
 template <int R>
-bool cluster_fits_r(int MT, bool fused, int cluster);
+bool cluster_fits_r(int MT, bool fused, bool u5, int cluster);
 
 #define Q8_INSTANTIATE_R(R)                                                                          \
   template <>                                                                                        \
-  cudaError_t launch_gemv_r<R>(const GemvArgs& args, int MT, bool fused, int grid, int cluster,      \
-                               bool pdl, cudaStream_t s) {                                           \
+  cudaError_t launch_gemv_r<R>(const GemvArgs& args, int MT, bool fused, bool u5, int grid,          \
+                               int cluster, bool pdl, cudaStream_t s) {                              \
     switch (MT) {                                                                                    \
-      case 1: return fused ? launch_gemv_t<R, 1, true>(args, grid, cluster, pdl, s)                           \
-                           : launch_gemv_t<R, 1, false>(args, grid, cluster, pdl, s);                         \
-      case 2: return fused ? launch_gemv_t<R, 2, true>(args, grid, cluster, pdl, s)                           \
-                           : launch_gemv_t<R, 2, false>(args, grid, cluster, pdl, s);                         \
-      case 4: return fused ? launch_gemv_t<R, 4, true>(args, grid, cluster, pdl, s)                           \
-                           : launch_gemv_t<R, 4, false>(args, grid, cluster, pdl, s);                         \
-      case 8: return fused ? launch_gemv_t<R, 8, true>(args, grid, cluster, pdl, s)                           \
-                           : launch_gemv_t<R, 8, false>(args, grid, cluster, pdl, s);                         \
-      default: return fused ? launch_gemv_t<R, 16, true>(args, grid, cluster, pdl, s)                         \
-                            : launch_gemv_t<R, 16, false>(args, grid, cluster, pdl, s);                       \
+      case 1: return fused ? launch_gemv_t<R, 1, true, false>(args, grid, cluster, pdl, s)           \
+                           : launch_gemv_t<R, 1, false, false>(args, grid, cluster, pdl, s);         \
+      case 2: return fused ? launch_gemv_t<R, 2, true, false>(args, grid, cluster, pdl, s)           \
+                           : launch_gemv_t<R, 2, false, false>(args, grid, cluster, pdl, s);         \
+      case 4: return fused ? launch_gemv_t<R, 4, true, false>(args, grid, cluster, pdl, s)           \
+                           : launch_gemv_t<R, 4, false, false>(args, grid, cluster, pdl, s);         \
+      case 8: return fused ? launch_gemv_t<R, 8, true, false>(args, grid, cluster, pdl, s)           \
+                           : launch_gemv_t<R, 8, false, false>(args, grid, cluster, pdl, s);         \
+      default: return fused ? launch_gemv_16<R, true>(args, u5, grid, cluster, pdl, s)               \
+                            : launch_gemv_16<R, false>(args, u5, grid, cluster, pdl, s);             \
     }                                                                                                \
   }                                                                                                  \
   template <>                                                                                        \
-  int occupancy_r<R>(int MT, bool fused) {                                                           \
+  int occupancy_r<R>(int MT, bool fused, bool u5) {                                                  \
     switch (MT) {                                                                                    \
-      case 1: return fused ? occupancy_t<R, 1, true>() : occupancy_t<R, 1, false>();                 \
-      case 2: return fused ? occupancy_t<R, 2, true>() : occupancy_t<R, 2, false>();                 \
-      case 4: return fused ? occupancy_t<R, 4, true>() : occupancy_t<R, 4, false>();                 \
-      case 8: return fused ? occupancy_t<R, 8, true>() : occupancy_t<R, 8, false>();                 \
-      default: return fused ? occupancy_t<R, 16, true>() : occupancy_t<R, 16, false>();              \
+      case 1: return fused ? occupancy_t<R, 1, true, false>() : occupancy_t<R, 1, false, false>();   \
+      case 2: return fused ? occupancy_t<R, 2, true, false>() : occupancy_t<R, 2, false, false>();   \
+      case 4: return fused ? occupancy_t<R, 4, true, false>() : occupancy_t<R, 4, false, false>();   \
+      case 8: return fused ? occupancy_t<R, 8, true, false>() : occupancy_t<R, 8, false, false>();   \
+      default: return fused ? occupancy_16<R, true>(u5) : occupancy_16<R, false>(u5);                \
     }                                                                                                \
   }                                                                                                  \
   template <>                                                                                        \
-  bool cluster_fits_r<R>(int MT, bool fused, int c) {                                                \
+  bool cluster_fits_r<R>(int MT, bool fused, bool u5, int c) {                                       \
     switch (MT) {                                                                                    \
-      case 1: return fused ? cluster_fits_t<R, 1, true>(c) : cluster_fits_t<R, 1, false>(c);         \
-      case 2: return fused ? cluster_fits_t<R, 2, true>(c) : cluster_fits_t<R, 2, false>(c);         \
-      case 4: return fused ? cluster_fits_t<R, 4, true>(c) : cluster_fits_t<R, 4, false>(c);         \
-      case 8: return fused ? cluster_fits_t<R, 8, true>(c) : cluster_fits_t<R, 8, false>(c);         \
-      default: return fused ? cluster_fits_t<R, 16, true>(c) : cluster_fits_t<R, 16, false>(c);      \
+      case 1: return fused ? cluster_fits_t<R, 1, true, false>(c) : cluster_fits_t<R, 1, false, false>(c); \
+      case 2: return fused ? cluster_fits_t<R, 2, true, false>(c) : cluster_fits_t<R, 2, false, false>(c); \
+      case 4: return fused ? cluster_fits_t<R, 4, true, false>(c) : cluster_fits_t<R, 4, false, false>(c); \
+      case 8: return fused ? cluster_fits_t<R, 8, true, false>(c) : cluster_fits_t<R, 8, false, false>(c); \
+      default: return fused ? cluster_fits_16<R, true>(u5, c) : cluster_fits_16<R, false>(u5, c);    \
     }                                                                                                \
   }
 

@@ -23,6 +23,7 @@ struct GemvPlan {
   int units = 0;
   int grid = 0;      // persistent CTAs
   int cluster = 1;   // CTAs per thread-block cluster (shared activation staging)
+  bool u5 = false;   // block dots on the tcgen05 tensor cores (128-row tiles, 16 rows per pass)
   size_t smem = 0;   // dynamic shared memory per CTA
   size_t ws_bytes = 0;
 };
@@ -34,7 +35,7 @@ struct DeviceInfo {
 };
 
 cudaError_t current_device_info(DeviceInfo* out);
-bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, GemvPlan* p);
+bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, bool tcgen05, GemvPlan* p);
 
 // Kernel launchers (q8_aux.cu / q8_gemv.cu).  Each returns the CUDA error of
 // the launch.  `pdl` launches with programmatic stream serialization.

@@ -71,7 +71,7 @@ extern "C" int q8_gemm_noalloc(const void* W, int64_t N, int64_t K, const void* 
   if (d.cc_major != 10 || d.cc_minor != 3) return Q8_EDEVICE;
   if (d.device < 0 || d.device >= MAX_DEVICES) return Q8_EDEVICE;
   GemvPlan p;
-  if (!plan_gemv(d, N, K, M, false, &p)) return Q8_ESHAPE;
+  if (!plan_gemv(d, N, K, M, false, false, &p)) return Q8_ESHAPE;
   if (p.ws_bytes > NOALLOC_BYTES) return Q8_ESCRATCH;  // this shape needs more scratch than built in
   void* ws = nullptr;
   if (p.ws_bytes > 0) {

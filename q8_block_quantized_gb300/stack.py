@@ -20,7 +20,7 @@ from dataclasses import dataclass, field
 import torch
 
 import q8_synth
-from . import (FLAG_PDL, empty_blocks, pack_weights_f32, q8_fused_quant_gemm, q8_gemm,
+from . import (FLAG_PDL, FLAG_TCGEN05, empty_blocks, pack_weights_f32, q8_fused_quant_gemm, q8_gemm,
                q8_quantize_act, q8_workspace_bytes)
 
 MODES = ("shared", "fused", "unfused")
@@ -47,6 +47,7 @@ class Q8Stack:
     layers: int | None = None
     seed: int = 0
     pdl: bool = True
+    tcgen05: bool = False                # Q8_FLAG_TCGEN05 on every GEMV call
     device: str = "cuda"
     shared_weights: dict | None = None   # reuse another stack's packed weights
     calls: list = field(default_factory=list)
@@ -109,14 +110,15 @@ class Q8Stack:
     # -- the step -------------------------------------------------------------------
     def step(self, stream=None):
         flags = FLAG_PDL if self.pdl else 0
+        gflags = flags | (FLAG_TCGEN05 if self.tcgen05 else 0)
         ws = self.workspace
         for c in self.calls:
             if c.kind == "quant":
                 q8_quantize_act(c.x, c.A, flags=flags, stream=stream)
             elif c.kind == "gemm":
-                q8_gemm(c.W, c.N, c.K, c.A, self.M, c.y, workspace=ws, flags=flags, stream=stream)
+                q8_gemm(c.W, c.N, c.K, c.A, self.M, c.y, workspace=ws, flags=gflags, stream=stream)
             else:
-                q8_fused_quant_gemm(c.W, c.N, c.K, c.x, self.M, c.y, workspace=ws, flags=flags,
+                q8_fused_quant_gemm(c.W, c.N, c.K, c.x, self.M, c.y, workspace=ws, flags=gflags,
                                     stream=stream)
 
     def capture(self) -> torch.cuda.CUDAGraph:

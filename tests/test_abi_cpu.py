@@ -65,7 +65,7 @@ def test_host_argument_checks_reject_before_any_device_work(lib):
     g = lib.q8_gemm
     assert g(None, 8, 64, fake, 1, y, None, 0, 0, None) == -1          # null W
     assert g(fake, 8, 64, None, 1, y, None, 0, 0, None) == -1          # null A
-    assert g(fake, 8, 64, fake, 1, y, None, 0, 2, None) == -1          # unknown flag
+    assert g(fake, 8, 64, fake, 1, y, None, 0, 4, None) == -1          # unknown flag
     assert g(fake, 8, 63, fake, 1, y, None, 0, 0, None) == -2          # K % 32
     assert g(fake, 8, 0, fake, 1, y, None, 0, 0, None) == -2           # K = 0
     assert g(fake, 0, 64, fake, 1, y, None, 0, 0, None) == -2          # N = 0

@@ -304,3 +304,34 @@ def test_host_errors_raise(q8):
     with pytest.raises(q8.Q8Error):
         q8.q8_gemm(W[1:], N, K, A, M, y)                 # misaligned W
     assert q8.q8_device_error() == 0
+
+
+@pytest.mark.parametrize("N,K", [(10000, 2080), (16384, 3072), (12800, 8192)])
+@pytest.mark.parametrize("M", [9, 16, 33, 64])
+def test_tcgen05_flag_gives_the_same_bits(q8, N, K, M):
+    # Q8_FLAG_TCGEN05: 128-row tiles with 9-16 rows per pass take the tcgen05
+    # kernel (ragged last tile, ragged last chunk, split K, several passes)
+    assert q8.q8_packed_tile_rows(N) == 128
+    w, x = _case(N, K, M, 21)
+    W = _gpu_pack(q8, w)
+    Ab = oracle.quantize(x.numpy())
+    A = torch.from_numpy(Ab).to(DEV)
+    xd = x.to(DEV)
+    ws = q8.new_workspace(N, K, M)
+    outs = {}
+    for flags in (0, q8.FLAG_TCGEN05, q8.FLAG_TCGEN05 | q8.FLAG_PDL):
+        y = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+        q8.q8_gemm(W, N, K, A, M, y, workspace=ws, flags=flags)
+        yf = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+        q8.q8_fused_quant_gemm(W, N, K, xd, M, yf, workspace=ws, flags=flags)
+        outs[flags] = (y, yf)
+    torch.cuda.synchronize()
+    base = outs[0][0]
+    for y, yf in outs.values():
+        assert torch.equal(y, base) and torch.equal(yf, base)
+    if N * K <= 30_000_000:
+        y_ref, S_ref = oracle.gemm(oracle.quantize(w.numpy()), Ab, K)
+        _assert_within_tol(outs[q8.FLAG_TCGEN05][0], y_ref, S_ref)
+    if ws is not None:  # split along K: the tickets are left zero
+        assert not ws[:16384].any()
+    assert q8.q8_device_error() == 0
