@@ -174,15 +174,16 @@ Q8_API int q8_residual_rmsnorm_quantize(const float *x, const float *delta, cons
  *   out_blocks [M][F/32] blocks, 2-byte aligned.
  *   flags      0 or Q8_FLAG_PDL.
  * silu(g) = g / (1 + e^-g).  e^x is a fixed procedure (Cody and Waite's
- * reduction, then a Taylor polynomial), identical wherever it runs:
+ * reduction, then a Taylor polynomial), identical wherever it runs; fma is
+ * a fused multiply-add (one rounding):
  *   x > 88: +inf;  x < -87: 0;  otherwise n = rint(x * L2E),
- *   r = (x - n * LN2_HI) - n * LN2_LO,
- *   p = ((((((C7 r + C6) r + C5) r + C4) r + C3) r + 1/2) r + 1) r + 1,
+ *   r = fma(-n, LN2_LO, fma(-n, LN2_HI, x)),
+ *   p = C7, then p = fma(p, r, c) for c = C6, C5, C4, C3, 1/2, 1, 1,
  *   e^x = p * 2^n,
  * with L2E = 0x1.715476p+0 (1/ln 2), LN2_HI = 0x1.63p-1 (355/512),
  * LN2_LO = -0x1.bd0106p-13 (ln 2 - 355/512), C3..C7 = 1/3!..1/7! rounded to
  * single precision (0x1.555556p-3, 0x1.555556p-5, 0x1.111112p-7,
- * 0x1.6c16c2p-10, 0x1.a01a02p-13); within 1 ulp of e^x.
+ * 0x1.6c16c2p-10, 0x1.a01a02p-13); within 0.7 ulp of e^x.
  */
 Q8_API int q8_swiglu_quantize(const float *gate_up, int64_t M, int64_t F, void *out_blocks,
                               unsigned flags, void *stream);

@@ -275,8 +275,9 @@ void q8o_ember_tile_unpack(const uint8_t *tile, uint8_t *dst)
  *     summed as the pairwise tree over k padded with zeros to a power of
  *     two; ms = s / K; r = 1 / sqrt(ms + eps); y_k = (h_k * r) * gamma_k.
  *   - SwiGLU: h = silu(g) * u with silu(g) = g / (1 + e^-g), e^x being the
- *     fixed procedure q8o_exp below; gate g and up u are the first and the
- *     second half of each row of the gate/up product.
+ *     fixed procedure q8o_exp below (fused multiply-adds, each one
+ *     rounding); gate g and up u are the first and the second half of each
+ *     row of the gate/up product.
  *   - then every 32-block of y (or h) is quantized by q8o_quantize_block.
  * ------------------------------------------------------------------------- */
 
@@ -305,9 +306,10 @@ float q8o_pairwise_sum(const float *v, int64_t n)
 /* e^x by a fixed single-precision procedure: Cody and Waite's reduction
  * x = n ln2 + r with ln2 split into 355/512 (9 significant bits, so n * 355/512
  * is exact for |n| <= 128) plus the rest of ln2 rounded to single precision,
- * then the Taylor polynomial of degree 7 of e^r in Horner form (|r| <= 0.35,
- * truncation below 6e-9 relative), then the exact scaling by 2^n.  Outside
- * [-87, 88] the result is 0 or +infinity. */
+ * each step one fused multiply-add (fmaf, one rounding); then the Taylor
+ * polynomial of degree 7 of e^r in Horner form, each step one fmaf (|r| <=
+ * 0.35, truncation below 6e-9 relative); then the exact scaling by 2^n.
+ * Outside [-87, 88] the result is 0 or +infinity. */
 #define Q8O_LOG2E 0x1.715476p+0f      /* 1/ln 2 rounded            */
 #define Q8O_LN2_HI 0x1.63p-1f         /* 355/512                   */
 #define Q8O_LN2_LO -0x1.bd0106p-13f   /* ln 2 - 355/512 rounded    */
@@ -323,15 +325,16 @@ float q8o_exp(float x)
     if (x < -87.0f)
         return 0.0f;
     float n = rintf(x * Q8O_LOG2E);
-    float r = (x - n * Q8O_LN2_HI) - n * Q8O_LN2_LO;
+    float r = fmaf(-n, Q8O_LN2_HI, x);
+    r = fmaf(-n, Q8O_LN2_LO, r);
     float p = Q8O_C7;
-    p = p * r + Q8O_C6;
-    p = p * r + Q8O_C5;
-    p = p * r + Q8O_C4;
-    p = p * r + Q8O_C3;
-    p = p * r + 0.5f;
-    p = p * r + 1.0f;
-    p = p * r + 1.0f;
+    p = fmaf(p, r, Q8O_C6);
+    p = fmaf(p, r, Q8O_C5);
+    p = fmaf(p, r, Q8O_C4);
+    p = fmaf(p, r, Q8O_C3);
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
     return p * ldexpf(1.0f, (int)n);
 }
 

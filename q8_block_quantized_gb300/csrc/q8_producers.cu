@@ -242,9 +242,10 @@ __global__ void __launch_bounds__(NORM_THREADS)
 // ---- SwiGLU + quantization ----
 // e^x by a fixed single-precision procedure: Cody and Waite's reduction
 // x = n ln2 + r, ln2 split into 355/512 (9 significant bits: n * 355/512 is
-// exact for |n| <= 128) and the rest of ln2 rounded to single precision;
-// the Taylor polynomial of degree 7 of e^r in Horner form (|r| <= 0.35);
-// scaling by 2^n (exact).  Outside [-87, 88] the result is 0 or +infinity.
+// exact for |n| <= 128) and the rest of ln2 rounded to single precision, one
+// fused multiply-add per step; the Taylor polynomial of degree 7 of e^r in
+// Horner form, one fused multiply-add per step (|r| <= 0.35); scaling by 2^n
+// (exact).  Outside [-87, 88] the result is 0 or +infinity.
 constexpr float EXP_LOG2E = 0x1.715476p+0f;    // 1/ln 2, rounded
 constexpr float EXP_LN2_HI = 0x1.63p-1f;       // 355/512
 constexpr float EXP_LN2_LO = -0x1.bd0106p-13f; // ln 2 - 355/512, rounded
@@ -258,15 +259,15 @@ __device__ __forceinline__ float exp_cw(float x) {
   if (x > 88.0f) return __int_as_float(0x7f800000);
   if (x < -87.0f) return 0.0f;
   const float n = rintf(__fmul_rn(x, EXP_LOG2E));
-  const float r = __fsub_rn(__fsub_rn(x, __fmul_rn(n, EXP_LN2_HI)), __fmul_rn(n, EXP_LN2_LO));
+  const float r = __fmaf_rn(-n, EXP_LN2_LO, __fmaf_rn(-n, EXP_LN2_HI, x));
   float p = EXP_C7;
-  p = __fadd_rn(__fmul_rn(p, r), EXP_C6);
-  p = __fadd_rn(__fmul_rn(p, r), EXP_C5);
-  p = __fadd_rn(__fmul_rn(p, r), EXP_C4);
-  p = __fadd_rn(__fmul_rn(p, r), EXP_C3);
-  p = __fadd_rn(__fmul_rn(p, r), 0.5f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-  p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+  p = __fmaf_rn(p, r, EXP_C6);
+  p = __fmaf_rn(p, r, EXP_C5);
+  p = __fmaf_rn(p, r, EXP_C4);
+  p = __fmaf_rn(p, r, EXP_C3);
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
   return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));  // 2^n, -126 <= n <= 127
 }
 
@@ -278,24 +279,26 @@ __device__ __forceinline__ float swiglu_one(float g, float u) {
 // (row b / nbr, block b % nbr) reads 32 gate and 32 up values.  A group of 8
 // lanes takes SWIGLU_B blocks per pass (two measured slower: the kernel is
 // bound by the arithmetic of the exact e^x and division, not by latency).
+// The block index arithmetic runs in Idx (32-bit whenever the block count
+// fits: a 64-bit division per block costs as much as the block's exponentials).
 constexpr int SWIGLU_B = 1;
+template <typename Idx>
 __global__ void __launch_bounds__(SWIGLU_THREADS)
-    swiglu_quant_kernel(const float* __restrict__ gu, int64_t F, int64_t nbr, int64_t total,
-                        uint8_t* __restrict__ out) {
+    swiglu_quant_kernel(const float* __restrict__ gu, int64_t F, Idx nbr, Idx total, uint8_t* __restrict__ out) {
   pdl_launch_dependents();
   pdl_wait();
   const int sub = threadIdx.x & 7;
-  const int64_t grp = ((int64_t)blockIdx.x * SWIGLU_THREADS + threadIdx.x) >> 3;
-  const int64_t ngrp = ((int64_t)gridDim.x * SWIGLU_THREADS) >> 3;
-  for (int64_t b0 = 0; b0 < total; b0 += ngrp * SWIGLU_B) {  // same trip count in every thread
+  const Idx grp = (Idx)(((int64_t)blockIdx.x * SWIGLU_THREADS + threadIdx.x) >> 3);
+  const Idx ngrp = (Idx)(((int64_t)gridDim.x * SWIGLU_THREADS) >> 3);
+  for (Idx b0 = 0; b0 < total; b0 += ngrp * SWIGLU_B) {  // same trip count in every thread
     float4 g[SWIGLU_B], u[SWIGLU_B], v[SWIGLU_B];
 #pragma unroll
     for (int q = 0; q < SWIGLU_B; ++q) {
-      const int64_t b = b0 + grp + q * ngrp;
+      const Idx b = b0 + grp + q * ngrp;
       g[q] = u[q] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       if (b < total) {
-        const int64_t m = b / nbr, j = b - (b / nbr) * nbr;
-        const float* row = gu + m * 2 * F + j * QK + 4 * sub;
+        const Idx m = b / nbr, j = b - m * nbr;
+        const float* row = gu + (int64_t)m * 2 * F + (int64_t)j * QK + 4 * sub;
         g[q] = __ldcg(reinterpret_cast<const float4*>(row));
         u[q] = __ldcg(reinterpret_cast<const float4*>(row + F));
       }
@@ -309,8 +312,8 @@ __global__ void __launch_bounds__(SWIGLU_THREADS)
     quantize_group8<SWIGLU_B>(v, w, d);
 #pragma unroll
     for (int q = 0; q < SWIGLU_B; ++q) {
-      const int64_t b = b0 + grp + q * ngrp;
-      if (b < total) store_block_lane(out + b * BLOCK_BYTES, sub, w[q], d[q]);
+      const Idx b = b0 + grp + q * ngrp;
+      if (b < total) store_block_lane(out + (int64_t)b * BLOCK_BYTES, sub, w[q], d[q]);
     }
   }
 }
@@ -355,8 +358,12 @@ cudaError_t launch_swiglu_quantize(const float* gu, int64_t M, int64_t F, uint8_
   int64_t grid = (total + per_cta - 1) / per_cta;
   const int64_t cap = (int64_t)sm_count * 16;
   if (grid > cap) grid = cap;
-  return launch_pdl(swiglu_quant_kernel, dim3((unsigned)grid), SWIGLU_THREADS, pdl, s, gu, F, nbr, total,
-                    out);
+  // 32-bit indices while every index stays below 2^32 (b0 + ngrp included)
+  if (total + grid * per_cta < ((int64_t)1 << 32))
+    return launch_pdl(swiglu_quant_kernel<uint32_t>, dim3((unsigned)grid), SWIGLU_THREADS, pdl, s, gu, F,
+                      (uint32_t)nbr, (uint32_t)total, out);
+  return launch_pdl(swiglu_quant_kernel<int64_t>, dim3((unsigned)grid), SWIGLU_THREADS, pdl, s, gu, F, nbr,
+                    total, out);
 }
 
 }  // namespace q8
