@@ -295,11 +295,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
-// Bulk prefetch of a contiguous range into L2 (no shared-memory destination).
-// src 16-byte aligned, bytes a positive multiple of 16.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -397,20 +392,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                              uint32_t d) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
 __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void st_cluster_u16(uint32_t addr, unsigned short v) {
   asm volatile("st.shared::cluster.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 // Programmatic dependent launch: no-ops when the grid was launched normally.
@@ -439,9 +425,6 @@ __device__ __forceinline__ void load_block_quants_u16(const uint8_t* blk, uint4&
     w[k] = (uint32_t)__ldcg(p + 2 * k) | ((uint32_t)__ldcg(p + 2 * k + 1) << 16);
   a0 = make_uint4(w[0], w[1], w[2], w[3]);
   a1 = make_uint4(w[4], w[5], w[6], w[7]);
-}
-__device__ __forceinline__ uint16_t load_block_scale_bits(const uint8_t* blk) {
-  return __ldcg(reinterpret_cast<const unsigned short*>(blk));
 }
 
 // Device time limit for every spin on an mbarrier (2 s).
