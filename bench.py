@@ -242,6 +242,7 @@ def run_ours(args):
     roof = roofline(st, q8) if rank == 0 else None
     prod = producers(q8, shape) if (rank == 0 and not args.no_producers) else None
     tc5 = tcgen05_vs_default(q8, st) if (rank == 0 and world == 1 and not args.no_producers) else None
+    pre = prefill(q8, st) if (rank == 0 and world == 1 and not args.no_producers) else None
     peak, peak_kind = _peaks()
     if rank == 0:
         cpu = cpu_baseline(shape, args.M) if (world == 1 and not args.no_cpu) else None
@@ -264,6 +265,7 @@ def run_ours(args):
             "roofline": roof,
             "producers": prod,
             "tcgen05_vs_default": tc5,
+            "prefill": pre,
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
                     "h2d_bytes_per_step": st.x_all.numel() * 4,
@@ -480,6 +482,33 @@ def producers(q8, shape, launches=20):
     out["swiglu_quantize"] = rows
     torch.cuda.empty_cache()
     return out
+
+
+def prefill(q8, st, M=512, steps=3):
+    """A 512-row pass over the same projection stack (prefill of 512 tokens
+    through q8_fused_quant_gemm: 32 passes of 16 rows per GEMV, W streamed
+    once per pass), as one CUDA graph: time per step and tokens/s."""
+    import torch
+
+    from q8_block_quantized_gb300.stack import Q8Stack
+    s2 = Q8Stack(st.shape, M=M, mode="fused", layers=st.n_layers, shared_weights=st.weights)
+    g = s2.capture()
+    g.replay()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(cur)
+    for _ in range(steps):
+        g.replay()
+    b.record(cur)
+    b.synchronize()
+    ms = a.elapsed_time(b) / steps
+    res = {"M": M, "ms_per_step": round(ms, 3), "tok_s": round(M / (ms * 1e-3), 1),
+           "launches_per_step": s2.launches_per_step(),
+           "GB/s": round(s2.bytes_per_step() / (ms * 1e-3) / 1e9, 1)}
+    del g, s2
+    torch.cuda.empty_cache()
+    return res
 
 
 def tcgen05_vs_default(q8, st, M=16, steps=100):

@@ -67,7 +67,8 @@ extern "C" {
 
 #define Q8_QK 32            /* values per block                               */
 #define Q8_BLOCK_BYTES 34   /* bytes per block: fp16 scale + 32 int8          */
-#define Q8_MAX_M 64         /* most activation rows per q8_gemm call          */
+#define Q8_MAX_M 4096       /* most activation rows per q8_gemm call          */
+#define Q8_MAX_DOTS_M 64    /* most activation rows per q8_block_dots call    */
 #define Q8_MAX_TILE_ROWS 128 /* packed layout: most output rows per tile       */
 #define Q8_CHUNK_BLOCKS 8   /* packed layout: blocks per chunk                */
 
@@ -223,7 +224,13 @@ Q8_API int q8_repack_weights(const void *src_blocks, int64_t N, int64_t K, void 
  *   N         output rows, 1 <= N <= 2^31-1.
  *   K         positive multiple of 32.
  *   A_blocks  [M][K/32] activation blocks (q8_quantize_act), 2-byte aligned.
- *   M         activation rows, 1 <= M <= Q8_MAX_M.
+ *   M         activation rows, 1 <= M <= Q8_MAX_M.  Decode batches (up to
+ *             16 rows) run in one launch; more rows (prefill) run as passes
+ *             of 16 rows, each streaming W again, with the same per-row
+ *             arithmetic, so a prefill row is bitwise the row decoded alone
+ *             (Ferro README, "Exactness contract": a row's result does not
+ *             depend on the other rows of the launch).  No tile GEMM with
+ *             activation reuse is provided.
  *   y         [M][N] fp32 output, row-major, 4-byte aligned; overwritten.
  *   workspace q8_workspace_bytes(N, K, M) bytes (may be NULL when that is 0),
  *             16-byte aligned.  Its first 16384 bytes hold per-tile tickets
@@ -308,7 +315,7 @@ Q8_API int q8_unpack_weights(const void *packed, int64_t N, int64_t K,
                       void *dst_blocks, void *stream);
 
 /* Exact per-block int32 dots from packed W and activation blocks:
- * isum[m][n][b] (int32, [M][N][K/32], 4-byte aligned), 1 <= M <= Q8_MAX_M. */
+ * isum[m][n][b] (int32, [M][N][K/32], 4-byte aligned), 1 <= M <= Q8_MAX_DOTS_M. */
 Q8_API int q8_block_dots(const void *W, int64_t N, int64_t K, const void *A_blocks,
                   int M, int32_t *isum, void *stream);
 

@@ -21,7 +21,8 @@ LIB_PATH = os.path.join(_HERE, "libq8.so")
 
 QK = 32
 BLOCK_BYTES = 34
-MAX_M = 64
+MAX_M = 4096
+MAX_DOTS_M = 64
 MAX_TILE_ROWS = 128
 CHUNK_BLOCKS = 8
 FLAG_PDL = 1

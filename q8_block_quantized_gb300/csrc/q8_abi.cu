@@ -215,7 +215,7 @@ int q8_swiglu_quantize(const float* gate_up, int64_t M, int64_t F, void* out_blo
 int q8_block_dots(const void* W, int64_t N, int64_t K, const void* A_blocks, int M, int32_t* isum,
                   void* stream) {
   if (W == nullptr || A_blocks == nullptr || isum == nullptr) return Q8_EINVAL;
-  if (N <= 0 || N > INT32_MAX || !k_ok(K) || M < 1 || M > Q8_MAX_M) return Q8_ESHAPE;
+  if (N <= 0 || N > INT32_MAX || !k_ok(K) || M < 1 || M > Q8_MAX_DOTS_M) return Q8_ESHAPE;
   if (!aligned(W, 16) || !aligned(A_blocks, 2) || !aligned(isum, 4)) return Q8_EALIGN;
   DeviceInfo d;
   int st = device_ok(&d);

@@ -70,7 +70,8 @@ def test_host_argument_checks_reject_before_any_device_work(lib):
     assert g(fake, 8, 0, fake, 1, y, None, 0, 0, None) == -2           # K = 0
     assert g(fake, 0, 64, fake, 1, y, None, 0, 0, None) == -2          # N = 0
     assert g(fake, 8, 64, fake, 0, y, None, 0, 0, None) == -2          # M = 0
-    assert g(fake, 8, 64, fake, 65, y, None, 0, 0, None) == -2         # M > 64
+    assert g(fake, 8, 64, fake, 4097, y, None, 0, 0, None) == -2       # M > Q8_MAX_M
+    assert lib.q8_block_dots(fake, 8, 64, fake, 65, fake, None) == -2  # M > Q8_MAX_DOTS_M
     assert g(odd, 8, 64, fake, 1, y, None, 0, 0, None) == -3           # W misaligned
     assert g(fake, 8, 64, odd, 1, y, None, 0, 0, None) == -3           # A misaligned
     f = lib.q8_fused_quant_gemm

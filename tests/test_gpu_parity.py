@@ -335,3 +335,29 @@ def test_tcgen05_flag_gives_the_same_bits(q8, N, K, M):
     if ws is not None:  # split along K: the tickets are left zero
         assert not ws[:16384].any()
     assert q8.q8_device_error() == 0
+
+
+@pytest.mark.parametrize("N,K,M", [(300, 512, 65), (2048, 2048, 200), (1000, 3072, 1000)])
+def test_prefill_rows_equal_decode_rows(q8, N, K, M):
+    # more than 16 rows run as 16-row passes through the same kernels: every
+    # row of a prefill batch is bitwise the row computed alone (M = 1)
+    w, x = _case(N, K, M, 31)
+    W = _gpu_pack(q8, w)
+    Ab = oracle.quantize(x.numpy())
+    A = torch.from_numpy(Ab).to(DEV)
+    y = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+    q8.q8_gemm(W, N, K, A, M, y, workspace=q8.new_workspace(N, K, M))
+    yf = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+    q8.q8_fused_quant_gemm(W, N, K, x.to(DEV), M, yf, workspace=q8.new_workspace(N, K, M))
+    torch.cuda.synchronize()
+    assert torch.equal(y, yf)
+    ws1 = q8.new_workspace(N, K, 1)
+    for m in (0, 17, M // 2, M - 1):
+        y1 = torch.empty((1, N), dtype=torch.float32, device=DEV)
+        q8.q8_gemm(W, N, K, A[m:m + 1].contiguous(), 1, y1, workspace=ws1)
+        torch.cuda.synchronize()
+        assert torch.equal(y1[0], y[m]), m
+    if M * N * K <= 700_000_000:
+        y_ref, S_ref = oracle.gemm(oracle.quantize(w.numpy()), Ab, K)
+        _assert_within_tol(y, y_ref, S_ref)
+    assert q8.q8_device_error() == 0
