@@ -147,6 +147,48 @@ def cpu_baseline(shape, M, budget_s=12.0):
                       "%.1f s on 1 host thread" % (shape.name, per_rep / 1e6, M, reps, el)}
 
 
+def _cpu_slice_worker(job):
+    """One host process of the all-cores baseline: its own slice of the rows of
+    each layer-0 projection (seeded per slice), the oracle as it stands,
+    repeated for `seconds`; returns (bytes processed, elapsed seconds)."""
+    shape_name, M, idx, parts, seconds = job
+    import oracle
+    import q8_synth
+    shape = q8_synth.LLAMA_3B if shape_name == q8_synth.LLAMA_3B.name else q8_synth.LLAMA_1B
+    data = []
+    for p in shape.layer_projs():
+        n = (p.N + parts - 1) // parts
+        w = q8_synth.normal_np((n, p.K), q8_synth.WEIGHT_STD, q8_synth.derive_seed("cpu", p.name, idx))
+        x = q8_synth.normal_np((M, p.K), 1.0, q8_synth.derive_seed("cpu-x", p.name))
+        data.append((p, oracle.quantize(w), x))
+        del w
+    per_rep = sum(W.nbytes + x.nbytes + M * (W.shape[0]) * 4 for p, W, x in data)
+    for p, W, x in data:  # warm
+        oracle.quant_gemm(W, x, p.K)
+    reps, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        for p, W, x in data:
+            oracle.quant_gemm(W, x, p.K)
+        reps += 1
+    return per_rep * reps, time.perf_counter() - t0
+
+
+def cpu_baseline_all_cores(shape, M, seconds=10.0):
+    """The same oracle work on every host core: one spawned process per core,
+    each on its slice of the output rows; aggregate = all bytes / the slowest
+    process's time."""
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    jobs = [(shape.name, M, i, cores, seconds) for i in range(cores)]
+    with mp.get_context("spawn").Pool(cores) as pool:
+        res = pool.map(_cpu_slice_worker, jobs)
+    total = sum(b for b, _ in res)
+    el = max(t for _, t in res)
+    return {"value": round(total / el / 1e9, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "layer-0 projections of %s at M=%d split by output rows over %d host processes "
+                      "(one per core), oracle quantize + fp64 product, %.1f s" % (shape.name, M, cores, el)}
+
+
 # ---------------------------------------------------------------------------
 # multi-rank bookkeeping (replicas: no data-path collective)
 # ---------------------------------------------------------------------------
@@ -246,6 +288,7 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     if rank == 0:
         cpu = cpu_baseline(shape, args.M) if (world == 1 and not args.no_cpu) else None
+        cpu_all = cpu_baseline_all_cores(shape, args.M) if (world == 1 and not args.no_cpu) else None
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
@@ -267,6 +310,7 @@ def run_ours(args):
             "tcgen05_vs_default": tc5,
             "prefill": pre,
             "cpu_baseline": cpu,
+            "cpu_baseline_all_cores": cpu_all,
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
                     "h2d_bytes_per_step": st.x_all.numel() * 4,
                     "d2h_bytes_per_step": st.y_all.numel() * 4,

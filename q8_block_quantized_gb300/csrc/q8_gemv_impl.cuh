@@ -93,11 +93,10 @@ struct MCfg {
   // at 96 registers and two CTAs per SM: 0.373 ms per M = 1 step; uncapped,
   // one CTA per SM: 0.326 ms)
   static constexpr int MIN_CTAS = 1;
-  // activation staging: passes of NCW*4 blocks (8 lanes per block), STAGE_BATCH
-  // passes with their loads in flight together (larger batches measured
-  // slower for every row count; every pass of a batch is quantized, so the
-  // 256-thread kernel, whose 32-block passes cover K = 2048 in two, takes 2)
-  static constexpr int STAGE_BATCH = NCW == 8 ? 2 : 4;
+  // activation staging: passes of NCW*4 = 32 blocks (8 lanes per block),
+  // STAGE_BATCH passes with their loads in flight together (K = 2048 in one
+  // batch; larger batches measured slower for every row count)
+  static constexpr int STAGE_BATCH = 2;
   // blocks one CTA stages by itself (one batch: passes of NCW*4 blocks)
   // before the planner shares the staging among the CTAs of a cluster
   static constexpr int STAGE_TARGET = NCW * 4 * STAGE_BATCH;
