@@ -89,6 +89,7 @@ def test_host_argument_checks_reject_before_any_device_work(lib):
     assert r(fake, 8, 40, fake, None) == -2
     assert lib.q8_block_dots(fake, 8, 64, fake, 1, odd, None) == -3
     assert lib.q8_unpack_weights(fake, 8, 64, None, None) == -1
+    assert lib.q8_gemm_noalloc(fake, 8, 64, fake, 1, y, 2, None) == -1   # only Q8_FLAG_PDL there
     n = lib.q8_residual_rmsnorm_quantize
     assert n(None, None, fake, 1e-5, 1, 64, None, fake, 0, None) == -1          # null x
     assert n(fake, None, None, 1e-5, 1, 64, None, fake, 0, None) == -1          # null gamma

@@ -361,3 +361,36 @@ def test_prefill_rows_equal_decode_rows(q8, N, K, M):
         y_ref, S_ref = oracle.gemm(oracle.quantize(w.numpy()), Ab, K)
         _assert_within_tol(y, y_ref, S_ref)
     assert q8.q8_device_error() == 0
+
+
+@pytest.mark.parametrize("N,K,M", [(20_000_000, 32, 1), (20_000_000, 32, 3), (16, 1 << 20, 1), (40, 1 << 20, 5)])
+def test_extreme_shapes_sampled_against_oracle(q8, N, K, M):
+    # a very tall matrix (row and tile offsets past 2^31 bytes) and a very
+    # wide one (deep splits along K): sampled rows against the oracle, and
+    # the fused path bitwise equal to quantize + GEMV
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(N + K + M)
+    w = torch.randn((N, K), generator=gen, device=DEV) * q8_synth.WEIGHT_STD
+    x = torch.randn((M, K), generator=gen, device=DEV)
+    W = q8.pack_weights_f32(w)
+    A = q8.empty_blocks(M, K)
+    q8.q8_quantize_act(x, A)
+    ws = q8.new_workspace(N, K, M)
+    y = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    q8.q8_gemm(W, N, K, A, M, y, workspace=ws)
+    yf = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    q8.q8_fused_quant_gemm(W, N, K, x, M, yf, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y, yf)
+    rows = np.unique(np.concatenate([[0, 1, N // 2, N - 1], np.random.default_rng(N).integers(0, N, 60)]))
+    Wb = oracle.quantize(w[torch.from_numpy(rows).to(DEV)].cpu().numpy())
+    Ab = A.cpu().numpy()
+    assert np.array_equal(Ab, oracle.quantize(x.cpu().numpy()))
+    y_ref, S_ref = oracle.gemm(Wb, Ab, K)
+    err = np.abs(y[:, torch.from_numpy(rows).to(DEV)].double().cpu().numpy() - y_ref)
+    assert (err <= TOL_REL * S_ref + TOL_ABS).all(), err.max()
+    if ws is not None:
+        assert not ws[:16384].any()
+    del w, W
+    torch.cuda.empty_cache()
+    assert q8.q8_device_error() == 0
