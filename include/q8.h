@@ -301,6 +301,7 @@ Q8_API int q8_fused_quant_gemm(const void *W, int64_t N, int64_t K, const float 
  * (cudaGetSymbolAddress, with that device current); make that first call
  * before any stream capture.
  *
+ * flags is 0 or Q8_FLAG_PDL (the tcgen05 option is not offered here).
  * Arguments, alignment and errors otherwise as q8_gemm.
  */
 #define Q8_NOALLOC_SCRATCH_BYTES (4u << 20)
