@@ -524,6 +524,26 @@ def producers(q8, shape, launches=20):
     guo = q8_synth.normal_np((1, 2 * F), 1.0, 8)
     rows["oracle_us_decode"] = round(oracle_us(lambda: oracle.swiglu_quantize(guo, F)), 2)
     out["swiglu_quantize"] = rows
+    # SwiGLU in the gate/up GEMV's epilogue against the GEMV followed by the
+    # separate SwiGLU kernel (one decode row, each chained with PDL)
+    if q8.q8_packed_tile_rows(2 * F) in (64, 128):
+        gate = q8_synth.normal_torch((F, K), q8_synth.WEIGHT_STD, 9, dev)
+        up = q8_synth.normal_torch((F, K), q8_synth.WEIGHT_STD, 10, dev)
+        Wgu = q8.pack_weights_f32(q8.interleave_gate_up(gate, up))
+        del gate, up
+        x1 = q8_synth.normal_torch((1, K), 1.0, 11, dev)
+        y1 = torch.empty((1, 2 * F), dtype=torch.float32, device=dev)
+        hb = q8.empty_blocks(1, F)
+        ws = q8.new_workspace(2 * F, K, 1)
+        us_epi = timed(lambda f: q8.q8_fused_quant_gemm_swiglu(Wgu, F, K, x1, 1, hb, flags=f), True)
+
+        def two(f):
+            q8.q8_fused_quant_gemm(Wgu, 2 * F, K, x1, 1, y1, workspace=ws, flags=f)
+            q8.q8_swiglu_quantize(y1, hb, flags=f)
+        us_two = timed(two, True)
+        out["swiglu_epilogue"] = {"M": 1, "F": F, "K": K, "us_gemv_with_epilogue": round(us_epi, 3),
+                                  "us_gemv_then_swiglu": round(us_two, 3)}
+        del Wgu
     torch.cuda.empty_cache()
     return out
 

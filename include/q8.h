@@ -278,6 +278,34 @@ Q8_API int q8_fused_quant_gemm(const void *W, int64_t N, int64_t K, const float 
                         size_t workspace_bytes, unsigned flags, void *stream);
 
 /*
+ * q8_gemm_swiglu / q8_fused_quant_gemm_swiglu -- the gate/up GEMV with SwiGLU
+ * in its epilogue: it writes the quantized input of the down projection,
+ * q8_quantize_act(silu(gate) * up), instead of y (Ferro README, "How the iGPU
+ * path is fast", item 3: SwiGLU emits the next GEMM's int8 input directly).
+ * One launch replaces the GEMV and q8_swiglu_quantize.  silu and the
+ * rounding are those of q8_swiglu_quantize, applied to the outputs this GEMV
+ * computes (bitwise those of q8_gemm / q8_fused_quant_gemm on the same W).
+ *
+ *   W          packed (q8_repack_weights) N = 2F rows of K, 16-byte aligned,
+ *              whose rows are gate and up interleaved in groups of G =
+ *              q8_packed_tile_rows(2F) / 2 rows: for every g, rows
+ *              [2gG, 2gG + G) are gate rows [gG, gG + G) and rows
+ *              [2gG + G, 2gG + 2G) are up rows [gG, gG + G).
+ *   F          outputs per row of h; q8_packed_tile_rows(2F) must be 64 or
+ *              128 and F a multiple of G, else Q8_ESHAPE.
+ *   K, M       as q8_gemm; the product must not need a split along K for
+ *              this M (true for F >= 2432 with 64-row tiles, F >= 4864
+ *              with 128-row tiles, and K <= 8192), else Q8_ESHAPE.
+ *   A_blocks / x  the activations, as q8_gemm / q8_fused_quant_gemm.
+ *   out_blocks [M][F/32] blocks of h (2-byte aligned).
+ *   flags      0 or Q8_FLAG_PDL.  No workspace is needed.
+ */
+Q8_API int q8_gemm_swiglu(const void *W, int64_t F, int64_t K, const void *A_blocks, int M,
+                          void *out_blocks, unsigned flags, void *stream);
+Q8_API int q8_fused_quant_gemm_swiglu(const void *W, int64_t F, int64_t K, const float *x, int M,
+                                      void *out_blocks, unsigned flags, void *stream);
+
+/*
  * q8_gemm_noalloc -- q8_gemm without a workspace argument, for callers that
  * cannot allocate device memory (for example a plugin inside an application
  * whose own allocator owns the device, or a latency-critical loop that must

@@ -48,6 +48,8 @@ SIGNATURES = {
     "q8_gemm": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _vp, _sz, _u, _vp]),
     "q8_fused_quant_gemm": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _vp, _vp, _sz, _u, _vp]),
     "q8_gemm_noalloc": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _u, _vp]),
+    "q8_gemm_swiglu": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _u, _vp]),
+    "q8_fused_quant_gemm_swiglu": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _u, _vp]),
     "q8_unpack_weights": (_int, [_vp, _i64, _i64, _vp, _vp]),
     "q8_block_dots": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _vp]),
     "q8_device_error": (_int, [ctypes.POINTER(ctypes.c_uint)]),
@@ -193,6 +195,35 @@ def q8_gemm_noalloc(W: torch.Tensor, N: int, K: int, A_blocks: torch.Tensor, M: 
         _dev(W, torch.uint8, "W"), N, K, _dev(A_blocks, torch.uint8, "A_blocks"), M,
         _dev(y, torch.float32, "y"), flags, _stream(stream)))
     return y
+
+
+def q8_gemm_swiglu(W: torch.Tensor, F: int, K: int, A_blocks: torch.Tensor, M: int,
+                   out_blocks: torch.Tensor, flags: int = 0, stream=None):
+    """The gate/up GEMV with SwiGLU in its epilogue (W rows interleaved, see
+    interleave_gate_up): out_blocks = quantized silu(gate) * up."""
+    _check("q8_gemm_swiglu", lib().q8_gemm_swiglu(
+        _dev(W, torch.uint8, "W"), F, K, _dev(A_blocks, torch.uint8, "A_blocks"), M,
+        _dev(out_blocks, torch.uint8, "out_blocks"), flags, _stream(stream)))
+    return out_blocks
+
+
+def q8_fused_quant_gemm_swiglu(W: torch.Tensor, F: int, K: int, x: torch.Tensor, M: int,
+                               out_blocks: torch.Tensor, flags: int = 0, stream=None):
+    _check("q8_fused_quant_gemm_swiglu", lib().q8_fused_quant_gemm_swiglu(
+        _dev(W, torch.uint8, "W"), F, K, _dev(x, torch.float32, "x"), M,
+        _dev(out_blocks, torch.uint8, "out_blocks"), flags, _stream(stream)))
+    return out_blocks
+
+
+def interleave_gate_up(gate: torch.Tensor, up: torch.Tensor) -> torch.Tensor:
+    """[F][K] gate and up rows -> the [2F][K] row order q8_gemm_swiglu expects:
+    groups of G = q8_packed_tile_rows(2F) / 2 gate rows, each followed by the
+    up rows of the same indices (a copy; no arithmetic)."""
+    F, K = gate.shape
+    G = q8_packed_tile_rows(2 * F) // 2
+    if G < 32 or F % G:
+        raise ValueError("F = %d has no SwiGLU epilogue layout (group %d)" % (F, G))
+    return torch.stack([gate.reshape(F // G, G, K), up.reshape(F // G, G, K)], dim=1).reshape(2 * F, K)
 
 
 # ---- test hooks ----------------------------------------------------------------

@@ -71,6 +71,29 @@ int check_workspace(const GemvPlan& p, void* ws, size_t ws_bytes) {
   return Q8_OK;
 }
 
+// The SwiGLU epilogue's extra conditions: 64- or 128-row tiles holding whole
+// gate/up groups, and no split along K (checked on the plan).
+int swiglu_gemm(const void* W, int64_t F, int64_t K, const void* A_blocks, const float* x, int M,
+                void* out_blocks, void* workspace, size_t workspace_bytes, unsigned flags, void* stream) {
+  if (W == nullptr || out_blocks == nullptr || (A_blocks == nullptr && x == nullptr)) return Q8_EINVAL;
+  if ((flags & ~Q8_FLAG_PDL) != 0) return Q8_EINVAL;
+  if (F <= 0 || F > INT32_MAX / 2 || !k_ok(K) || M < 1 || M > Q8_MAX_M) return Q8_ESHAPE;
+  const int R = layout_tile_rows(2 * F);
+  if ((R != 64 && R != 128) || F % (R / 2) != 0) return Q8_ESHAPE;
+  if (!aligned(W, 16) || !aligned(out_blocks, 2)) return Q8_EALIGN;
+  if ((A_blocks != nullptr && !aligned(A_blocks, 2)) || (x != nullptr && !aligned(x, 16))) return Q8_EALIGN;
+  DeviceInfo d;
+  int st = device_ok(&d);
+  if (st != Q8_OK) return st;
+  GemvPlan p;
+  if (!plan_gemv(d, 2 * F, K, M, x != nullptr, false, &p) || p.S != 1) return Q8_ESHAPE;
+  (void)workspace;
+  (void)workspace_bytes;  // no split along K: no workspace is used
+  return cuda_status(launch_gemv(p, static_cast<const uint8_t*>(W), static_cast<const uint8_t*>(A_blocks), x,
+                                 nullptr, nullptr, nullptr, (flags & Q8_FLAG_PDL) != 0,
+                                 static_cast<cudaStream_t>(stream), static_cast<uint8_t*>(out_blocks)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -211,6 +234,19 @@ int q8_swiglu_quantize(const float* gate_up, int64_t M, int64_t F, void* out_blo
   return cuda_status(launch_swiglu_quantize(gate_up, M, F, static_cast<uint8_t*>(out_blocks), d.sm_count,
                                             (flags & Q8_FLAG_PDL) != 0, static_cast<cudaStream_t>(stream)));
 }
+
+int q8_gemm_swiglu(const void* W, int64_t F, int64_t K, const void* A_blocks, int M, void* out_blocks,
+                   unsigned flags, void* stream) {
+  if (A_blocks == nullptr) return Q8_EINVAL;
+  return swiglu_gemm(W, F, K, A_blocks, nullptr, M, out_blocks, nullptr, 0, flags, stream);
+}
+
+int q8_fused_quant_gemm_swiglu(const void* W, int64_t F, int64_t K, const float* x, int M, void* out_blocks,
+                               unsigned flags, void* stream) {
+  if (x == nullptr) return Q8_EINVAL;
+  return swiglu_gemm(W, F, K, nullptr, x, M, out_blocks, nullptr, 0, flags, stream);
+}
+
 
 int q8_block_dots(const void* W, int64_t N, int64_t K, const void* A_blocks, int M, int32_t* isum,
                   void* stream) {

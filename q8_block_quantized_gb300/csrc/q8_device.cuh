@@ -187,6 +187,54 @@ __device__ __forceinline__ void quantize_group8(const float4 (&v)[B], uint32_t (
 }
 
 // ---------------------------------------------------------------------------
+// Fused producers' arithmetic, shared by their kernels and the GEMV's SwiGLU
+// epilogue.
+// ---------------------------------------------------------------------------
+// The 8 lanes of a group store one block: lane s the quants of values
+// 4s..4s+3 (bytes 2+4s..5+4s, 2-byte aligned), lane 0 also the scale.
+__device__ __forceinline__ void store_block_lane(uint8_t* ob, int sub, uint32_t w, float d) {
+  uint16_t* o16 = reinterpret_cast<uint16_t*>(ob);
+  o16[1 + 2 * sub] = (uint16_t)(w & 0xffffu);
+  o16[2 + 2 * sub] = (uint16_t)(w >> 16);
+  if (sub == 0) o16[0] = __half_as_ushort(__float2half_rn(d));  // d is a binary16 value: exact
+}
+
+// e^x by a fixed single-precision procedure: Cody and Waite's reduction
+// x = n ln2 + r, ln2 split into 355/512 (9 significant bits: n * 355/512 is
+// exact for |n| <= 128) and the rest of ln2 rounded to single precision, one
+// fused multiply-add per step; the Taylor polynomial of degree 7 of e^r in
+// Horner form, one fused multiply-add per step (|r| <= 0.35); scaling by 2^n
+// (exact).  Outside [-87, 88] the result is 0 or +infinity.
+constexpr float EXP_LOG2E = 0x1.715476p+0f;    // 1/ln 2, rounded
+constexpr float EXP_LN2_HI = 0x1.63p-1f;       // 355/512
+constexpr float EXP_LN2_LO = -0x1.bd0106p-13f; // ln 2 - 355/512, rounded
+constexpr float EXP_C3 = 0x1.555556p-3f;       // 1/3!
+constexpr float EXP_C4 = 0x1.555556p-5f;       // 1/4!
+constexpr float EXP_C5 = 0x1.111112p-7f;       // 1/5!
+constexpr float EXP_C6 = 0x1.6c16c2p-10f;      // 1/6!
+constexpr float EXP_C7 = 0x1.a01a02p-13f;      // 1/7!
+
+__device__ __forceinline__ float exp_cw(float x) {
+  if (x > 88.0f) return __int_as_float(0x7f800000);
+  if (x < -87.0f) return 0.0f;
+  const float n = rintf(__fmul_rn(x, EXP_LOG2E));
+  const float r = __fmaf_rn(-n, EXP_LN2_LO, __fmaf_rn(-n, EXP_LN2_HI, x));
+  float p = EXP_C7;
+  p = __fmaf_rn(p, r, EXP_C6);
+  p = __fmaf_rn(p, r, EXP_C5);
+  p = __fmaf_rn(p, r, EXP_C4);
+  p = __fmaf_rn(p, r, EXP_C3);
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));  // 2^n, -126 <= n <= 127
+}
+
+__device__ __forceinline__ float swiglu_one(float g, float u) {
+  return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, exp_cw(-g))), u);
+}
+
+// ---------------------------------------------------------------------------
 // int8 block dot (exact int32) and the canonical block term.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int dot_block(const uint4& w0, const uint4& w1, const uint4& a0,

@@ -11,12 +11,12 @@
 namespace q8 {
 
 template <int R>
-cudaError_t launch_gemv_r(const GemvArgs& args, int MT, bool fused, bool u5, int grid, int cluster, bool pdl,
+cudaError_t launch_gemv_r(const GemvArgs& args, int MT, bool fused, int var, int grid, int cluster, bool pdl,
                          cudaStream_t s);
 template <int R>
-int occupancy_r(int MT, bool fused, bool u5);
+int occupancy_r(int MT, bool fused, int var);
 template <int R>
-bool cluster_fits_r(int MT, bool fused, bool u5, int cluster);
+bool cluster_fits_r(int MT, bool fused, int var, int cluster);
 
 namespace {
 
@@ -40,10 +40,10 @@ cudaError_t error_word(int dev, unsigned** out) {
 
 int occupancy(int R, int MT, bool fused, bool u5) {
   switch (R) {
-    case 16: return occupancy_r<16>(MT, fused, u5);
-    case 32: return occupancy_r<32>(MT, fused, u5);
-    case 64: return occupancy_r<64>(MT, fused, u5);
-    default: return occupancy_r<128>(MT, fused, u5);
+    case 16: return occupancy_r<16>(MT, fused, u5 ? VAR_TCGEN05 : VAR_DEFAULT);
+    case 32: return occupancy_r<32>(MT, fused, u5 ? VAR_TCGEN05 : VAR_DEFAULT);
+    case 64: return occupancy_r<64>(MT, fused, u5 ? VAR_TCGEN05 : VAR_DEFAULT);
+    default: return occupancy_r<128>(MT, fused, u5 ? VAR_TCGEN05 : VAR_DEFAULT);
   }
 }
 
@@ -59,10 +59,10 @@ bool cluster_fits(int R, int MT, bool fused, bool u5, int c) {
   if (v == 0) {
     bool ok;
     switch (R) {
-      case 16: ok = cluster_fits_r<16>(MT, fused, u5, c); break;
-      case 32: ok = cluster_fits_r<32>(MT, fused, u5, c); break;
-      case 64: ok = cluster_fits_r<64>(MT, fused, u5, c); break;
-      default: ok = cluster_fits_r<128>(MT, fused, u5, c); break;
+      case 16: ok = cluster_fits_r<16>(MT, fused, u5 ? VAR_TCGEN05 : VAR_DEFAULT, c); break;
+      case 32: ok = cluster_fits_r<32>(MT, fused, u5 ? VAR_TCGEN05 : VAR_DEFAULT, c); break;
+      case 64: ok = cluster_fits_r<64>(MT, fused, u5 ? VAR_TCGEN05 : VAR_DEFAULT, c); break;
+      default: ok = cluster_fits_r<128>(MT, fused, u5 ? VAR_TCGEN05 : VAR_DEFAULT, c); break;
     }
     v = ok ? 1 : -1;
   }
@@ -80,7 +80,7 @@ int stage_target_of(int MT) {
   }
 }
 int budget_of(int R, int MT, bool u5) {
-  if (u5 && R == 128 && MT == 16) return act_budget<128, 16, true>();  // the tcgen05 path's smaller area
+  if (u5 && R == 128 && MT == 16) return act_budget<128, 16, VAR_TCGEN05>();  // the tcgen05 path's smaller area
   switch (MT) {
     case 1: return MCfg<1>::ACT_BUDGET;
     case 2: return MCfg<2>::ACT_BUDGET;
@@ -168,7 +168,8 @@ bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, b
 }
 
 cudaError_t launch_gemv(const GemvPlan& p, const uint8_t* W, const uint8_t* A, const float* x,
-                        uint8_t* A_out, float* y, void* workspace, bool pdl, cudaStream_t s) {
+                        uint8_t* A_out, float* y, void* workspace, bool pdl, cudaStream_t s,
+                        uint8_t* h_blocks) {
   const bool fused = (x != nullptr);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -182,7 +183,8 @@ cudaError_t launch_gemv(const GemvPlan& p, const uint8_t* W, const uint8_t* A, c
     args.A = A ? A + (size_t)m0 * p.NB * BLOCK_BYTES : nullptr;
     args.x = x ? x + (size_t)m0 * p.K : nullptr;
     args.A_out = A_out ? A_out + (size_t)m0 * p.NB * BLOCK_BYTES : nullptr;
-    args.y = y + (size_t)m0 * p.N;
+    args.y = y != nullptr ? y + (size_t)m0 * p.N : nullptr;
+    args.h_blocks = h_blocks != nullptr ? h_blocks + (size_t)m0 * (p.N / 64) * BLOCK_BYTES : nullptr;
     args.ws_cnt = p.S > 1 ? reinterpret_cast<unsigned*>(workspace) : nullptr;
     args.ws_part = p.S > 1 ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(workspace) + TICKET_BYTES)
                            : nullptr;
@@ -206,11 +208,14 @@ cudaError_t launch_gemv(const GemvPlan& p, const uint8_t* W, const uint8_t* A, c
     // shared memory for the unit's staged activations only (a launch with a
     // short K range does not reserve the whole budget)
     args.act_smem = (act_bytes(MT, 128 / p.R, p.RU) + 15) / 16 * 16;
+    // kernel variant: the SwiGLU epilogue when h_blocks is given, the tcgen05
+    // block dots when the plan asks for them (16-row passes), else the default
+    const int var = h_blocks != nullptr ? VAR_SWIGLU : (p.u5 && MT == 16) ? VAR_TCGEN05 : VAR_DEFAULT;
     switch (p.R) {
-      case 16: e = launch_gemv_r<16>(args, MT, fused, p.u5 && MT == 16, p.grid, p.cluster, pdl, s); break;
-      case 32: e = launch_gemv_r<32>(args, MT, fused, p.u5 && MT == 16, p.grid, p.cluster, pdl, s); break;
-      case 64: e = launch_gemv_r<64>(args, MT, fused, p.u5 && MT == 16, p.grid, p.cluster, pdl, s); break;
-      default: e = launch_gemv_r<128>(args, MT, fused, p.u5 && MT == 16, p.grid, p.cluster, pdl, s); break;
+      case 16: e = launch_gemv_r<16>(args, MT, fused, var, p.grid, p.cluster, pdl, s); break;
+      case 32: e = launch_gemv_r<32>(args, MT, fused, var, p.grid, p.cluster, pdl, s); break;
+      case 64: e = launch_gemv_r<64>(args, MT, fused, var, p.grid, p.cluster, pdl, s); break;
+      default: e = launch_gemv_r<128>(args, MT, fused, var, p.grid, p.cluster, pdl, s); break;
     }
     if (e != cudaSuccess) return e;
   }

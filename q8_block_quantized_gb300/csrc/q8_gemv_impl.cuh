@@ -110,7 +110,11 @@ struct MCfg {
 // Activation rows at or above this use the tensor-core path.
 constexpr int TC_MIN_MT = 8;
 
-// 5th-generation tensor-core path (tcgen05), selected per call (U5): tiles
+// Kernel variants (template parameter V): the default, the tcgen05 block
+// dots (VAR_TCGEN05) and the SwiGLU epilogue (VAR_SWIGLU).
+constexpr int VAR_DEFAULT = 0, VAR_TCGEN05 = 1, VAR_SWIGLU = 2;
+
+// 5th-generation tensor-core path (tcgen05), selected per call: tiles
 // of 128 rows (one chunk per round) with 16 activation rows.  Each round the consumer warps convert
 // the chunk's int8 weights and the round's activation blocks exactly to fp16
 // in the MMA's canonical layout (no swizzle, K-major: core matrices of 8 rows
@@ -119,9 +123,9 @@ constexpr int TC_MIN_MT = 8;
 // fp32 accumulator per block: every partial sum is an integer below 2^24, so
 // it holds the exact block dot), and the consumers read the block dots back
 // for the canonical terms and trees.
-template <int R, int MT, bool U5>
+template <int R, int MT, int V>
 struct UCfg {
-  static constexpr bool ON = U5 && R == 128 && MT == 16;
+  static constexpr bool ON = V == VAR_TCGEN05 && R == 128 && MT == 16;
   static constexpr int SLICE_A = 128 * 16 * 2;  // one 16-wide k slice of the 128 weight rows, fp16
   static constexpr int SLICE_B = MT * 16 * 2;   // the same slice of the activation rows
   static constexpr int A_BYTES = ON ? 2 * CHUNK_BLOCKS * SLICE_A : 0;
@@ -145,18 +149,18 @@ __host__ __device__ constexpr int act_bytes(int MT, int P, int RU) {
 
 // bytes of staged activations a unit may use: MCfg's budget, or on the
 // tcgen05 path what the stages and the fp16 operands leave of SMEM_LIMIT
-template <int R, int MT, bool U5>
+template <int R, int MT, int V>
 __host__ __device__ constexpr int act_budget() {
-  return UCfg<R, MT, U5>::ON
-             ? (SMEM_LIMIT - MCfg<MT>::STAGES * RCfg<R>::STAGE_BYTES - UCfg<R, MT, U5>::A_BYTES -
-                UCfg<R, MT, U5>::B_BYTES - 2 * MCfg<MT>::STAGES * 8 - UCfg<R, MT, U5>::MISC_INTS * 4) / 16 * 16
+  return UCfg<R, MT, V>::ON
+             ? (SMEM_LIMIT - MCfg<MT>::STAGES * RCfg<R>::STAGE_BYTES - UCfg<R, MT, V>::A_BYTES -
+                UCfg<R, MT, V>::B_BYTES - 2 * MCfg<MT>::STAGES * 8 - UCfg<R, MT, V>::MISC_INTS * 4) / 16 * 16
              : MCfg<MT>::ACT_BUDGET;
 }
 
-template <int R, int MT, bool U5>
+template <int R, int MT, int V>
 __host__ __device__ constexpr int ru_max() {
   int c = MAX_ROUNDS_PER_UNIT;
-  while (c > 1 && act_bytes(MT, RCfg<R>::P, c) > act_budget<R, MT, U5>()) c >>= 1;
+  while (c > 1 && act_bytes(MT, RCfg<R>::P, c) > act_budget<R, MT, V>()) c >>= 1;
   return c;
 }
 __host__ __device__ constexpr int log2_floor(int v) { return v <= 1 ? 0 : 1 + log2_floor(v >> 1); }
@@ -171,17 +175,17 @@ constexpr int red_stride() {
 // per-round exchange of chunk values between the parts of a row (and, on
 // the tensor path, from the MMA fragment layout to one thread per row):
 // [2 buffers][P parts][R rows][red_stride]
-template <int R, int MT, bool U5>
+template <int R, int MT, int V>
 constexpr int red_bytes() {
-  return !UCfg<R, MT, U5>::ON && (RCfg<R>::P > 1 || MT >= TC_MIN_MT || MCfg<MT>::HALVES > 1)
+  return !UCfg<R, MT, V>::ON && (RCfg<R>::P > 1 || MT >= TC_MIN_MT || MCfg<MT>::HALVES > 1)
              ? 2 * MCfg<MT>::HALVES * 128 * red_stride<MT>() * 4
              : 0;
 }
 
-template <int R, int MT, bool U5>
-constexpr size_t gemv_smem_bytes(int act = act_budget<R, MT, U5>()) {
-  return (size_t)MCfg<MT>::STAGES * RCfg<R>::STAGE_BYTES + UCfg<R, MT, U5>::A_BYTES + UCfg<R, MT, U5>::B_BYTES + act +
-         red_bytes<R, MT, U5>() + 2 * MCfg<MT>::STAGES * sizeof(uint64_t) + UCfg<R, MT, U5>::MISC_INTS * sizeof(int);
+template <int R, int MT, int V>
+constexpr size_t gemv_smem_bytes(int act = act_budget<R, MT, V>()) {
+  return (size_t)MCfg<MT>::STAGES * RCfg<R>::STAGE_BYTES + UCfg<R, MT, V>::A_BYTES + UCfg<R, MT, V>::B_BYTES + act +
+         red_bytes<R, MT, V>() + 2 * MCfg<MT>::STAGES * sizeof(uint64_t) + UCfg<R, MT, V>::MISC_INTS * sizeof(int);
 }
 
 struct GemvArgs {
@@ -190,6 +194,7 @@ struct GemvArgs {
   const float* x;        // fp32 activations [M][K] (fused)
   uint8_t* A_out;        // fused: optional activation blocks out
   float* y;              // [M][N]
+  uint8_t* h_blocks;     // SwiGLU epilogue: blocks of silu(gate) * up [M][N/64], or null (y written)
   float* ws_part;        // [S][M][N] partials (S > 1)
   unsigned* ws_cnt;      // [T] tickets (S > 1)
   unsigned* err;         // device error word
@@ -592,27 +597,57 @@ __device__ __forceinline__ float tree_of(const float* w, int stride, int hstride
   }
 }
 
-template <int R, int MT, bool FUSED, bool U5>
+// SwiGLU epilogue of one tile: ysm holds the tile's outputs [R][MT] (the
+// first R/2 rows gate rows j, the last R/2 the up rows of the same j); 8
+// lanes per 32 consecutive j form h = silu(gate) * up and quantize it into
+// block t * R/64 + jb of each activation row (only in the VAR_SWIGLU
+// kernels, so the other kernels' registers are untouched).
+template <int R, int MT, int NT>
+__device__ __forceinline__ void swiglu_epilogue(const float* ysm, uint8_t* h_blocks, int64_t N, int M, int t,
+                                             bool ok) {
+  constexpr int JB = R / 64;  // output blocks per tile and row
+  const int sub = threadIdx.x & 7, grp = threadIdx.x >> 3;
+  for (int t0 = 0; t0 < MT * JB; t0 += NT / 8) {  // the same trip count in every thread
+    const int task = t0 + grp;
+    const int m = task / JB, jb = task - (task / JB) * JB;
+    const bool on = ok && task < MT * JB && m < M;
+    float hv[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (on) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int jj = jb * 32 + 4 * sub + e;
+        hv[e] = swiglu_one(ysm[jj * MT + m], ysm[(R / 2 + jj) * MT + m]);
+      }
+    }
+    float4 v[1] = {make_float4(hv[0], hv[1], hv[2], hv[3])};
+    uint32_t w[1];
+    float d[1];
+    quantize_group8<1>(v, w, d);
+    if (on) store_block_lane(h_blocks + ((int64_t)m * (N / 64) + (int64_t)t * JB + jb) * BLOCK_BYTES, sub, w[0], d[0]);
+  }
+}
+
+template <int R, int MT, bool FUSED, int V>
 __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_kernel(const GemvArgs a) {
   constexpr int P = RCfg<R>::P;
   constexpr int NCW = MCfg<MT>::NCW;
   constexpr int NT = NCW * 32;  // consumer threads
   constexpr int STAGES = MCfg<MT>::STAGES;
-  constexpr int LV = log2_floor(ru_max<R, MT, U5>()) + 1;
+  constexpr int LV = log2_floor(ru_max<R, MT, V>()) + 1;
   constexpr bool TC = MT >= TC_MIN_MT;  // tensor-core path
   constexpr int HALVES = MCfg<MT>::HALVES;
   constexpr bool EXCHANGE = (P > 1) || TC || (HALVES > 1);
   constexpr int RS = red_stride<MT>();
   constexpr int BAR_CONSUMERS = 1;  // named barrier of the consumer warps
-  constexpr bool UM = UCfg<R, MT, U5>::ON;  // tcgen05 path
+  constexpr bool UM = UCfg<R, MT, V>::ON;  // tcgen05 path
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stage_buf = smem;
   uint8_t* umA = smem + (size_t)STAGES * RCfg<R>::STAGE_BYTES;  // fp16 operands (tcgen05 path)
-  uint8_t* umB = umA + UCfg<R, MT, U5>::A_BYTES;
-  uint8_t* act_base = umB + UCfg<R, MT, U5>::B_BYTES;
+  uint8_t* umB = umA + UCfg<R, MT, V>::A_BYTES;
+  uint8_t* act_base = umB + UCfg<R, MT, V>::B_BYTES;
   // the activation area is sized per launch (the unit's blocks), the rest follows it
   float* red = reinterpret_cast<float*>(act_base + a.act_smem);  // [2][HALVES][P][R][RS]
-  uint64_t* full = reinterpret_cast<uint64_t*>(act_base + a.act_smem + red_bytes<R, MT, U5>());
+  uint64_t* full = reinterpret_cast<uint64_t*>(act_base + a.act_smem + red_bytes<R, MT, V>());
   uint64_t* empty = full + STAGES;
   volatile int* misc = reinterpret_cast<volatile int*>(empty + STAGES);
   // misc[0]: abort flag, misc[1]: "this CTA combines the tile", misc[2]: rounds issued;
@@ -662,7 +697,7 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
   uint32_t tmem = 0;     // tensor memory of the block dots (tcgen05 path)
   uint32_t mphase = 0;   // parity of the MMA mbarrier's next completion
   if constexpr (UM) {
-    if (warp == 0) tmem_alloc(tmem_slot, UCfg<R, MT, U5>::TMEM_COLS);
+    if (warp == 0) tmem_alloc(tmem_slot, UCfg<R, MT, V>::TMEM_COLS);
     tc_fence_before_sync();
     named_bar_sync(BAR_CONSUMERS, NT);
     tc_fence_after_sync();
@@ -746,13 +781,13 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
           for (int task = threadIdx.x; task < kb * 2 * 128; task += NT) {
             const int row = task & 127, jh = task >> 7;  // jh = 2 * block + half
             const uint4 q = row < r ? lds128(cq + chunk_quant_off(jh >> 1, jh & 1, row, r)) : make_uint4(0u, 0u, 0u, 0u);
-            store_f16_slice(umA + jh * UCfg<R, MT, U5>::SLICE_A + (row >> 3) * 256 + (row & 7) * 16, q);
+            store_f16_slice(umA + jh * UCfg<R, MT, V>::SLICE_A + (row >> 3) * 256 + (row & 7) * 16, q);
           }
 #pragma unroll 1
           for (int task = threadIdx.x; task < kb * 2 * MT; task += NT) {
             const int m = task % MT, jh = task / MT;
             const uint4 q = lds128(L.q + m * L.mq + (rho * CHUNK_BLOCKS + (jh >> 1)) * 32 + (jh & 1) * 16);
-            store_f16_slice(umB + jh * UCfg<R, MT, U5>::SLICE_B + (m >> 3) * 256 + (m & 7) * 16, q);
+            store_f16_slice(umB + jh * UCfg<R, MT, V>::SLICE_B + (m >> 3) * 256 + (m & 7) * 16, q);
           }
         }
         fence_proxy_async_smem();
@@ -763,8 +798,8 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
           constexpr uint32_t IDESC = umma_idesc_f16(128, MT);
           for (int jh = 0; jh < 2 * kb; ++jh)
             umma_f16(tmem + (uint32_t)(MT * (jh >> 1)),
-                     umma_smem_desc(smem_u32(umA + jh * UCfg<R, MT, U5>::SLICE_A), 128, 256),
-                     umma_smem_desc(smem_u32(umB + jh * UCfg<R, MT, U5>::SLICE_B), 128, 256), IDESC, (jh & 1) != 0);
+                     umma_smem_desc(smem_u32(umA + jh * UCfg<R, MT, V>::SLICE_A), 128, 256),
+                     umma_smem_desc(smem_u32(umB + jh * UCfg<R, MT, V>::SLICE_B), 128, 256), IDESC, (jh & 1) != 0);
           umma_commit(mma_bar);
         }
         bool done = false;
@@ -933,12 +968,27 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
     }
 
     if (a.S == 1) {
-      if (ok && merger && i < r) {
+      if constexpr (V != VAR_SWIGLU) {
+        if (ok && merger && i < r) {
 #pragma unroll
-        for (int c = 0; c < MC; ++c) {
-          const int m = mcg * MC + c;
-          if (m < a.M) a.y[(int64_t)m * a.N + n] = pv[c];
+          for (int c = 0; c < MC; ++c) {
+            const int m = mcg * MC + c;
+            if (m < a.M) a.y[(int64_t)m * a.N + n] = pv[c];
+          }
         }
+      } else {
+        // SwiGLU epilogue: the outputs meet in the exchange buffer ([R][MT],
+        // after every thread is past the last round's exchange), then
+        // swiglu_epilogue forms and quantizes h.
+        float* ysm = red;
+        named_bar_sync(BAR_CONSUMERS, NT);
+        if (merger) {
+#pragma unroll
+          for (int c = 0; c < MC; ++c) ysm[i * MT + mcg * MC + c] = pv[c];
+        }
+        named_bar_sync(BAR_CONSUMERS, NT);
+        swiglu_epilogue<R, MT, NT>(ysm, a.h_blocks, a.N, a.M, t, ok);
+        named_bar_sync(BAR_CONSUMERS, NT);  // the exchange buffer is free for the next unit
       }
       continue;
     }
@@ -1028,32 +1078,32 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
     if (warp == 0) {
       if (lane == 0 && misc[0]) (void)mbar_wait_bounded(mma_bar, mphase, WAIT_LIMIT_NS / 4);
       __syncwarp();
-      tmem_dealloc(tmem, UCfg<R, MT, U5>::TMEM_COLS);
+      tmem_dealloc(tmem, UCfg<R, MT, V>::TMEM_COLS);
     }
   }
 }
 
 // Every libq8 kernel asks for the largest shared-memory carveout (the same
 // for all, so an SM switching between kernels needs no reconfiguration).
-template <int R, int MT, bool FUSED, bool U5>
+template <int R, int MT, bool FUSED, int V>
 cudaError_t set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<R, MT, FUSED, U5>,
+  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<R, MT, FUSED, V>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)gemv_smem_bytes<R, MT, U5>());
+                                       (int)gemv_smem_bytes<R, MT, V>());
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gemv_kernel<R, MT, FUSED, U5>,
+  return cudaFuncSetAttribute(gemv_kernel<R, MT, FUSED, V>,
                               cudaFuncAttributePreferredSharedMemoryCarveout,
                               (int)cudaSharedmemCarveoutMaxShared);
 }
 
-template <int R, int MT, bool FUSED, bool U5>
+template <int R, int MT, bool FUSED, int V>
 cudaError_t launch_gemv_t(const GemvArgs& args, int grid, int cluster, bool pdl, cudaStream_t s) {
-  cudaError_t e = set_attributes<R, MT, FUSED, U5>();
+  cudaError_t e = set_attributes<R, MT, FUSED, V>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(MCfg<MT>::THREADS);
-  cfg.dynamicSmemBytes = gemv_smem_bytes<R, MT, U5>(args.act_smem);
+  cfg.dynamicSmemBytes = gemv_smem_bytes<R, MT, V>(args.act_smem);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   int na = 0;
@@ -1071,27 +1121,27 @@ cudaError_t launch_gemv_t(const GemvArgs& args, int grid, int cluster, bool pdl,
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<R, MT, FUSED, U5>, args);
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<R, MT, FUSED, V>, args);
 }
 
-template <int R, int MT, bool FUSED, bool U5>
+template <int R, int MT, bool FUSED, int V>
 int occupancy_t() {
-  if (set_attributes<R, MT, FUSED, U5>() != cudaSuccess) return 0;
+  if (set_attributes<R, MT, FUSED, V>() != cudaSuccess) return 0;
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_kernel<R, MT, FUSED, U5>, MCfg<MT>::THREADS,
-                                                    gemv_smem_bytes<R, MT, U5>()) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_kernel<R, MT, FUSED, V>, MCfg<MT>::THREADS,
+                                                    gemv_smem_bytes<R, MT, V>()) != cudaSuccess)
     return 0;
   return occ;
 }
 
 // Whether clusters of `cluster` CTAs of this kernel can be resident at all.
-template <int R, int MT, bool FUSED, bool U5>
+template <int R, int MT, bool FUSED, int V>
 bool cluster_fits_t(int cluster) {
-  if (set_attributes<R, MT, FUSED, U5>() != cudaSuccess) return false;
+  if (set_attributes<R, MT, FUSED, V>() != cudaSuccess) return false;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(cluster);
   cfg.blockDim = dim3(MCfg<MT>::THREADS);
-  cfg.dynamicSmemBytes = gemv_smem_bytes<R, MT, U5>();
+  cfg.dynamicSmemBytes = gemv_smem_bytes<R, MT, V>();
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cluster;
@@ -1100,81 +1150,85 @@ bool cluster_fits_t(int cluster) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemv_kernel<R, MT, FUSED, U5>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, gemv_kernel<R, MT, FUSED, V>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
   return n > 0;
 }
 
-// 16 activation rows: the tcgen05 kernel exists for 128-row tiles only
-// (u5 selects it there and is ignored elsewhere).
-template <int R, bool FUSED>
-cudaError_t launch_gemv_16(const GemvArgs& args, bool u5, int grid, int cluster, bool pdl, cudaStream_t s) {
-  if constexpr (R == 128) {
-    if (u5) return launch_gemv_t<R, 16, FUSED, true>(args, grid, cluster, pdl, s);
+// The variants a tile height and row count instantiate: the default always,
+// tcgen05 for 128-row tiles with 16 rows, the SwiGLU epilogue for 64- and
+// 128-row tiles; another request falls back to the default.
+template <int R, int MT, bool FUSED>
+cudaError_t launch_gemv_v(const GemvArgs& args, int var, int grid, int cluster, bool pdl, cudaStream_t s) {
+  if constexpr (R == 128 && MT == 16) {
+    if (var == VAR_TCGEN05) return launch_gemv_t<R, MT, FUSED, VAR_TCGEN05>(args, grid, cluster, pdl, s);
   }
-  return launch_gemv_t<R, 16, FUSED, false>(args, grid, cluster, pdl, s);
+  if constexpr (R >= 64) {
+    if (var == VAR_SWIGLU) return launch_gemv_t<R, MT, FUSED, VAR_SWIGLU>(args, grid, cluster, pdl, s);
+  }
+  return launch_gemv_t<R, MT, FUSED, VAR_DEFAULT>(args, grid, cluster, pdl, s);
 }
-template <int R, bool FUSED>
-int occupancy_16(bool u5) {
-  if constexpr (R == 128) {
-    if (u5) return occupancy_t<R, 16, FUSED, true>();
+template <int R, int MT, bool FUSED>
+int occupancy_v(int var) {
+  if constexpr (R == 128 && MT == 16) {
+    if (var == VAR_TCGEN05) return occupancy_t<R, MT, FUSED, VAR_TCGEN05>();
   }
-  return occupancy_t<R, 16, FUSED, false>();
+  return occupancy_t<R, MT, FUSED, VAR_DEFAULT>();  // the SwiGLU variant has the default's resources
 }
-template <int R, bool FUSED>
-bool cluster_fits_16(bool u5, int c) {
-  if constexpr (R == 128) {
-    if (u5) return cluster_fits_t<R, 16, FUSED, true>(c);
+template <int R, int MT, bool FUSED>
+bool cluster_fits_v(int var, int c) {
+  if constexpr (R == 128 && MT == 16) {
+    if (var == VAR_TCGEN05) return cluster_fits_t<R, MT, FUSED, VAR_TCGEN05>(c);
   }
-  return cluster_fits_t<R, 16, FUSED, false>(c);
+  return cluster_fits_t<R, MT, FUSED, VAR_DEFAULT>(c);
 }
 
 // Per-R translation units instantiate these for every MT and FUSED.
 template <int R>
-cudaError_t launch_gemv_r(const GemvArgs& args, int MT, bool fused, bool u5, int grid, int cluster, bool pdl,
+cudaError_t launch_gemv_r(const GemvArgs& args, int MT, bool fused, int var, int grid, int cluster, bool pdl,
                          cudaStream_t s);
 template <int R>
-int occupancy_r(int MT, bool fused, bool u5);
+int occupancy_r(int MT, bool fused, int var);
 template <int R>
-bool cluster_fits_r(int MT, bool fused, bool u5, int cluster);
+bool cluster_fits_r(int MT, bool fused, int var, int cluster);
 
 #define Q8_INSTANTIATE_R(R)                                                                          \
   template <>                                                                                        \
-  cudaError_t launch_gemv_r<R>(const GemvArgs& args, int MT, bool fused, bool u5, int grid,          \
+  cudaError_t launch_gemv_r<R>(const GemvArgs& args, int MT, bool fused, int var, int grid,          \
                                int cluster, bool pdl, cudaStream_t s) {                              \
     switch (MT) {                                                                                    \
-      case 1: return fused ? launch_gemv_t<R, 1, true, false>(args, grid, cluster, pdl, s)           \
-                           : launch_gemv_t<R, 1, false, false>(args, grid, cluster, pdl, s);         \
-      case 2: return fused ? launch_gemv_t<R, 2, true, false>(args, grid, cluster, pdl, s)           \
-                           : launch_gemv_t<R, 2, false, false>(args, grid, cluster, pdl, s);         \
-      case 4: return fused ? launch_gemv_t<R, 4, true, false>(args, grid, cluster, pdl, s)           \
-                           : launch_gemv_t<R, 4, false, false>(args, grid, cluster, pdl, s);         \
-      case 8: return fused ? launch_gemv_t<R, 8, true, false>(args, grid, cluster, pdl, s)           \
-                           : launch_gemv_t<R, 8, false, false>(args, grid, cluster, pdl, s);         \
-      default: return fused ? launch_gemv_16<R, true>(args, u5, grid, cluster, pdl, s)               \
-                            : launch_gemv_16<R, false>(args, u5, grid, cluster, pdl, s);             \
+      case 1: return fused ? launch_gemv_v<R, 1, true>(args, var, grid, cluster, pdl, s)             \
+                           : launch_gemv_v<R, 1, false>(args, var, grid, cluster, pdl, s);           \
+      case 2: return fused ? launch_gemv_v<R, 2, true>(args, var, grid, cluster, pdl, s)             \
+                           : launch_gemv_v<R, 2, false>(args, var, grid, cluster, pdl, s);           \
+      case 4: return fused ? launch_gemv_v<R, 4, true>(args, var, grid, cluster, pdl, s)             \
+                           : launch_gemv_v<R, 4, false>(args, var, grid, cluster, pdl, s);           \
+      case 8: return fused ? launch_gemv_v<R, 8, true>(args, var, grid, cluster, pdl, s)             \
+                           : launch_gemv_v<R, 8, false>(args, var, grid, cluster, pdl, s);           \
+      default: return fused ? launch_gemv_v<R, 16, true>(args, var, grid, cluster, pdl, s)           \
+                            : launch_gemv_v<R, 16, false>(args, var, grid, cluster, pdl, s);         \
     }                                                                                                \
   }                                                                                                  \
   template <>                                                                                        \
-  int occupancy_r<R>(int MT, bool fused, bool u5) {                                                  \
+  int occupancy_r<R>(int MT, bool fused, int var) {                                                  \
     switch (MT) {                                                                                    \
-      case 1: return fused ? occupancy_t<R, 1, true, false>() : occupancy_t<R, 1, false, false>();   \
-      case 2: return fused ? occupancy_t<R, 2, true, false>() : occupancy_t<R, 2, false, false>();   \
-      case 4: return fused ? occupancy_t<R, 4, true, false>() : occupancy_t<R, 4, false, false>();   \
-      case 8: return fused ? occupancy_t<R, 8, true, false>() : occupancy_t<R, 8, false, false>();   \
-      default: return fused ? occupancy_16<R, true>(u5) : occupancy_16<R, false>(u5);                \
+      case 1: return fused ? occupancy_v<R, 1, true>(var) : occupancy_v<R, 1, false>(var);           \
+      case 2: return fused ? occupancy_v<R, 2, true>(var) : occupancy_v<R, 2, false>(var);           \
+      case 4: return fused ? occupancy_v<R, 4, true>(var) : occupancy_v<R, 4, false>(var);           \
+      case 8: return fused ? occupancy_v<R, 8, true>(var) : occupancy_v<R, 8, false>(var);           \
+      default: return fused ? occupancy_v<R, 16, true>(var) : occupancy_v<R, 16, false>(var);        \
     }                                                                                                \
   }                                                                                                  \
   template <>                                                                                        \
-  bool cluster_fits_r<R>(int MT, bool fused, bool u5, int c) {                                       \
+  bool cluster_fits_r<R>(int MT, bool fused, int var, int c) {                                       \
     switch (MT) {                                                                                    \
-      case 1: return fused ? cluster_fits_t<R, 1, true, false>(c) : cluster_fits_t<R, 1, false, false>(c); \
-      case 2: return fused ? cluster_fits_t<R, 2, true, false>(c) : cluster_fits_t<R, 2, false, false>(c); \
-      case 4: return fused ? cluster_fits_t<R, 4, true, false>(c) : cluster_fits_t<R, 4, false, false>(c); \
-      case 8: return fused ? cluster_fits_t<R, 8, true, false>(c) : cluster_fits_t<R, 8, false, false>(c); \
-      default: return fused ? cluster_fits_16<R, true>(u5, c) : cluster_fits_16<R, false>(u5, c);    \
+      case 1: return fused ? cluster_fits_v<R, 1, true>(var, c) : cluster_fits_v<R, 1, false>(var, c); \
+      case 2: return fused ? cluster_fits_v<R, 2, true>(var, c) : cluster_fits_v<R, 2, false>(var, c); \
+      case 4: return fused ? cluster_fits_v<R, 4, true>(var, c) : cluster_fits_v<R, 4, false>(var, c); \
+      case 8: return fused ? cluster_fits_v<R, 8, true>(var, c) : cluster_fits_v<R, 8, false>(var, c); \
+      default: return fused ? cluster_fits_v<R, 16, true>(var, c) : cluster_fits_v<R, 16, false>(var, c); \
     }                                                                                                \
   }
 

@@ -46,8 +46,11 @@ cudaError_t launch_unpack(const uint8_t* packed, int64_t N, int64_t K, uint8_t* 
                           cudaStream_t s);
 cudaError_t launch_block_dots(const uint8_t* W, int64_t N, int64_t K, const uint8_t* A, int M,
                               int32_t* isum, cudaStream_t s);
+// h_blocks non-null: the SwiGLU epilogue writes blocks of silu(gate) * up
+// there instead of y (the plan must not split K; tiles of 64 or 128 rows).
 cudaError_t launch_gemv(const GemvPlan& p, const uint8_t* W, const uint8_t* A, const float* x,
-                        uint8_t* A_out, float* y, void* workspace, bool pdl, cudaStream_t s);
+                        uint8_t* A_out, float* y, void* workspace, bool pdl, cudaStream_t s,
+                        uint8_t* h_blocks = nullptr);
 cudaError_t read_and_clear_gemv_error(unsigned* code);
 
 // Fused producers (q8_producers.cu).

@@ -104,6 +104,14 @@ def test_host_argument_checks_reject_before_any_device_work(lib):
     assert n(fake, eight, fake, 1e-5, 1, 64, None, fake, 0, None) == -3         # delta
     assert n(fake, None, fake, 1e-5, 1, 64, eight, fake, 0, None) == -3         # h_out
     assert n(fake, None, fake, 1e-5, 1, 64, None, odd, 0, None) == -3           # out odd
+    e = lib.q8_gemm_swiglu
+    assert e(None, 64, 64, fake, 1, fake, 0, None) == -1                        # null W
+    assert e(fake, 64, 64, None, 1, fake, 0, None) == -1                        # null A
+    assert e(fake, 64, 64, fake, 1, fake, 2, None) == -1                        # tcgen05 not offered
+    assert e(fake, 48, 64, fake, 1, fake, 0, None) == -2                        # F % 32
+    assert e(fake, 64, 64, fake, 0, fake, 0, None) == -2                        # M = 0
+    assert e(fake, 64, 64, fake, 1, odd, 0, None) == -2                         # 16-row tiles: no layout
+    assert lib.q8_fused_quant_gemm_swiglu(fake, 8192, 64, None, 1, fake, 0, None) == -1
     s = lib.q8_swiglu_quantize
     assert s(None, 1, 64, fake, 0, None) == -1
     assert s(fake, 1, 64, fake, 2, None) == -1                                  # unknown flag

@@ -126,3 +126,52 @@ def test_producers_feed_the_gemv_and_chain_with_pdl(q8):
     y2_ref, S2 = oracle.gemm(oracle.quantize(w_dn.cpu().numpy()), A2_ref, F)
     assert (np.abs(y2.double().cpu().numpy() - y2_ref) <= 1e-5 * S2 + 1e-6).all()
     assert q8.q8_device_error() == 0
+
+
+@pytest.mark.parametrize("F,K,M", [(8192, 2048, 1), (8192, 2048, 3), (4864, 3072, 16), (8192, 2048, 33),
+                                   (2496, 512, 5)])
+def test_swiglu_epilogue_gemv(q8, F, K, M):
+    # gate/up GEMV with SwiGLU in its epilogue: equal, bit for bit, to
+    # SwiGLU + quantization of the plain GEMV's outputs on the same W
+    gate = q8_synth.weights(F, K, q8_synth.derive_seed("sw-g", F, K), DEV)
+    up = q8_synth.weights(F, K, q8_synth.derive_seed("sw-u", F, K), DEV)
+    W = q8.pack_weights_f32(q8.interleave_gate_up(gate, up))
+    x = q8_synth.activations(M, K, q8_synth.derive_seed("sw-x", M, K), DEV)
+    A = q8.empty_blocks(M, K)
+    q8.q8_quantize_act(x, A)
+    out = torch.full((M, (F // 32) * 34), 0xEE, dtype=torch.uint8, device=DEV)
+    q8.q8_gemm_swiglu(W, F, K, A, M, out)
+    outf = torch.zeros_like(out)
+    q8.q8_fused_quant_gemm_swiglu(W, F, K, x, M, outf, flags=q8.FLAG_PDL)
+    y = torch.empty((M, 2 * F), dtype=torch.float32, device=DEV)
+    q8.q8_gemm(W, 2 * F, K, A, M, y, workspace=q8.new_workspace(2 * F, K, M))
+    torch.cuda.synchronize()
+    G = q8.q8_packed_tile_rows(2 * F) // 2
+    yg = y.view(M, F // G, 2, G)
+    gu = torch.cat([yg[:, :, 0, :].reshape(M, F), yg[:, :, 1, :].reshape(M, F)], dim=1)
+    ref = oracle.swiglu_quantize(gu.cpu().numpy(), F)
+    assert np.array_equal(out.cpu().numpy(), ref)
+    assert np.array_equal(outf.cpu().numpy(), ref)
+    # the GEMV part against the oracle on sampled rows of the interleaved matrix
+    rows = np.array([0, G - 1, G, 2 * G, 2 * F - 1])
+    w_rows = q8.interleave_gate_up(gate, up)[torch.from_numpy(rows).to(DEV)].cpu().numpy()
+    y_ref, S_ref = oracle.gemm(oracle.quantize(w_rows), A.cpu().numpy(), K)
+    err = np.abs(y[:, torch.from_numpy(rows).to(DEV)].double().cpu().numpy() - y_ref)
+    assert (err <= 1e-5 * S_ref + 1e-6).all()
+    assert q8.q8_device_error() == 0
+
+
+def test_swiglu_epilogue_gemv_shape_errors(q8):
+    dummy = torch.zeros(64, dtype=torch.uint8, device=DEV)
+    xd = torch.zeros(64, dtype=torch.float32, device=DEV)
+    for F, K, M in ((2432, 512, 1),       # 32-row tiles: no epilogue layout
+                    (8192 + 32, 512, 1),  # F not a multiple of the group
+                    (8192, 65536, 16)):   # would split along K
+        with pytest.raises(q8.Q8Error) as e:
+            q8._check("q8_gemm_swiglu", q8.lib().q8_gemm_swiglu(dummy.data_ptr(), F, K, dummy.data_ptr(), M,
+                                                                dummy.data_ptr(), 0, None))
+        assert e.value.status == -2
+    with pytest.raises(q8.Q8Error) as e:
+        q8._check("q8_fused_quant_gemm_swiglu", q8.lib().q8_fused_quant_gemm_swiglu(
+            dummy.data_ptr(), 8192, 2048, xd.data_ptr(), 1, dummy.data_ptr(), 2, None))
+    assert e.value.status == -1  # the tcgen05 option is not offered here
