@@ -45,6 +45,15 @@ def _peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_peaks() -> dict:
+    """MEASURED_PEAKS.json as a dict ({} when the file is absent)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if not os.path.exists(p):
+        return {}
+    with open(p) as f:
+        return json.load(f)
+
+
 def _workload_name(shape, M, layers):
     return "%s q8_0 projection stack (%d layers x qkv/o/gate_up/down + lm_head), decode M=%d" % (
         shape.name, layers, M)
@@ -548,29 +557,53 @@ def producers(q8, shape, launches=20):
     return out
 
 
-def prefill(q8, st, M=512, steps=3):
-    """A 512-row pass over the same projection stack (prefill of 512 tokens
-    through q8_fused_quant_gemm: 32 passes of 16 rows per GEMV, W streamed
-    once per pass), as one CUDA graph: time per step and tokens/s."""
+def prefill(q8, st, M=512, steps=3, tile_rows=(512, 2048)):
+    """Prefill over the same projection stack, each case one CUDA graph:
+    the prefill tile GEMM (q8_fused_quant_gemm_prefill: quantize, pack, one
+    tile GEMM per projection; each 128-row weight tile reused across 128
+    activation rows) at `tile_rows` tokens, and for comparison the decode
+    GEMV at M rows (q8_fused_quant_gemm: passes of 16 rows, W streamed once
+    per pass).  Time per step, tokens/s; for the tile GEMM also the int8
+    multiply-accumulate rate (2 ops per MAC) and the fraction of the
+    measured dense bf16 tensor peak (fp16 operands run at the same rate)."""
     import torch
 
     from q8_block_quantized_gb300.stack import Q8Stack
+
+    def timed(s2, n):
+        g = s2.capture()
+        for _ in range(2):
+            g.replay()
+        torch.cuda.synchronize()
+        cur = torch.cuda.current_stream()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        for _ in range(n):
+            g.replay()
+        b.record(cur)
+        b.synchronize()
+        del g
+        return a.elapsed_time(b) / n
+
+    peaks = measured_peaks()
+    res = {"tile_gemm": []}
+    for Mt in tile_rows:
+        s2 = Q8Stack(st.shape, M=Mt, mode="prefill", layers=st.n_layers, shared_weights=st.weights)
+        ms = timed(s2, steps)
+        tops = 2 * s2.mac_per_step() / (ms * 1e-3) / 1e12
+        ent = {"M": Mt, "ms_per_step": round(ms, 3), "tok_s": round(Mt / (ms * 1e-3), 1),
+               "launches_per_step": s2.launches_per_step(), "TOPS": round(tops, 1)}
+        if peaks.get("bf16_tflops"):
+            ent["tensor_frac_of_measured_bf16"] = round(tops / peaks["bf16_tflops"], 4)
+        res["tile_gemm"].append(ent)
+        del s2
+        torch.cuda.empty_cache()
     s2 = Q8Stack(st.shape, M=M, mode="fused", layers=st.n_layers, shared_weights=st.weights)
-    g = s2.capture()
-    g.replay()
-    torch.cuda.synchronize()
-    cur = torch.cuda.current_stream()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(cur)
-    for _ in range(steps):
-        g.replay()
-    b.record(cur)
-    b.synchronize()
-    ms = a.elapsed_time(b) / steps
-    res = {"M": M, "ms_per_step": round(ms, 3), "tok_s": round(M / (ms * 1e-3), 1),
-           "launches_per_step": s2.launches_per_step(),
-           "GB/s": round(s2.bytes_per_step() / (ms * 1e-3) / 1e9, 1)}
-    del g, s2
+    ms = timed(s2, steps)
+    res["decode_gemv_passes"] = {"M": M, "ms_per_step": round(ms, 3), "tok_s": round(M / (ms * 1e-3), 1),
+                                 "launches_per_step": s2.launches_per_step(),
+                                 "GB/s": round(s2.bytes_per_step() / (ms * 1e-3) / 1e9, 1)}
+    del s2
     torch.cuda.empty_cache()
     return res
 

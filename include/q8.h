@@ -71,6 +71,11 @@ extern "C" {
 #define Q8_MAX_DOTS_M 64    /* most activation rows per q8_block_dots call    */
 #define Q8_MAX_TILE_ROWS 128 /* packed layout: most output rows per tile       */
 #define Q8_CHUNK_BLOCKS 8   /* packed layout: blocks per chunk                */
+#define Q8_PREFILL_TILE_ROWS 128 /* prefill GEMM: weight rows and activation
+                                    rows of one output tile                  */
+#define Q8_PREFILL_SEGMENT 16 /* prefill GEMM: blocks per segment of its
+                                 summation order (see q8_gemm_prefill)       */
+#define Q8_MAX_PREFILL_K 65536 /* prefill GEMM: largest K                     */
 
 /* Flags for the compute calls. */
 #define Q8_FLAG_PDL 1u      /* launch as a programmatic dependent of the
@@ -335,6 +340,56 @@ Q8_API int q8_fused_quant_gemm_swiglu(const void *W, int64_t F, int64_t K, const
 #define Q8_NOALLOC_SCRATCH_BYTES (4u << 20)
 Q8_API int q8_gemm_noalloc(const void *W, int64_t N, int64_t K, const void *A_blocks,
                            int M, float *y, unsigned flags, void *stream);
+
+/*
+ * q8_gemm_prefill / q8_fused_quant_gemm_prefill -- the prefill tile GEMM:
+ * y = W (Q8_0, packed) times M activation rows (the tokens of a prompt),
+ * each 128-row weight tile reused across 128 activation rows.  (Ferro
+ * README, "Exactness contract": prefill rows always take the tile GEMM, so
+ * a row's arithmetic does not depend on how many rows share the launch, and
+ * a prompt filled in slices equals the prompt filled at once; "How the iGPU
+ * path is fast", item 1: int8 block dots of Q8_0 weights and activations
+ * quantized per 32-block.)
+ *
+ * Every output is the same function of its two rows, whatever M is and
+ * wherever the row sits: with isum_b the exact int32 dot of block b,
+ * s_b = fp32(d_w[n][b] * d_a[m][b]) (both binary16 scales widened to fp32),
+ *   sigma = +0; sigma = fma(isum_b, s_b, sigma) for the blocks b of one
+ *           segment of Q8_PREFILL_SEGMENT consecutive blocks, in order;
+ *   Y = +0; Y = Y + sigma for the segments, in order; y[m][n] = Y.
+ * (IEEE single precision, round to nearest even, fma rounded once.)  This
+ * is not the decode order of q8_gemm, so a prefill row is not bitwise the
+ * decoded row; both are within the library's tolerance of the exact sum:
+ * here |y - exact| <= (17 + ceil(K/512)) * 2^-24 * S with S the sum of the
+ * block terms' magnitudes, below 1e-5 * S for K <= Q8_MAX_PREFILL_K.
+ *
+ *   W          packed weights from q8_repack_weights, 16-byte aligned.
+ *   N          output rows, 1 <= N <= 2^31-1.
+ *   K          positive multiple of 32, at most Q8_MAX_PREFILL_K.
+ *   A_blocks   [M][K/32] activation blocks (q8_quantize_act), 2-byte aligned
+ *              (q8_gemm_prefill).
+ *   x          [M][K] fp32 activations, 4-byte aligned, quantized first
+ *              exactly as q8_quantize_act does (q8_fused_quant_gemm_prefill).
+ *   M          activation rows, >= 1.
+ *   y          [M][N] fp32 output, row-major, 4-byte aligned; overwritten.
+ *   A_blocks_out  (fused call only, may be NULL) receives the [M][K/32]
+ *              blocks of x, 2-byte aligned.
+ *   workspace  16-byte aligned, at least q8_prefill_workspace_bytes(K, M)
+ *              bytes, not overlapping the other buffers: it receives the
+ *              activation blocks packed in 128-row tiles (and, in the fused
+ *              call without A_blocks_out, the blocks of x).  Scratch only.
+ *   flags      0 or Q8_FLAG_PDL (the first launch is a programmatic
+ *              dependent of the previous work on the stream; the call waits
+ *              for that work before it reads anything).
+ * A call is two launches (three when fused): pack (quantize), GEMM.
+ */
+Q8_API size_t q8_prefill_workspace_bytes(int64_t K, int M);
+Q8_API int q8_gemm_prefill(const void *W, int64_t N, int64_t K, const void *A_blocks, int M,
+                           float *y, void *workspace, size_t workspace_bytes, unsigned flags,
+                           void *stream);
+Q8_API int q8_fused_quant_gemm_prefill(const void *W, int64_t N, int64_t K, const float *x, int M,
+                                       float *y, void *A_blocks_out, void *workspace,
+                                       size_t workspace_bytes, unsigned flags, void *stream);
 
 /* ---- test hooks (not on the hot path) ----------------------------------- */
 

@@ -74,6 +74,7 @@ def _load():
         lib.q8o_block_dots.argtypes = [u8p, i64, i64, u8p, i64, i32p]
         lib.q8o_gemm.argtypes = [u8p, i64, i64, u8p, i64, f64p, f64p]
         lib.q8o_quant_gemm.argtypes = [u8p, i64, i64, f32p, i64, u8p, f64p, f64p]
+        lib.q8o_gemm_prefill_order.argtypes = [u8p, i64, i64, u8p, i64, i64, f32p]
         lib.q8o_ember_tile_pack.argtypes = [u8p, u8p]
         lib.q8o_pairwise_sum.argtypes = [f32p, i64]
         lib.q8o_pairwise_sum.restype = ctypes.c_float
@@ -166,6 +167,21 @@ def gemm(W, A, K: int):
     lib.q8o_gemm(_ptr(W, ctypes.c_uint8), N, K, _ptr(A, ctypes.c_uint8), M,
                  _ptr(y, ctypes.c_double), _ptr(S, ctypes.c_double))
     return y, S
+
+
+def gemm_prefill_order(W, A, K: int, seg: int = 16) -> np.ndarray:
+    """float32 [M][N]: the prefill product in its fixed single-precision
+    order (fma through segments of `seg` blocks, segment sums added in
+    order); see q8o_gemm_prefill_order."""
+    lib = _load()
+    W, A = _u8(W), _u8(A)
+    nb = K // QK
+    N = W.size // (nb * BLOCK_BYTES)
+    M = A.size // (nb * BLOCK_BYTES)
+    y = np.zeros((M, N), dtype=np.float32)
+    lib.q8o_gemm_prefill_order(_ptr(W, ctypes.c_uint8), N, K, _ptr(A, ctypes.c_uint8), M, seg,
+                               _ptr(y, ctypes.c_float))
+    return y
 
 
 def quant_gemm(W, x, K: int):

@@ -223,6 +223,43 @@ void q8o_gemm(const uint8_t *W, int64_t N, int64_t K,
         }
 }
 
+/* ---------------------------------------------------------------------------
+ * The prefill product's single-precision summation order.  [Ferro],
+ * "Exactness contract": prefill rows take the tile GEMM, and a row's result
+ * depends neither on how many rows share the launch nor on how the prompt
+ * is sliced.  The page fixes no order; the reading taken is the plainest
+ * one a tile GEMM can keep per row: for each output, the blocks in order,
+ * cut into segments of `seg` consecutive blocks (the last may be shorter);
+ *   s_b   = d_w * d_a in fp32 (exact: two 11-bit significands),
+ *   sigma = fma(isum_b, s_b, sigma) through a segment, from +0,
+ *   Y     = Y + sigma through the segments, from +0.
+ * y[m][n] = Y (float).  Every step is one IEEE single-precision operation
+ * rounded to nearest even; fmaf rounds once.
+ * ------------------------------------------------------------------------- */
+void q8o_gemm_prefill_order(const uint8_t *W, int64_t N, int64_t K,
+                            const uint8_t *A, int64_t M, int64_t seg, float *y)
+{
+    int64_t nb = K / QK;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            float Y = 0.0f, sigma = 0.0f;
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t *wb = W + (n * nb + b) * BLOCK_BYTES;
+                const uint8_t *ab = A + (m * nb + b) * BLOCK_BYTES;
+                int32_t isum = 0;
+                for (int i = 0; i < QK; ++i)
+                    isum += (int32_t)q_at(wb, i) * (int32_t)q_at(ab, i);
+                float s_b = scale_of(wb) * scale_of(ab);
+                sigma = fmaf((float)isum, s_b, sigma);
+                if ((b + 1) % seg == 0 || b == nb - 1) {
+                    Y = Y + sigma;
+                    sigma = 0.0f;
+                }
+            }
+            y[m * N + n] = Y;
+        }
+}
+
 /* Quantize fp32 activations, then the product: the fused operation. */
 void q8o_quant_gemm(const uint8_t *W, int64_t N, int64_t K,
                     const float *x, int64_t M, uint8_t *A_scratch,

@@ -27,6 +27,9 @@ MAX_TILE_ROWS = 128
 CHUNK_BLOCKS = 8
 FLAG_PDL = 1
 FLAG_TCGEN05 = 2
+PREFILL_TILE_ROWS = 128
+PREFILL_SEGMENT = 16
+MAX_PREFILL_K = 65536
 
 STATUS = {0: "Q8_OK", -1: "Q8_EINVAL", -2: "Q8_ESHAPE", -3: "Q8_EALIGN", -4: "Q8_EDEVICE",
           -5: "Q8_ECUDA", -6: "Q8_EWORKSPACE", -7: "Q8_ETIMEOUT", -8: "Q8_ESCRATCH"}
@@ -50,6 +53,9 @@ SIGNATURES = {
     "q8_gemm_noalloc": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _u, _vp]),
     "q8_gemm_swiglu": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _u, _vp]),
     "q8_fused_quant_gemm_swiglu": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _u, _vp]),
+    "q8_prefill_workspace_bytes": (_sz, [_i64, _int]),
+    "q8_gemm_prefill": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _vp, _sz, _u, _vp]),
+    "q8_fused_quant_gemm_prefill": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _vp, _vp, _sz, _u, _vp]),
     "q8_unpack_weights": (_int, [_vp, _i64, _i64, _vp, _vp]),
     "q8_block_dots": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _vp]),
     "q8_device_error": (_int, [ctypes.POINTER(ctypes.c_uint)]),
@@ -187,6 +193,29 @@ def q8_fused_quant_gemm(W: torch.Tensor, N: int, K: int, x: torch.Tensor, M: int
     return y
 
 
+def q8_prefill_workspace_bytes(K: int, M: int) -> int:
+    return lib().q8_prefill_workspace_bytes(K, M)
+
+
+def q8_gemm_prefill(W: torch.Tensor, N: int, K: int, A_blocks: torch.Tensor, M: int, y: torch.Tensor,
+                    workspace: torch.Tensor, flags: int = 0, stream=None):
+    _check("q8_gemm_prefill", lib().q8_gemm_prefill(
+        _dev(W, torch.uint8, "W"), N, K, _dev(A_blocks, torch.uint8, "A_blocks"), M,
+        _dev(y, torch.float32, "y"), _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+        flags, _stream(stream)))
+    return y
+
+
+def q8_fused_quant_gemm_prefill(W: torch.Tensor, N: int, K: int, x: torch.Tensor, M: int, y: torch.Tensor,
+                                workspace: torch.Tensor, A_blocks_out: torch.Tensor | None = None,
+                                flags: int = 0, stream=None):
+    _check("q8_fused_quant_gemm_prefill", lib().q8_fused_quant_gemm_prefill(
+        _dev(W, torch.uint8, "W"), N, K, _dev(x, torch.float32, "x"), M,
+        _dev(y, torch.float32, "y"), _opt(A_blocks_out, torch.uint8, "A_blocks_out"),
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), flags, _stream(stream)))
+    return y
+
+
 def q8_gemm_noalloc(W: torch.Tensor, N: int, K: int, A_blocks: torch.Tensor, M: int,
                     y: torch.Tensor, flags: int = 0, stream=None):
     """q8_gemm for callers that cannot allocate: split-K scratch is the
@@ -268,6 +297,10 @@ def empty_packed(N: int, K: int, device="cuda") -> torch.Tensor:
 def new_workspace(N: int, K: int, M: int, device="cuda") -> torch.Tensor | None:
     n = q8_workspace_bytes(N, K, M)
     return torch.zeros(n, dtype=torch.uint8, device=device) if n else None
+
+
+def new_prefill_workspace(K: int, M: int, device="cuda") -> torch.Tensor:
+    return torch.empty(q8_prefill_workspace_bytes(K, M), dtype=torch.uint8, device=device)
 
 
 def pack_weights_f32(w: torch.Tensor, stream=None) -> torch.Tensor:

@@ -94,6 +94,42 @@ int swiglu_gemm(const void* W, int64_t F, int64_t K, const void* A_blocks, const
                                  static_cast<cudaStream_t>(stream), static_cast<uint8_t*>(out_blocks)));
 }
 
+// Packed activations of the prefill GEMM: the blocks' bytes, to 16 bytes.
+size_t prefill_packed_bytes(int64_t K, int64_t M) {
+  return ((size_t)M * (size_t)(K / QK) * BLOCK_BYTES + 15) & ~(size_t)15;
+}
+
+int prefill_gemm(const void* W, int64_t N, int64_t K, const void* A_blocks, const float* x, int M, float* y,
+                 void* A_out, void* workspace, size_t workspace_bytes, unsigned flags, void* stream) {
+  if (W == nullptr || y == nullptr || (A_blocks == nullptr && x == nullptr)) return Q8_EINVAL;
+  if ((flags & ~Q8_FLAG_PDL) != 0) return Q8_EINVAL;
+  if (N <= 0 || N > INT32_MAX || !k_ok(K) || K > Q8_MAX_PREFILL_K || M < 1) return Q8_ESHAPE;
+  if (!aligned(W, 16) || !aligned(y, 4)) return Q8_EALIGN;
+  if ((A_blocks != nullptr && !aligned(A_blocks, 2)) || (x != nullptr && !aligned(x, 4)) ||
+      (A_out != nullptr && !aligned(A_out, 2)))
+    return Q8_EALIGN;
+  const size_t pk = prefill_packed_bytes(K, M);
+  const size_t need = (x != nullptr && A_out == nullptr) ? 2 * pk : pk;
+  if (workspace == nullptr || workspace_bytes < need) return Q8_EWORKSPACE;
+  if (!aligned(workspace, 16)) return Q8_EALIGN;
+  DeviceInfo d;
+  int st = device_ok(&d);
+  if (st != Q8_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  bool pdl = (flags & Q8_FLAG_PDL) != 0;
+  uint8_t* packed = static_cast<uint8_t*>(workspace);
+  const uint8_t* blocks = static_cast<const uint8_t*>(A_blocks);
+  cudaError_t e;
+  if (x != nullptr) {
+    uint8_t* out = A_out != nullptr ? static_cast<uint8_t*>(A_out) : packed + pk;
+    if ((e = launch_quantize(x, M, K, out, pdl, s)) != cudaSuccess) return Q8_ECUDA;
+    blocks = out;
+    pdl = true;  // the next launches depend on this library's own launch
+  }
+  if ((e = launch_pack_act(blocks, M, K, packed, pdl, s)) != cudaSuccess) return Q8_ECUDA;
+  return cuda_status(launch_prefill(d, static_cast<const uint8_t*>(W), N, K, packed, M, y, true, s));
+}
+
 }  // namespace
 
 extern "C" {
@@ -123,6 +159,24 @@ size_t q8_blocks_bytes(int64_t rows, int64_t K) {
 size_t q8_packed_bytes(int64_t N, int64_t K) { return q8_blocks_bytes(N, K); }
 
 int q8_packed_tile_rows(int64_t N) { return N > 0 ? layout_tile_rows(N) : 0; }
+
+size_t q8_prefill_workspace_bytes(int64_t K, int M) {
+  if (!k_ok(K) || K > Q8_MAX_PREFILL_K || M < 1) return 0;
+  return 2 * prefill_packed_bytes(K, M);
+}
+
+int q8_gemm_prefill(const void* W, int64_t N, int64_t K, const void* A_blocks, int M, float* y, void* workspace,
+                    size_t workspace_bytes, unsigned flags, void* stream) {
+  if (A_blocks == nullptr) return Q8_EINVAL;
+  return prefill_gemm(W, N, K, A_blocks, nullptr, M, y, nullptr, workspace, workspace_bytes, flags, stream);
+}
+
+int q8_fused_quant_gemm_prefill(const void* W, int64_t N, int64_t K, const float* x, int M, float* y,
+                                void* A_blocks_out, void* workspace, size_t workspace_bytes, unsigned flags,
+                                void* stream) {
+  if (x == nullptr) return Q8_EINVAL;
+  return prefill_gemm(W, N, K, nullptr, x, M, y, A_blocks_out, workspace, workspace_bytes, flags, stream);
+}
 
 size_t q8_workspace_bytes(int64_t N, int64_t K, int M) {
   if (N <= 0 || N > INT32_MAX || !k_ok(K) || M < 1 || M > Q8_MAX_M) return 0;

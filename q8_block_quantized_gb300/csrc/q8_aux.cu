@@ -34,8 +34,11 @@ __global__ void __launch_bounds__(QUANT_THREADS) quantize_kernel(const float* __
 // neighbouring threads are contiguous.
 // `rows` holds [N][nb] row-contiguous blocks, `packed` the packed layout;
 // inverse == false copies rows -> packed, inverse == true packed -> rows.
-__global__ void repack_kernel(uint8_t* rows, int64_t N, int64_t nb, uint8_t* packed, bool inverse) {
-  const int R = layout_tile_rows(N);
+// R is the tile height: q8_packed_tile_rows(N) for weights, 128 for the
+// activations of the prefill GEMM.
+__global__ void repack_kernel(uint8_t* rows, int64_t N, int64_t nb, int R, uint8_t* packed, bool inverse) {
+  pdl_launch_dependents();
+  pdl_wait();  // (a no-op unless launched as a programmatic dependent)
   const int64_t T = (N + R - 1) / R;
   const int64_t total = T * nb * R;
   for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
@@ -135,8 +138,24 @@ cudaError_t launch_repack(const uint8_t* src, int64_t N, int64_t K, uint8_t* dst
   const int64_t nb = K / QK;
   const int R = layout_tile_rows(N);
   const int64_t total = ((N + R - 1) / R) * nb * R;
-  repack_kernel<<<grid_for(total, 256), 256, 0, s>>>(const_cast<uint8_t*>(src), N, nb, dst, false);
+  repack_kernel<<<grid_for(total, 256), 256, 0, s>>>(const_cast<uint8_t*>(src), N, nb, R, dst, false);
   return cudaGetLastError();
+}
+
+cudaError_t launch_pack_act(const uint8_t* src, int64_t M, int64_t K, uint8_t* dst, bool pdl, cudaStream_t s) {
+  const int64_t nb = K / QK;
+  const int R = MAX_TILE_ROWS;
+  const int64_t total = ((M + R - 1) / R) * nb * R;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid_for(total, 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, repack_kernel, const_cast<uint8_t*>(src), M, nb, R, dst, false);
 }
 
 cudaError_t launch_unpack(const uint8_t* packed, int64_t N, int64_t K, uint8_t* dst,
@@ -144,7 +163,7 @@ cudaError_t launch_unpack(const uint8_t* packed, int64_t N, int64_t K, uint8_t* 
   const int64_t nb = K / QK;
   const int R = layout_tile_rows(N);
   const int64_t total = ((N + R - 1) / R) * nb * R;
-  repack_kernel<<<grid_for(total, 256), 256, 0, s>>>(dst, N, nb, const_cast<uint8_t*>(packed), true);
+  repack_kernel<<<grid_for(total, 256), 256, 0, s>>>(dst, N, nb, R, const_cast<uint8_t*>(packed), true);
   return cudaGetLastError();
 }
 

@@ -92,6 +92,8 @@ int budget_of(int R, int MT, bool u5) {
 
 }  // namespace
 
+cudaError_t device_error_word(int dev, unsigned** out) { return error_word(dev, out); }
+
 bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, bool tcgen05, GemvPlan* out) {
   GemvPlan q;
   q.N = N;

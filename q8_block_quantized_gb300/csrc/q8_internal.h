@@ -52,6 +52,15 @@ cudaError_t launch_gemv(const GemvPlan& p, const uint8_t* W, const uint8_t* A, c
                         uint8_t* A_out, float* y, void* workspace, bool pdl, cudaStream_t s,
                         uint8_t* h_blocks = nullptr);
 cudaError_t read_and_clear_gemv_error(unsigned* code);
+// The device word the kernels set bits in when a bounded wait gives up.
+cudaError_t device_error_word(int dev, unsigned** out);
+
+// Prefill tile GEMM (q8_prefill.cu): activation blocks [M][K/32] are packed
+// into 128-row tiles (the weights' packed layout with R = 128), then every
+// 128 x 128 output tile is one CTA's work.
+cudaError_t launch_pack_act(const uint8_t* src, int64_t M, int64_t K, uint8_t* dst, bool pdl, cudaStream_t s);
+cudaError_t launch_prefill(const DeviceInfo& dev, const uint8_t* W, int64_t N, int64_t K, const uint8_t* A_packed,
+                           int64_t M, float* y, bool pdl, cudaStream_t s);
 
 // Fused producers (q8_producers.cu).
 cudaError_t launch_rmsnorm_quantize(const float* x, const float* delta, const float* gamma, float eps,

@@ -20,15 +20,18 @@ from dataclasses import dataclass, field
 import torch
 
 import q8_synth
-from . import (FLAG_PDL, FLAG_TCGEN05, empty_blocks, pack_weights_f32, q8_fused_quant_gemm, q8_gemm,
-               q8_quantize_act, q8_workspace_bytes)
+from . import (FLAG_PDL, FLAG_TCGEN05, empty_blocks, pack_weights_f32, q8_fused_quant_gemm,
+               q8_fused_quant_gemm_prefill, q8_gemm, q8_prefill_workspace_bytes, q8_quantize_act,
+               q8_workspace_bytes)
 
-MODES = ("shared", "fused", "unfused")
+# "prefill": every projection through the prefill tile GEMM (quantize, pack,
+# tile GEMM per call) instead of the decode GEMV
+MODES = ("shared", "fused", "unfused", "prefill")
 
 
 @dataclass
 class Call:
-    kind: str            # "quant", "gemm", "fused"
+    kind: str            # "quant", "gemm", "fused", "prefill"
     proj: str
     layer: int
     N: int = 0
@@ -69,6 +72,7 @@ class Q8Stack:
         self.weights = {}
         xo = yo = 0
         ws_need = 0
+        pf_need = 0
         calls = []
         for li, p in entries:
             if self.shared_weights is not None:
@@ -82,8 +86,12 @@ class Q8Stack:
             xo += self.M * p.K
             y = self.y_all[yo:yo + self.M * p.N].view(self.M, p.N)
             yo += self.M * p.N
-            ws_need = max(ws_need, q8_workspace_bytes(p.N, p.K, self.M))
             shared_input = p.name in ("qkv", "gate_up")
+            if self.mode == "prefill":
+                pf_need = max(pf_need, q8_prefill_workspace_bytes(p.K, self.M))
+                calls.append(Call("prefill", p.name, li, p.N, p.K, W=W, x=x, y=y))
+                continue
+            ws_need = max(ws_need, q8_workspace_bytes(p.N, p.K, self.M))
             if self.mode == "fused" or (self.mode == "shared" and not shared_input):
                 calls.append(Call("fused", p.name, li, p.N, p.K, W=W, x=x, y=y))
             else:
@@ -93,6 +101,8 @@ class Q8Stack:
         self.calls = calls
         self.workspace = (torch.zeros(ws_need, dtype=torch.uint8, device=dev)
                           if ws_need else None)
+        self.pf_workspace = (torch.empty(pf_need, dtype=torch.uint8, device=dev)
+                             if pf_need else None)
         self.refill_inputs(step=0)
         torch.cuda.synchronize()
 
@@ -115,6 +125,9 @@ class Q8Stack:
         for c in self.calls:
             if c.kind == "quant":
                 q8_quantize_act(c.x, c.A, flags=flags, stream=stream)
+            elif c.kind == "prefill":
+                q8_fused_quant_gemm_prefill(c.W, c.N, c.K, c.x, self.M, c.y, self.pf_workspace, flags=flags,
+                                            stream=stream)
             elif c.kind == "gemm":
                 q8_gemm(c.W, c.N, c.K, c.A, self.M, c.y, workspace=ws, flags=gflags, stream=stream)
             else:
@@ -138,8 +151,17 @@ class Q8Stack:
     def launches_per_step(self) -> int:
         n = 0
         for c in self.calls:
-            n += 1 if c.kind == "quant" else (self.M + 15) // 16
+            if c.kind == "quant":
+                n += 1
+            elif c.kind == "prefill":
+                n += 3  # quantize, pack, tile GEMM
+            else:
+                n += (self.M + 15) // 16
         return n
+
+    def mac_per_step(self) -> int:
+        """Multiply-accumulates of one step: M * sum of N * K."""
+        return self.M * sum(c.N * c.K for c in self.calls if c.kind != "quant")
 
     def weight_bytes(self) -> int:
         return sum(W.numel() for W in self.weights.values())

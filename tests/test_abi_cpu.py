@@ -112,6 +112,28 @@ def test_host_argument_checks_reject_before_any_device_work(lib):
     assert e(fake, 64, 64, fake, 0, fake, 0, None) == -2                        # M = 0
     assert e(fake, 64, 64, fake, 1, odd, 0, None) == -2                         # 16-row tiles: no layout
     assert lib.q8_fused_quant_gemm_swiglu(fake, 8192, 64, None, 1, fake, 0, None) == -1
+    pf = lib.q8_gemm_prefill
+    big = 1 << 20
+    assert pf(None, 64, 64, fake, 1, y, fake, big, 0, None) == -1              # null W
+    assert pf(fake, 64, 64, None, 1, y, fake, big, 0, None) == -1              # null A
+    assert pf(fake, 64, 64, fake, 1, None, fake, big, 0, None) == -1           # null y
+    assert pf(fake, 64, 64, fake, 1, y, fake, big, 2, None) == -1              # only Q8_FLAG_PDL
+    assert pf(fake, 64, 48, fake, 1, y, fake, big, 0, None) == -2              # K % 32
+    assert pf(fake, 64, 65536 + 32, fake, 1, y, fake, big, 0, None) == -2      # K > Q8_MAX_PREFILL_K
+    assert pf(fake, 0, 64, fake, 1, y, fake, big, 0, None) == -2               # N = 0
+    assert pf(fake, 64, 64, fake, 0, y, fake, big, 0, None) == -2              # M = 0
+    assert pf(odd, 64, 64, fake, 1, y, fake, big, 0, None) == -3               # W misaligned
+    assert pf(fake, 64, 64, odd, 1, y, fake, big, 0, None) == -3               # A misaligned
+    assert pf(fake, 64, 64, fake, 1, y, eight, big, 0, None) == -3             # workspace 8-aligned
+    assert pf(fake, 64, 64, fake, 3, y, None, big, 0, None) == -6              # no workspace
+    assert pf(fake, 64, 64, fake, 3, y, fake, 3 * 2 * 34 - 1, 0, None) == -6   # one byte short
+    fq = lib.q8_fused_quant_gemm_prefill
+    assert fq(fake, 64, 64, None, 1, y, None, fake, big, 0, None) == -1        # null x
+    assert fq(fake, 64, 64, fake, 1, y, odd, fake, big, 0, None) == -3         # A_blocks_out odd
+    assert fq(fake, 64, 64, fake, 3, y, None, fake, 2 * 208 - 1, 0, None) == -6  # x's blocks need room too
+    assert lib.q8_prefill_workspace_bytes(64, 3) == 2 * 208                    # 3*2*34 = 204 -> 208, twice
+    assert lib.q8_prefill_workspace_bytes(65536 + 32, 3) == 0
+    assert lib.q8_prefill_workspace_bytes(64, 0) == 0
     s = lib.q8_swiglu_quantize
     assert s(None, 1, 64, fake, 0, None) == -1
     assert s(fake, 1, 64, fake, 2, None) == -1                                  # unknown flag
