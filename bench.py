@@ -557,7 +557,7 @@ def producers(q8, shape, launches=20):
     return out
 
 
-def prefill(q8, st, M=512, steps=3, tile_rows=(512, 2048)):
+def prefill(q8, st, M=512, steps=3, tile_rows=(512, 2048), decode_passes=True, warmup=2):
     """Prefill over the same projection stack, each case one CUDA graph:
     the prefill tile GEMM (q8_fused_quant_gemm_prefill: quantize, pack, one
     tile GEMM per projection; each 128-row weight tile reused across 128
@@ -572,7 +572,7 @@ def prefill(q8, st, M=512, steps=3, tile_rows=(512, 2048)):
 
     def timed(s2, n):
         g = s2.capture()
-        for _ in range(2):
+        for _ in range(warmup):
             g.replay()
         torch.cuda.synchronize()
         cur = torch.cuda.current_stream()
@@ -598,6 +598,8 @@ def prefill(q8, st, M=512, steps=3, tile_rows=(512, 2048)):
         res["tile_gemm"].append(ent)
         del s2
         torch.cuda.empty_cache()
+    if not decode_passes:
+        return res
     s2 = Q8Stack(st.shape, M=M, mode="fused", layers=st.n_layers, shared_weights=st.weights)
     ms = timed(s2, steps)
     res["decode_gemv_passes"] = {"M": M, "ms_per_step": round(ms, 3), "tok_s": round(M / (ms * 1e-3), 1),
@@ -701,6 +703,25 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_prefill_only(args):
+    """The prefill leg alone (for profiling): the tile GEMM over the stack at
+    --prefill-only rows, --warmup untimed and --steps timed graph replays."""
+    import torch
+
+    import __graft_entry__
+    import q8_synth
+    __graft_entry__.build()
+    import q8_block_quantized_gb300 as q8
+    from q8_block_quantized_gb300.stack import Q8Stack
+    shape = q8_synth.LLAMA_1B if args.model == "1b" else q8_synth.LLAMA_3B
+    st = Q8Stack(shape, M=1, mode="fused", layers=args.layers)
+    res = prefill(q8, st, steps=max(args.steps, 1), tile_rows=(args.prefill_only,), decode_passes=False,
+                  warmup=args.warmup)
+    res["layers"] = st.n_layers
+    print(json.dumps(res))
+    torch.cuda.synchronize()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -716,8 +737,13 @@ def main():
                     help="skip the fused-producer and tcgen05-variant measurements")
     ap.add_argument("--tcgen05", action="store_true",
                     help="GEMV calls with Q8_FLAG_TCGEN05 (tcgen05 block dots where they apply)")
+    ap.add_argument("--prefill-only", type=int, default=0, metavar="ROWS",
+                    help="only time the prefill tile GEMM over the stack at ROWS tokens (one JSON line; "
+                         "not the benchmark line)")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.prefill_only:
+        run_prefill_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

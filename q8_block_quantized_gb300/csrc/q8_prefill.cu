@@ -7,15 +7,26 @@
 // One CTA computes one 128 (weight rows) x 128 (activation rows) output
 // tile at a time, persistent over the tiles.  Per 32-block b:
 //   - the worker warps convert the block's int8 quants of both operands to
-//     fp16 (exact) in the no-swizzle K-major layout of the tensor cores;
+//     fp16 (exact) in the no-swizzle K-major layout of the tensor cores, and
+//     the activation scales d_a to fp32 in shared memory;
 //   - one thread issues two tcgen05.mma (K = 16 each) into a 128 x 128 fp32
 //     accumulator in tensor memory: every entry is the exact integer block
 //     dot isum_b (|isum| <= 516128 < 2^24);
 //   - the worker warps read the accumulator back (tcgen05.ld) and fold it
-//     into their rows' sums in the fixed order below, on the CUDA cores.
-// The MMA of block b runs while the workers convert block b + 1's operands
-// and fold block b - 1 (two accumulators, two operand buffers; a fold two
-// blocks behind with three of each measured slower).
+//     into their rows' sums in the fixed order below: per output and block
+//     one multiply (d_w d_a, exact) and one fma, two outputs per f32x2 op.
+// The MMA of block b runs while the workers convert block b + 1 and fold
+// block b - 1 (two accumulators, two operand buffers).  Tensor memory: the
+// two accumulators and the segment sums Y (384 of 512 columns).  Warp
+// roles: 8 worker warps (two warpgroups, 216 registers each after
+// setmaxnreg) convert and fold; in a third warpgroup (72 registers) one
+// thread issues a block's MMAs once all 8 workers have converted it, and
+// another issues the bulk copies of a chunk into a stage once all 8 have
+// converted the last block of the chunk it held.  Only mbarriers connect
+// them; a CTA-wide barrier per block and a single thread issuing both MMAs
+// and copies measured 1.6x slower, as did the scale products by a rank-1
+// MMA (its accumulator fits only once, which chained each block's MMA
+// latency behind the previous block's fold).
 //
 // Fixed order of one output y[m][n] (the same whatever M is and wherever
 // row m sits in the launch, so a prompt filled in slices equals the prompt
@@ -39,35 +50,44 @@ namespace {
 constexpr int PF_TN = Q8_PREFILL_TILE_ROWS;  // weight rows per tile: MMA M, tensor-memory lanes
 constexpr int PF_TM = Q8_PREFILL_TILE_ROWS;  // activation rows per tile: MMA N
 constexpr int PF_SEG = Q8_PREFILL_SEGMENT;   // blocks per segment of the summation order
-constexpr int PF_NW = 8;                     // worker warps
-constexpr int PF_WT = PF_NW * 32;            // worker threads
-constexpr int PF_THREADS = PF_WT + 32;       // + one producer warp
+constexpr int PF_NW = 8;                     // worker warps (warpgroups 0 and 1)
+constexpr int PF_WT = PF_NW * 32;
+constexpr int PF_THREADS = PF_WT + 128;      // + warpgroup 2: MMA issuer, copy issuer, two idle warps
+// Registers: launched at 65536 / 384 = 168 per thread; warpgroup 2 gives
+// back down to 72, the workers take 216: per SM sub-partition
+// 2 x 32 x 216 + 32 x 72 = 16128 <= 16384, in all
+// 256 x 216 + 128 x 72 = 64512 = 384 x 168.
+constexpr int PF_REG_LAUNCH = 168, PF_REG_WORKER = 216, PF_REG_ISSUER = 72;
+static_assert(PF_WT * PF_REG_WORKER + 128 * PF_REG_ISSUER <= PF_THREADS * PF_REG_LAUNCH, "register split");
 constexpr int PF_STAGES = 2;
 constexpr int PF_CHUNK = MAX_TILE_ROWS * CHUNK_BLOCKS * BLOCK_BYTES;  // 34816: one chunk of 128 rows
 constexpr int PF_STAGE = 2 * PF_CHUNK;                                // weights, then activations
 constexpr int PF_SLICE = 128 * 16 * 2;  // fp16 operand of one MMA: 128 rows x 16 k
 constexpr int PF_OPS = 4 * PF_SLICE;    // one block: weight halves 0, 1; activation halves 0, 1
 constexpr int PF_NBUF = 2;              // accumulators and operand buffers in flight
-constexpr int PF_DA_BUFS = PF_NBUF + 1; // activation scales: written at conversion, read a block later
-constexpr uint32_t PF_TMEM_COLS = 512;  // accumulators of two blocks (128 columns each), then the sums Y
-constexpr uint32_t PF_Y_COL = PF_NBUF * PF_TM;
+// fp32 activation scales of a block: written at its conversion, read at its
+// fold a block later; a warp can be at most three blocks ahead of another
+constexpr int PF_DA_BUFS = 4;
+constexpr uint32_t PF_Y_COL = PF_NBUF * PF_TM;  // the segment sums Y
+constexpr uint32_t PF_TMEM_COLS = 512;
 constexpr size_t PF_OFF_OPS = (size_t)PF_STAGES * PF_STAGE;
 constexpr size_t PF_OFF_DA = PF_OFF_OPS + (size_t)PF_NBUF * PF_OPS;
 constexpr size_t PF_OFF_BAR = PF_OFF_DA + (size_t)PF_DA_BUFS * PF_TM * sizeof(float);
-constexpr size_t PF_SMEM = PF_OFF_BAR + (2 * PF_STAGES + PF_NBUF + 1) * sizeof(uint64_t) + 4 * sizeof(int);
-static_assert(PF_Y_COL + PF_TM <= PF_TMEM_COLS, "tensor-memory columns");
+constexpr size_t PF_SMEM = PF_OFF_BAR + (2 * PF_STAGES + 2 * PF_NBUF) * sizeof(uint64_t) + 4 * sizeof(int);
 static_assert(PF_OFF_OPS % 1024 == 0, "operand buffers aligned");
 static_assert(PF_SMEM <= 232448, "shared memory per CTA");
 static_assert(PF_TN == 128 && PF_TM == 128, "one MMA shape: M = N = 128");
+static_assert(PF_Y_COL + PF_TM <= PF_TMEM_COLS, "tensor-memory columns");
 
-enum : unsigned { ERR_PF_PRODUCER = 8u, ERR_PF_WORKER = 16u, ERR_PF_DRAIN = 32u };
+enum : unsigned { ERR_PF_WORKER = 16u, ERR_PF_DRAIN = 32u, ERR_PF_ISSUER = 64u, ERR_PF_PRODUCER = 128u };
 
 struct PrefillArgs {
   const uint8_t* W;  // packed weights, tiles of RW rows
   const uint8_t* A;  // packed activations, tiles of 128 rows
   float* y;          // [M][N]
-  int64_t N, M, NB, nch;
-  int64_t tn, tm, tiles;  // output tiles along N, along M, in all
+  int64_t N;
+  int M, NB, nch;
+  int tm, tiles;     // output tiles along M, in all (< 2^31, checked on the host)
   int RW;
   unsigned* err;
 };
@@ -89,61 +109,106 @@ __device__ __forceinline__ float half_at(const uint8_t* p) {
   return __half2float(*reinterpret_cast<const __half*>(p));
 }
 
-// Producer (one thread): per tile and chunk, the chunk of the 128/RW weight
-// tiles and of the activation tile, each one bulk copy (a ragged tail of
-// under 16 bytes by hand), completing on full[stage].
-__device__ __forceinline__ void pf_produce(const PrefillArgs& a, uint8_t* smem, uint64_t* full,
-                                           uint64_t* empty, volatile int* misc) {
-  const uint64_t pol_w = l2_policy_evict_normal();  // other CTAs read the same weight tile
-  const uint64_t pol_a = l2_policy_evict_last();    // every weight tile's CTA reads it
+// Chunk c of tile (nt, mt) into stage `stage`: the chunk of each of the
+// 128/RW weight tiles and of the activation tile, one bulk copy each (a
+// ragged tail under 16 bytes by hand), completing on full[stage].
+__device__ __noinline__ void pf_issue(const PrefillArgs& a, uint8_t* smem, uint64_t* full, int nt, int mt, int c,
+                                      int stage) {
+  const int ra = tile_rows(mt, a.M, PF_TM);
+  const int kb = chunk_blocks(c, a.NB);
   const int G = PF_TN / a.RW;
-  int stage = 0;
-  uint32_t phase = 0;
-  int issued = 0;
-  for (int64_t T = blockIdx.x; T < a.tiles; T += gridDim.x) {
-    const int64_t nt = T / a.tm, mt = T - (T / a.tm) * a.tm;
-    const int ra = tile_rows(mt, a.M, PF_TM);
-    for (int64_t c = 0; c < a.nch; ++c) {
-      if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, WAIT_LIMIT_NS)) {
-        atomicOr(a.err, ERR_PF_PRODUCER);
-        misc[3] = 1;
+  uint8_t* dst = smem + (size_t)stage * PF_STAGE;
+  const uint64_t pol_w = l2_policy_evict_normal();  // the other m-tiles' CTAs read the same weights
+  const uint64_t pol_a = l2_policy_evict_last();    // every weight tile's CTA reads the activations
+  for (int g = 0; g <= G; ++g) {  // g < G: weight tiles; g == G: the activation tile
+    const uint8_t* src;
+    uint8_t* d;
+    uint32_t bytes;
+    uint64_t pol;
+    if (g < G) {
+      const int64_t tw = (int64_t)nt * G + g;
+      if (tw * a.RW >= a.N) continue;
+      const int rw = tile_rows(tw, a.N, a.RW);
+      src = a.W + chunk_offset(tw, c, rw, a.RW, a.NB);
+      d = dst + (size_t)g * a.RW * CHUNK_BLOCKS * BLOCK_BYTES;
+      bytes = (uint32_t)(kb * rw * BLOCK_BYTES);
+      pol = pol_w;
+    } else {
+      src = a.A + chunk_offset(mt, c, ra, PF_TM, a.NB);
+      d = dst + PF_CHUNK;
+      bytes = (uint32_t)(kb * ra * BLOCK_BYTES);
+      pol = pol_a;
+    }
+    const uint32_t bulk = bytes & ~15u;
+    for (uint32_t i = bulk; i < bytes; ++i) d[i] = src[i];
+    if (bulk) {
+      mbar_expect_tx(&full[stage], bulk);
+      bulk_g2s(d, src, bulk, &full[stage], pol);
+    }
+  }
+  mbar_arrive(&full[stage]);
+}
+
+// The copy issuer: this CTA's chunks in order, chunk k into stage k % 2
+// once the 8 workers have released the stage (chunk k - 2 converted).
+__device__ __forceinline__ void pf_producer(const PrefillArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                            volatile int* misc) {
+  uint32_t k = 0;
+  for (int T = blockIdx.x; T < a.tiles; T += gridDim.x) {
+    const int nt = T / a.tm, mt = T - nt * a.tm;
+    for (int c = 0; c < a.nch; ++c, ++k) {
+      const int stage = (int)(k & 1u);
+      if (misc[0] != 0 || !mbar_wait_bounded(&empty[stage], ((k >> 1) & 1u) ^ 1u, WAIT_LIMIT_NS)) {
+        if (misc[0] == 0) atomicOr(a.err, ERR_PF_PRODUCER);
+        misc[0] = 1;
+        misc[1] = (int)k;  // copies issued
         return;
       }
+      pf_issue(a, smem, full, nt, mt, c, stage);
+    }
+  }
+  misc[1] = (int)k;
+}
+
+// The MMA issuer: per block, once the 8 workers have arrived on opready
+// (operands converted, and their fold of the block two back, which used the
+// same accumulator, done), the block's two MMAs and their commit.
+__device__ __forceinline__ void pf_issuer(const PrefillArgs& a, uint8_t* smem, uint64_t* opready, uint64_t* mma_bar,
+                                          volatile int* misc, uint32_t tmem) {
+  const uint32_t IDESC = umma_idesc_f16(PF_TN, PF_TM);
+  uint32_t b = 0;           // blocks issued (only its low bits are used)
+  uint32_t mma_issued = 0;  // bit p: parity of accumulator p's MMAs so far; bit 2 + p: any
+  bool stop = false;
+  for (int T = blockIdx.x; T < a.tiles && !stop; T += gridDim.x) {
+    for (int c = 0; c < a.nch && !stop; ++c) {
       const int kb = chunk_blocks(c, a.NB);
-      uint8_t* dst = smem + (size_t)stage * PF_STAGE;
-      for (int g = 0; g <= G; ++g) {  // g < G: weight tiles; g == G: the activation tile
-        const uint8_t* src;
-        uint8_t* d;
-        uint32_t bytes;
-        uint64_t pol;
-        if (g < G) {
-          const int64_t tw = nt * G + g;
-          if (tw * a.RW >= a.N) continue;
-          const int rw = tile_rows(tw, a.N, a.RW);
-          src = a.W + chunk_offset(tw, c, rw, a.RW, a.NB);
-          d = dst + (size_t)g * a.RW * CHUNK_BLOCKS * BLOCK_BYTES;
-          bytes = (uint32_t)(kb * rw * BLOCK_BYTES);
-          pol = pol_w;
-        } else {
-          src = a.A + chunk_offset(mt, c, ra, PF_TM, a.NB);
-          d = dst + PF_CHUNK;
-          bytes = (uint32_t)(kb * ra * BLOCK_BYTES);
-          pol = pol_a;
+      for (int j = 0; j < kb; ++j, ++b) {
+        const int pb = (int)(b & 1u);
+        if (misc[0] != 0 || !mbar_wait_bounded(&opready[pb], (b >> 1) & 1u, WAIT_LIMIT_NS)) {
+          if (misc[0] == 0) atomicOr(a.err, ERR_PF_ISSUER);
+          misc[0] = 1;
+          stop = true;
+          break;
         }
-        const uint32_t bulk = bytes & ~15u;
-        for (uint32_t k = bulk; k < bytes; ++k) d[k] = src[k];
-        if (bulk) {
-          mbar_expect_tx(&full[stage], bulk);
-          bulk_g2s(d, src, bulk, &full[stage], pol);
-        }
-      }
-      mbar_arrive(&full[stage]);
-      misc[1] = ++issued;
-      if (++stage == PF_STAGES) {
-        stage = 0;
-        phase ^= 1u;
+        tc_fence_after_sync();
+        uint8_t* ops = smem + PF_OFF_OPS + (size_t)pb * PF_OPS;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          umma_f16(tmem + (uint32_t)(pb * PF_TM), umma_smem_desc(smem_u32(ops + h * PF_SLICE), 128, 256),
+                   umma_smem_desc(smem_u32(ops + (2 + h) * PF_SLICE), 128, 256), IDESC, h == 1);
+        umma_commit(&mma_bar[pb]);
+        mma_issued = (mma_issued ^ (1u << pb)) | (4u << pb);
       }
     }
+  }
+  if (misc[0] != 0) {
+    // stopped early: let the MMAs in flight land before the tensor memory
+    // is given back (the last MMA on accumulator p completes the phase of
+    // parity bit p ^ 1)
+    for (int p = 0; p < PF_NBUF; ++p)
+      if (((mma_issued >> (2 + p)) & 1u) &&
+          !mbar_wait_bounded(&mma_bar[p], ((mma_issued >> p) & 1u) ^ 1u, WAIT_LIMIT_NS))
+        atomicOr(a.err, ERR_PF_DRAIN);
   }
 }
 
@@ -151,22 +216,23 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const PrefillArg
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + PF_OFF_BAR);
   uint64_t* empty = full + PF_STAGES;
-  uint64_t* mma_bar = empty + PF_STAGES;
-  // misc[0]: the workers' abort flag (written and read only by workers);
-  // misc[1]: chunks issued; misc[2]: tensor-memory base; misc[3]: producer stopped
-  volatile int* misc = reinterpret_cast<volatile int*>(mma_bar + PF_NBUF + 1);
+  uint64_t* opready = empty + PF_STAGES;
+  uint64_t* mma_bar = opready + PF_NBUF;
+  // misc[0]: abort flag; misc[1]: chunks the producer issued; misc[2]: tensor-memory base
+  volatile int* misc = reinterpret_cast<volatile int*>(mma_bar + PF_NBUF);
   float* da_s = reinterpret_cast<float*>(smem + PF_OFF_DA);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
   if (tid == 0) {
     for (int s = 0; s < PF_STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], PF_NW);
     }
-    for (int p = 0; p < PF_NBUF; ++p) mbar_init(&mma_bar[p], 1);
+    for (int p = 0; p < PF_NBUF; ++p) {
+      mbar_init(&opready[p], PF_NW);
+      mbar_init(&mma_bar[p], 1);
+    }
     misc[0] = 0;
     misc[1] = 0;
-    misc[3] = 0;
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(reinterpret_cast<uint32_t*>(const_cast<int*>(misc + 2)), PF_TMEM_COLS);
@@ -177,15 +243,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const PrefillArg
   pdl_launch_dependents();
   pdl_wait();  // activations and y belong to the previous work on the stream
 
-  // worker state that the drain at the end needs (thread 0's copy)
-  int consumed = 0;
-  uint32_t pending = 0u;  // bit p: an MMA into accumulator p not yet waited for
-  uint32_t mph = 0u;      // bit p: parity of accumulator p's next MMA completion
-
-  if (warp == PF_NW) {
-    if (lane == 0) pf_produce(a, smem, full, empty, misc);
-    __syncwarp();
+  uint32_t consumed = 0;  // chunks whose copies the workers saw land (warp 0's count)
+  if (warp >= PF_NW) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PF_REG_ISSUER));
+    if (warp == PF_NW && lane == 0) pf_issuer(a, smem, opready, mma_bar, misc, tmem);
+    if (warp == PF_NW + 1 && lane == 0) pf_producer(a, smem, full, empty, misc);
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(PF_REG_WORKER));
     // thread (warp w, lane l): weight row `row` of the tile = tensor-memory
     // lane 32 (w % 4) + l, which it also converts; columns [64 hf, 64 hf + 64)
     // of the accumulators; half hf of each block's 32 quants when converting
@@ -194,69 +258,59 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const PrefillArg
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int G = PF_TN / a.RW;
     const int g = row / a.RW, ii = row - g * a.RW;
-    const uint32_t IDESC = umma_idesc_f16(PF_TN, PF_TM);
-    int stage = 0;
-    uint32_t sphase = 0;
-    int64_t bc = 0;  // blocks this CTA has issued, over all its tiles
+    uint32_t bc = 0;    // blocks converted, over all this CTA's tiles (low bits used)
+    uint32_t kseq = 0;  // chunks
     bool dead = false;
 
-    for (int64_t T = blockIdx.x; T < a.tiles && !dead; T += gridDim.x) {
-      const int64_t nt = T / a.tm, mt = T - (T / a.tm) * a.tm;
+    for (int T = blockIdx.x; T < a.tiles && !dead; T += gridDim.x) {
+      const int nt = T / a.tm, mt = T - (T / a.tm) * a.tm;
       const int ra = tile_rows(mt, a.M, PF_TM);
-      const int64_t tw = nt * G + g;
+      const int64_t tw = (int64_t)nt * G + g;
       const int rw = tw * a.RW < a.N ? tile_rows(tw, a.N, a.RW) : 0;
       const bool wv = ii < rw;  // this row exists (n < N)
       uint64_t sig[32];         // sigma of columns 64 hf + 2e, + 2e + 1
 #pragma unroll
       for (int e = 0; e < 32; ++e) sig[e] = 0ull;
       bool first_seg = true;
-      // the block whose accumulator is still to be read
-      int64_t q1_blk = -1;
-      int q1_pb = 0, q1_d = 0;
+      int q1_blk = -1;  // the block whose accumulator is still to be read
+      uint32_t q1_bc = 0;
       float q1_dw = 0.0f;
 
-      // Fold the accumulator of block b (buffer pb, activation scales d3,
-      // weight scale dw) into sigma; at a segment's end into Y; at the
-      // tile's end store Y.  Warp-uniform control flow throughout.
-      auto fold = [&](int64_t b, int pb, int d3, float dw) {
-        bool ok = mbar_wait_bounded(&mma_bar[pb], (mph >> pb) & 1u, WAIT_LIMIT_NS);
-        if (!ok) {
-          atomicOr(a.err, ERR_PF_WORKER);
-          misc[0] = 1;
-        }
+      // Fold block b (the CTA's block number bcn: accumulator bcn % 2,
+      // activation scales bcn % 4, weight scale dw) into sigma; at a
+      // segment's end into Y; at the tile's end store Y.  Warp-uniform.
+      auto fold = [&](int b, uint32_t bcn, float dw) -> bool {
+        const int pb = (int)(bcn & 1u);
+        bool ok = mbar_wait_bounded(&mma_bar[pb], (bcn >> 1) & 1u, WAIT_LIMIT_NS);
         ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
-          mph ^= 1u << pb;
-          pending &= ~(1u << pb);
-        }
         tc_fence_after_sync();
-        if (!ok) return;
-        const float* dap = da_s + d3 * PF_TM + hf * 64;
-        const uint64_t dw2 = f2_pack(dw, dw);
+        if (!ok) return false;
         const uint32_t acc = tmem + lane_base + (uint32_t)(pb * PF_TM + hf * 64);
+        const float* dap = da_s + (bcn % PF_DA_BUFS) * PF_TM + hf * 64;
+        const uint64_t dw2 = f2_pack(dw, dw);
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t u0[16], u1[16];
-          tmem_ld16(acc + q * 32, u0);
-          tmem_ld16(acc + q * 32 + 16, u1);
+        for (int q = 0; q < 4; ++q) {
+          uint32_t u[16];
+          tmem_ld16(acc + q * 16, u);  // isum
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float4 d4 = *reinterpret_cast<const float4*>(dap + q * 32 + 4 * e);
-            const uint32_t* u = e < 4 ? u0 : u1;
-            const int k = (e & 3) * 4;
-            const uint64_t s01 = f2_mul(dw2, f2_pack(d4.x, d4.y));
+          for (int e = 0; e < 4; ++e) {
+            const float4 d4 = *reinterpret_cast<const float4*>(dap + q * 16 + 4 * e);
+            const uint64_t s01 = f2_mul(dw2, f2_pack(d4.x, d4.y));  // d_w * d_a, exact
             const uint64_t s23 = f2_mul(dw2, f2_pack(d4.z, d4.w));
-            sig[q * 16 + 2 * e] = f2_fma(f2_pack(__uint_as_float(u[k]), __uint_as_float(u[k + 1])), s01,
-                                         sig[q * 16 + 2 * e]);
-            sig[q * 16 + 2 * e + 1] = f2_fma(f2_pack(__uint_as_float(u[k + 2]), __uint_as_float(u[k + 3])), s23,
-                                             sig[q * 16 + 2 * e + 1]);
+            sig[q * 8 + 2 * e] = f2_fma(f2_pack(__uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1])), s01,
+                                        sig[q * 8 + 2 * e]);
+            sig[q * 8 + 2 * e + 1] = f2_fma(f2_pack(__uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3])),
+                                            s23, sig[q * 8 + 2 * e + 1]);
           }
         }
         const bool last = b == a.NB - 1;
-        if (!last && (b + 1) % PF_SEG != 0) return;
-        // end of a segment: Y = Y + sigma (Y = +0 + sigma for the first)
-        const uint32_t ycol = tmem + lane_base + PF_Y_COL + (uint32_t)(hf * 64);
+        if (!last && (b + 1) % PF_SEG != 0) return true;
+        // end of a segment: Y = Y + sigma (from +0), Y in tensor memory
+        const uint32_t yc = tmem + lane_base + PF_Y_COL + (uint32_t)(hf * 64);
+        float* yp = a.y + ((int64_t)mt * PF_TM + hf * 64) * a.N + (int64_t)nt * PF_TN + row;
+        const int64_t N = a.N;
+        const int mleft = wv ? ra - hf * 64 : 0;  // columns of this thread inside the tile
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t yv[16];
@@ -264,110 +318,89 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const PrefillArg
 #pragma unroll
             for (int k = 0; k < 16; ++k) yv[k] = 0u;
           } else {
-            tmem_ld16(ycol + q * 16, yv);
+            tmem_ld16(yc + q * 16, yv);
             tmem_ld_wait();
           }
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const uint64_t y2 = f2_add(f2_pack(__uint_as_float(yv[2 * e]), __uint_as_float(yv[2 * e + 1])),
-                                       sig[q * 8 + e]);
             float lo, hi;
-            f2_unpack(y2, lo, hi);
-            yv[2 * e] = __float_as_uint(lo);
-            yv[2 * e + 1] = __float_as_uint(hi);
+            f2_unpack(f2_add(f2_pack(__uint_as_float(yv[2 * e]), __uint_as_float(yv[2 * e + 1])), sig[q * 8 + e]),
+                      lo, hi);
             sig[q * 8 + e] = 0ull;
-          }
-          if (last) {
-            const int64_t n = nt * PF_TN + row;
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const int m = hf * 64 + q * 16 + k;
-              if (wv && m < ra) a.y[(mt * PF_TM + m) * a.N + n] = __uint_as_float(yv[k]);
+            if (last) {  // y[mt*128 + m][n] through a pointer stepped by N
+              if (q * 16 + 2 * e < mleft) *yp = lo;
+              yp += N;
+              if (q * 16 + 2 * e + 1 < mleft) *yp = hi;
+              yp += N;
+            } else {
+              yv[2 * e] = __float_as_uint(lo);
+              yv[2 * e + 1] = __float_as_uint(hi);
             }
-          } else {
-            tmem_st16(ycol + q * 16, yv);
           }
+          if (!last) tmem_st16(yc + q * 16, yv);
         }
         if (!last) tmem_st_wait();
         first_seg = false;
+        return true;
       };
 
-      for (int64_t c = 0; c < a.nch && !dead; ++c) {
-        const bool got = mbar_wait_bounded(&full[stage], sphase, WAIT_LIMIT_NS);
-        if (got) {
-          ++consumed;  // chunks whose copies have landed
-        } else {
-          atomicOr(a.err, ERR_PF_WORKER);
-          misc[0] = 1;
+      for (int c = 0; c < a.nch && !dead; ++c, ++kseq) {
+        const int stage = (int)(kseq & 1u);
+        const bool got =
+            __all_sync(0xffffffffu, misc[0] == 0 && mbar_wait_bounded(&full[stage], (kseq >> 1) & 1u, WAIT_LIMIT_NS));
+        if (!got) {
+          dead = true;
+          break;
         }
+        if (warp == 0) ++consumed;
         const int kb = chunk_blocks(c, a.NB);
         const uint8_t* cw = smem + (size_t)stage * PF_STAGE + (size_t)g * a.RW * CHUNK_BLOCKS * BLOCK_BYTES;
         const uint8_t* ca = smem + (size_t)stage * PF_STAGE + PF_CHUNK;
         for (int j = 0; j < kb; ++j) {
-          const int pb = (int)(bc % PF_NBUF), d3 = (int)(bc % PF_DA_BUFS);
+          const int pb = (int)(bc & 1u);
           uint8_t* ops = smem + PF_OFF_OPS + (size_t)pb * PF_OPS;
-          float dw = 0.0f;
-          if (got) {
-            const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-            const uint4 qw = wv ? lds128(cw + chunk_quant_off(j, hf, ii, rw)) : zero;
-            put_f16_row(ops + hf * PF_SLICE + (row >> 3) * 256 + (row & 7) * 16, qw);
-            const uint4 qa = row < ra ? lds128(ca + chunk_quant_off(j, hf, row, ra)) : zero;
-            put_f16_row(ops + (2 + hf) * PF_SLICE + (row >> 3) * 256 + (row & 7) * 16, qa);
-            if (hf == 0) da_s[d3 * PF_TM + row] = row < ra ? half_at(ca + chunk_scale_off(j, row, ra, kb)) : 0.0f;
-            dw = wv ? half_at(cw + chunk_scale_off(j, ii, rw, kb)) : 0.0f;
-          }
-          if (j == kb - 1) {  // this warp has read all it needs of the stage
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stage]);
-          }
+          const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+          const int rofs = (row >> 3) * 256 + (row & 7) * 16;
+          const uint4 qw = wv ? lds128(cw + chunk_quant_off(j, hf, ii, rw)) : zero;
+          put_f16_row(ops + hf * PF_SLICE + rofs, qw);
+          const uint4 qa = row < ra ? lds128(ca + chunk_quant_off(j, hf, row, ra)) : zero;
+          put_f16_row(ops + (2 + hf) * PF_SLICE + rofs, qa);
+          if (hf == 1) da_s[(bc % PF_DA_BUFS) * PF_TM + row] = row < ra ? half_at(ca + chunk_scale_off(j, row, ra, kb)) : 0.0f;
+          const float dw = wv ? half_at(cw + chunk_scale_off(j, ii, rw, kb)) : 0.0f;
           fence_proxy_async_smem();
           tc_fence_before_sync();
-          named_bar_sync(1, PF_WT);
-          if (misc[0] != 0) {  // read after the barrier: the same in every worker
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&opready[pb]);
+            if (j == kb - 1) mbar_arrive(&empty[stage]);  // this warp is done with the stage
+          }
+          if (q1_blk >= 0 && !fold(q1_blk, q1_bc, q1_dw)) {
             dead = true;
             break;
           }
-          if (tid == 0) {
-            tc_fence_after_sync();
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-              umma_f16(tmem + (uint32_t)(pb * PF_TM),
-                       umma_smem_desc(smem_u32(ops + h * PF_SLICE), 128, 256),
-                       umma_smem_desc(smem_u32(ops + (2 + h) * PF_SLICE), 128, 256), IDESC, h == 1);
-            umma_commit(&mma_bar[pb]);
-          }
-          pending |= 1u << pb;
-          if (q1_blk >= 0) fold(q1_blk, q1_pb, q1_d, q1_dw);
           q1_blk = c * CHUNK_BLOCKS + j;
-          q1_pb = pb;
-          q1_d = d3;
+          q1_bc = bc;
           q1_dw = dw;
           ++bc;
         }
-        if (dead) break;
-        if (++stage == PF_STAGES) {
-          stage = 0;
-          sphase ^= 1u;
-        }
       }
-      if (!dead && q1_blk >= 0) fold(q1_blk, q1_pb, q1_d, q1_dw);
+      if (!dead && q1_blk >= 0 && !fold(q1_blk, q1_bc, q1_dw)) dead = true;
+    }
+    if (dead) {
+      if (lane == 0) atomicOr(a.err, ERR_PF_WORKER);
+      misc[0] = 1;
     }
   }
 
-  __syncthreads();
-  if (tid == 0 && (misc[0] != 0 || misc[3] != 0)) {
-    // stopped early: let the MMAs and copies in flight land before the
-    // tensor memory and the CTA's shared memory are given back
-    for (int p = 0; p < PF_NBUF; ++p)
-      if (((pending >> p) & 1u) && !mbar_wait_bounded(&mma_bar[p], (mph >> p) & 1u, WAIT_LIMIT_NS))
-        atomicOr(a.err, ERR_PF_DRAIN);
-    const int issued = misc[1];
-    for (int k = consumed; k < issued; ++k)
-      if (!mbar_wait_bounded(&full[k % PF_STAGES], (uint32_t)((k / PF_STAGES) & 1), WAIT_LIMIT_NS))
-        atomicOr(a.err, ERR_PF_DRAIN);
-  }
   tc_fence_before_sync();
   __syncthreads();
+  if (tid == 0 && misc[0] != 0) {
+    // stopped early: let the copies in flight land before the shared
+    // memory is given back
+    const uint32_t issued = (uint32_t)misc[1];
+    for (uint32_t k = consumed; k < issued; ++k)
+      if (!mbar_wait_bounded(&full[k & 1u], (k >> 1) & 1u, WAIT_LIMIT_NS)) atomicOr(a.err, ERR_PF_DRAIN);
+  }
   if (warp == 0) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, PF_TMEM_COLS);
@@ -398,13 +431,14 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const uint8_t* W, int64_t N, i
   a.A = A_packed;
   a.y = y;
   a.N = N;
-  a.M = M;
-  a.NB = K / QK;
+  a.M = (int)M;
+  a.NB = (int)(K / QK);
   a.nch = (a.NB + CHUNK_BLOCKS - 1) / CHUNK_BLOCKS;
   a.RW = layout_tile_rows(N);
-  a.tn = (N + PF_TN - 1) / PF_TN;
-  a.tm = (M + PF_TM - 1) / PF_TM;
-  a.tiles = a.tn * a.tm;
+  const int64_t tn = (N + PF_TN - 1) / PF_TN, tm = (M + PF_TM - 1) / PF_TM;
+  if (tn * tm > INT32_MAX) return cudaErrorInvalidValue;
+  a.tm = (int)tm;
+  a.tiles = (int)(tn * tm);
   a.err = err;
   const int64_t grid = a.tiles < dev.sm_count ? a.tiles : dev.sm_count;
   cudaLaunchConfig_t cfg = {};

@@ -79,6 +79,34 @@ def test_prefill_bitwise_equals_oracle_order(q8, N, K, M):
     assert q8.q8_device_error() == 0
 
 
+def test_prefill_subnormal_and_zero_scales(q8):
+    # activation rows scaled down so their block scales (amax / 127) are
+    # binary16 subnormals, zero rows (d = 0), and weight rows likewise: the
+    # scale products must stay exact
+    N, K, M = 256, 1024, 130
+    w = q8_synth.weights(N, K, q8_synth.derive_seed("pf-sub-w"), DEV)
+    x = q8_synth.activations(M, K, q8_synth.derive_seed("pf-sub-x"), DEV)
+    x[0:40] *= 1e-4
+    x[40:50] *= 1e-7
+    x[50] = 0.0
+    w[0:30] *= 1e-3
+    w[31] = 0.0
+    Wb = q8.empty_blocks(N, K)
+    q8.q8_quantize_act(w, Wb)
+    W = q8.empty_packed(N, K)
+    q8.q8_repack_weights(Wb, N, K, W)
+    A = q8.empty_blocks(M, K)
+    q8.q8_quantize_act(x, A)
+    y = _prefill(q8, W, N, K, A, M)
+    torch.cuda.synchronize()
+    An = A.cpu().numpy()
+    d16 = An.reshape(M, K // 32, 34)[:, :, :2].copy().view(np.uint16)
+    assert ((d16 & 0x7C00) == 0).sum() > 1000  # many subnormal (or zero) scales
+    ref = oracle.gemm_prefill_order(Wb.cpu().numpy(), An, K)
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    assert q8.q8_device_error() == 0
+
+
 def test_prefill_rows_do_not_depend_on_the_launch(q8):
     N, K, M = 2048, 2048, 300
     _, _, _, W, A = _case(q8, N, K, M, "inv")
