@@ -61,6 +61,7 @@ CASES = [
     (300, 96, 1),
     (600, 1568, 257),
     (4096, 2048, 300),
+    (256, 65536, 130),  # K = Q8_MAX_PREFILL_K: 128 segments
 ]
 
 
