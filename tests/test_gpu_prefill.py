@@ -62,6 +62,7 @@ CASES = [
     (600, 1568, 257),
     (4096, 2048, 300),
     (256, 65536, 130),  # K = Q8_MAX_PREFILL_K: 128 segments
+    (1001, 416, 33),    # last weight tile of 9 rows: chunk copies with a ragged tail copied by hand
 ]
 
 
