@@ -370,7 +370,8 @@ Q8_API int q8_gemm_noalloc(const void *W, int64_t N, int64_t K, const void *A_bl
  *              (q8_gemm_prefill).
  *   x          [M][K] fp32 activations, 4-byte aligned, quantized first
  *              exactly as q8_quantize_act does (q8_fused_quant_gemm_prefill).
- *   M          activation rows, >= 1.
+ *   M          activation rows, >= 1; ceil(N/128) * ceil(M/128) output
+ *              tiles at most 2^31 - 1 (else Q8_ESHAPE).
  *   y          [M][N] fp32 output, row-major, 4-byte aligned; overwritten.
  *   A_blocks_out  (fused call only, may be NULL) receives the [M][K/32]
  *              blocks of x, 2-byte aligned.

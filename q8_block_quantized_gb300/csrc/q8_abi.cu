@@ -104,6 +104,8 @@ int prefill_gemm(const void* W, int64_t N, int64_t K, const void* A_blocks, cons
   if (W == nullptr || y == nullptr || (A_blocks == nullptr && x == nullptr)) return Q8_EINVAL;
   if ((flags & ~Q8_FLAG_PDL) != 0) return Q8_EINVAL;
   if (N <= 0 || N > INT32_MAX || !k_ok(K) || K > Q8_MAX_PREFILL_K || M < 1) return Q8_ESHAPE;
+  const int64_t T = Q8_PREFILL_TILE_ROWS;
+  if (((N + T - 1) / T) * (((int64_t)M + T - 1) / T) > INT32_MAX) return Q8_ESHAPE;  // output tiles
   if (!aligned(W, 16) || !aligned(y, 4)) return Q8_EALIGN;
   if ((A_blocks != nullptr && !aligned(A_blocks, 2)) || (x != nullptr && !aligned(x, 4)) ||
       (A_out != nullptr && !aligned(A_out, 2)))

@@ -122,6 +122,7 @@ def test_host_argument_checks_reject_before_any_device_work(lib):
     assert pf(fake, 64, 65536 + 32, fake, 1, y, fake, big, 0, None) == -2      # K > Q8_MAX_PREFILL_K
     assert pf(fake, 0, 64, fake, 1, y, fake, big, 0, None) == -2               # N = 0
     assert pf(fake, 64, 64, fake, 0, y, fake, big, 0, None) == -2              # M = 0
+    assert pf(fake, (1 << 31) - 1, 64, fake, (1 << 31) - 1, y, fake, big, 0, None) == -2  # > 2^31 tiles
     assert pf(odd, 64, 64, fake, 1, y, fake, big, 0, None) == -3               # W misaligned
     assert pf(fake, 64, 64, odd, 1, y, fake, big, 0, None) == -3               # A misaligned
     assert pf(fake, 64, 64, fake, 1, y, eight, big, 0, None) == -3             # workspace 8-aligned
