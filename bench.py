@@ -328,6 +328,7 @@ def run_ours(args):
     prod = producers(q8, shape) if (rank == 0 and not args.no_producers) else None
     tc5 = tcgen05_vs_default(q8, st) if (rank == 0 and world == 1 and not args.no_producers) else None
     pre = prefill(q8, st) if (rank == 0 and world == 1 and not args.no_producers) else None
+    cfgs = configs_table(q8, st) if (rank == 0 and world == 1 and not args.no_producers) else None
     peak, peak_kind = _peaks()
     if rank == 0:
         cpu = cpu_baseline(shape, args.M) if (world == 1 and not args.no_cpu) else None
@@ -352,6 +353,7 @@ def run_ours(args):
             "producers": prod,
             "tcgen05_vs_default": tc5,
             "prefill": pre,
+            "configs": cfgs,
             "cpu_baseline": cpu,
             "cpu_baseline_all_cores": cpu_all,
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
@@ -481,6 +483,104 @@ def roofline(st, q8, reps=3):
             "bytes_per_launch_avg": int(nbytes / n), "us_per_launch_avg": round(ms * 1e3 / n, 3),
             "classes": {k: {"launches": nn, "us": round(t * 1e3, 2), "GB/s": round(b / (t * 1e-3) / 1e9, 1)}
                         for t, k, b, nn, _ in rows}}
+
+
+def configs_table(q8, st, rounds=30, reps=20, seed=0):
+    """The workloads of the metric beside the headline step, each as its own
+    CUDA graph on the same weights (the pages' method: configurations
+    interleaved in a seeded random order, the median over rounds):
+      - the full stack at M = 1, 4, 8, 16 (config 4): GB/s and tok/s;
+      - one 2048 x 2048 GEMV at M = 1 (config 1), 40 chained calls per graph,
+        hot (one W, resident in L2) and cold (40 copies of W rotated,
+        179 MB > L2): us per call;
+      - the LM head 128256 x 2048 at M = 1 and 8 (config 3), 4 chained calls
+        per graph: us per call and GB/s.
+    Fused calls (quantization inside the GEMV), PDL chaining as in the step."""
+    import numpy as np
+    import torch
+
+    import q8_synth
+    from q8_block_quantized_gb300.stack import Q8Stack
+
+    dev = torch.device("cuda")
+    cases = {}  # name -> (graph, calls per replay, bytes per call, rows)
+    keep = []
+
+    def capture(fn):
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        return g
+
+    for M in (1, 4, 8, 16):
+        s2 = st if M == st.M else Q8Stack(st.shape, M=M, mode="fused", layers=st.n_layers,
+                                          shared_weights=st.weights)
+        keep.append(s2)
+        cases["stack M=%d" % M] = (s2.capture(), 1, s2.bytes_per_step(), M)
+
+    def gemv_case(W, N, K, M, calls=1, copies=1):
+        # `calls` chained calls per graph, rotating over `copies` copies of W
+        x = q8_synth.activations(M, K, q8_synth.derive_seed("cfg", N, K, M), dev)
+        y = torch.empty(M, N, device=dev)
+        ws = q8.new_workspace(N, K, M, dev)
+        Wc = [W] + [W.clone() for _ in range(copies - 1)]
+        Ws = [Wc[i % copies] for i in range(calls)]
+        keep.extend([x, y, ws, Ws])
+
+        def run():
+            for Wi in Ws:
+                q8.q8_fused_quant_gemm(Wi, N, K, x, M, y, workspace=ws, flags=q8.FLAG_PDL)
+        return capture(run), len(Ws), W.numel() + 4 * M * K + 4 * M * N
+
+    N1, K1 = 2048, 2048
+    W1 = q8.pack_weights_f32(q8_synth.weights(N1, K1, q8_synth.derive_seed("cfg-w1"), dev))
+    g, n, by = gemv_case(W1, N1, K1, 1, calls=40, copies=40)
+    cases["gemv 2048x2048 M=1 cold"] = (g, n, by, 1)
+    g, n, by = gemv_case(W1, N1, K1, 1, calls=40, copies=1)
+    cases["gemv 2048x2048 M=1 hot"] = (g, n, by, 1)
+    head = st.shape.head()
+    Wh = st.weights[(st.n_layers, head.name)]
+    for M in (1, 8):
+        g, n, by = gemv_case(Wh, head.N, head.K, M, calls=4)
+        cases["lm_head M=%d" % M] = (g, n, by, M)
+
+    names = list(cases)
+    samples = {k: [] for k in names}
+    cur = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for k in names:  # warm-up
+        for _ in range(3):
+            cases[k][0].replay()
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(seed)
+    for _ in range(rounds):
+        for i in rng.permutation(len(names)):
+            g, calls = cases[names[i]][0], cases[names[i]][1]
+            a.record(cur)
+            for _ in range(reps):
+                g.replay()
+            b.record(cur)
+            b.synchronize()
+            samples[names[i]].append(a.elapsed_time(b) / (reps * calls))
+    out = {"order": "seeded random permutation per round (numpy PCG64, seed %d)" % seed, "rounds": rounds,
+           "replays_per_visit": reps, "results": []}
+    for k in names:
+        ms = float(np.median(samples[k]))
+        by, M = cases[k][2], cases[k][3]
+        ent = {"case": k, "M": M, "us_median": round(ms * 1e3, 3), "GB/s": round(by / (ms * 1e-3) / 1e9, 1)}
+        if k.startswith("stack"):
+            ent["tok_s"] = round(M / (ms * 1e-3), 1)
+        out["results"].append(ent)
+    del cases, keep
+    torch.cuda.empty_cache()
+    return out
 
 
 def producers(q8, shape, launches=20):
