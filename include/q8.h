@@ -406,7 +406,11 @@ Q8_API int q8_block_dots(const void *W, int64_t N, int64_t K, const void *A_bloc
 
 /* Read and clear the device-side error word of the current device (waits for
  * the device).  *code = 0 when no kernel reported a failed wait; otherwise
- * Q8_ETIMEOUT's magnitude ORed with where it happened.  Returns a status. */
+ * (-Q8_ETIMEOUT) << 8 ORed with where it happened: 1 a GEMV's copy stream,
+ * 2 a GEMV's consumers, 4 a GEMV's drain of copies in flight; 16 the prefill
+ * GEMM's worker warps, 32 its drain, 64 its MMA issuer, 128 its copy issuer.
+ * A kernel whose wait gave up (2 s) stops its work and returns; its outputs
+ * are undefined.  Returns a status. */
 Q8_API int q8_device_error(unsigned *code);
 
 /* Properties the library uses: SM count and compute capability of the
