@@ -17,7 +17,7 @@
  *            tile figure (eight 64-byte groups of four coordinates for 16
  *            rows, then 16 fp16 scales; one record = 544 bytes = 16 blocks).
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - scale rule: d = amax / 127 in fp32, q = roundf(x * (1/d)) (ties away
  *     from zero), 1/d taken from the fp32 d (not from the stored fp16), d
  *     stored as IEEE binary16 rounded to nearest-even, subnormals kept.
@@ -306,7 +306,7 @@ void q8o_ember_tile_unpack(const uint8_t *tile, uint8_t *dst)
  * Fused producers [Ferro, "How the iGPU path is fast", item 3: the residual
  * add, the norm and the int8 quantization in one pass; SwiGLU emits the next
  * GEMM's int8 input].  The pages name these fusions, not their arithmetic.
- * Readings (each listed in the design doc), all in single precision, every
+ * Readings, all in single precision, every
  * operation one IEEE rounding (sqrt and division correctly rounded):
  *   - RMSNorm as in the Llama family: h = x + delta (or x); s = sum_k h_k^2
  *     summed as the pairwise tree over k padded with zeros to a power of
