@@ -205,7 +205,8 @@ def test_gemm_exact_integer_sum_with_unit_scales(q8):
 # batch invariance and order invariance (bitwise)
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("N,K", [(2048, 2048), (3072, 2048), (2048, 8192), (700, 3072)])
+@pytest.mark.parametrize("N,K", [(2048, 2048), (3072, 2048), (2048, 8192), (700, 3072),
+                                 (5120, 3072), (16384, 3072), (3072, 8192)])  # the 3B shapes too
 def test_batch_invariance_shuffled_rows(q8, N, K):
     Mmax = 64
     w, x = _case(N, K, Mmax, 3)
