@@ -234,8 +234,9 @@ Q8_API int q8_repack_weights(const void *src_blocks, int64_t N, int64_t K, void 
  *             of 16 rows, each streaming W again, with the same per-row
  *             arithmetic, so a prefill row is bitwise the row decoded alone
  *             (Ferro README, "Exactness contract": a row's result does not
- *             depend on the other rows of the launch).  No tile GEMM with
- *             activation reuse is provided.
+ *             depend on the other rows of the launch).  For many rows,
+ *             q8_gemm_prefill reuses each weight tile across 128 rows (its
+ *             own per-row order, not bitwise the decoded row).
  *   y         [M][N] fp32 output, row-major, 4-byte aligned; overwritten.
  *   workspace q8_workspace_bytes(N, K, M) bytes (may be NULL when that is 0),
  *             16-byte aligned.  Its first 16384 bytes hold per-tile tickets
