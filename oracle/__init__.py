@@ -16,6 +16,8 @@ arrays to it.  Each C function cites the page passage it follows:
   per 16 blocks).
 * "Ferro" README, "How the iGPU path is fast", item 3: fused producers (the
   residual add and the norm, SwiGLU) that emit the next GEMM's int8 input.
+* "Ferro" README, "Exactness, scheduling and operations (LM serving)", item
+  "KV cache": K/V rows as int8 with one fp32 scale per 32 values.
 
 Every function is pinned by ``tests/test_oracle_pins.py``; none is
 "parity unpinned".
@@ -84,7 +86,10 @@ def _load():
                                                       f32p, u8p]
         lib.q8o_swiglu_quantize.argtypes = [f32p, i64, i64, u8p]
         lib.q8o_ember_tile_unpack.argtypes = [u8p, u8p]
-        for name in ("q8o_qk", "q8o_block_bytes", "q8o_ember_tile_bytes"):
+        i8p = ctypes.POINTER(ctypes.c_int8)
+        lib.q8o_kv_quantize.argtypes = [f32p, i64, i64, i32p, i64, i8p, f32p]
+        lib.q8o_kv_dequantize.argtypes = [i8p, f32p, i64, i64, i32p, i64, f32p]
+        for name in ("q8o_qk", "q8o_block_bytes", "q8o_ember_tile_bytes", "q8o_kv_block_bytes"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -106,7 +111,8 @@ def _u8(a) -> np.ndarray:
 def constants() -> dict:
     lib = _load()
     return {"qk": lib.q8o_qk(), "block_bytes": lib.q8o_block_bytes(),
-            "ember_tile_bytes": lib.q8o_ember_tile_bytes()}
+            "ember_tile_bytes": lib.q8o_ember_tile_bytes(),
+            "kv_block_bytes": lib.q8o_kv_block_bytes()}
 
 
 def f32_to_f16_bits(x) -> np.ndarray:
@@ -273,6 +279,53 @@ def ember_tile_unpack(tile) -> np.ndarray:
     src = _u8(tile).reshape(EMBER_TILE_BYTES)
     out = np.zeros((16, BLOCK_BYTES), dtype=np.uint8)
     lib.q8o_ember_tile_unpack(_ptr(src, ctypes.c_uint8), _ptr(out, ctypes.c_uint8))
+    return out
+
+
+def kv_quantize(x, capacity: int, slots=None, cache=None):
+    """K/V rows x [rows][D] fp32 written into an int8 cache of `capacity`
+    slots: returns (q int8 [capacity][D], d fp32 [capacity][D/32]).  Row r
+    goes to slot slots[r] (slot r when slots is None); a slot outside
+    [0, capacity) is skipped.  `cache` = (q, d) arrays updated in place
+    (new zeroed arrays when None)."""
+    lib = _load()
+    x = _f32(x)
+    if x.ndim == 1:
+        x = x.reshape(1, -1)
+    rows, D = x.shape
+    if D % QK:
+        raise ValueError("D must be a multiple of 32")
+    if cache is None:
+        q = np.zeros((capacity, D), dtype=np.int8)
+        d = np.zeros((capacity, D // QK), dtype=np.float32)
+    else:
+        q, d = cache
+        assert q.dtype == np.int8 and d.dtype == np.float32 and q.flags["C_CONTIGUOUS"] and d.flags["C_CONTIGUOUS"]
+        assert q.shape == (capacity, D) and d.shape == (capacity, D // QK)
+    sl = None if slots is None else np.ascontiguousarray(slots, dtype=np.int32)
+    if sl is not None and sl.size != rows:
+        raise ValueError("one slot per row")
+    lib.q8o_kv_quantize(_ptr(x, ctypes.c_float), rows, D,
+                        None if sl is None else _ptr(sl, ctypes.c_int32), capacity,
+                        _ptr(q, ctypes.c_int8), _ptr(d, ctypes.c_float))
+    return q, d
+
+
+def kv_dequantize(q, d, slots=None, rows=None) -> np.ndarray:
+    """Read rows back from an int8 cache (q [capacity][D], d [capacity][D/32]):
+    out[r] = q[slot] * d[slot] per 32-value block, fp32; rows whose slot is
+    outside the cache stay zero."""
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    d = _f32(d)
+    capacity, D = q.shape
+    sl = None if slots is None else np.ascontiguousarray(slots, dtype=np.int32)
+    n = capacity if sl is None else sl.size
+    if rows is not None:
+        n = rows
+    out = np.zeros((n, D), dtype=np.float32)
+    lib.q8o_kv_dequantize(_ptr(q, ctypes.c_int8), _ptr(d, ctypes.c_float), capacity, D,
+                          None if sl is None else _ptr(sl, ctypes.c_int32), n, _ptr(out, ctypes.c_float))
     return out
 
 

@@ -438,3 +438,65 @@ void q8o_swiglu_quantize(const float *gu, int64_t M, int64_t F, uint8_t *out)
             q8o_quantize_block(h, out + (m * nb + b) * BLOCK_BYTES);
         }
 }
+
+/* ---------------------------------------------------------------------------
+ * Int8 KV cache codec ("Ferro" README, "Exactness, scheduling and operations
+ * (LM serving)", item "KV cache": K/V rows stored as int8 with one fp32
+ * scale per 32 values, llama.cpp's q8_0 scheme for the cache, written by the
+ * cache-write kernel and dequantized where attention reads it).
+ *
+ * Readings: the 32-value codebook is the one of q8o_quantize_block (d =
+ * amax / 127, q = roundf(x * (1/d)), 1/d from the fp32 d); the stored scale
+ * is that fp32 d itself, not rounded to binary16; a cache entry is D int8
+ * quants in the quant plane [slot][D] plus D/32 fp32 scales in the scale
+ * plane [slot][D/32] (36 bytes per 32 values); row r of the input goes to
+ * cache slot slots[r] (slot r when slots is NULL); a slot outside [0,
+ * capacity) is not written.  Dequantization is one single-precision
+ * multiply per value: x' = (float)q * d.
+ * ------------------------------------------------------------------------- */
+#define KV_BLOCK_BYTES 36   /* 32 int8 + one fp32 scale */
+
+int q8o_kv_block_bytes(void) { return KV_BLOCK_BYTES; }
+
+void q8o_kv_quantize(const float *x, int64_t rows, int64_t D, const int32_t *slots,
+                     int64_t capacity, int8_t *cache_q, float *cache_d)
+{
+    int64_t nb = D / QK;
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t s = slots != NULL ? (int64_t)slots[r] : r;
+        if (s < 0 || s >= capacity)
+            continue;
+        for (int64_t b = 0; b < nb; ++b) {
+            const float *v = x + r * D + b * QK;
+            float amax = 0.0f;
+            for (int i = 0; i < QK; ++i) {
+                float a = fabsf(v[i]);
+                if (a > amax)
+                    amax = a;
+            }
+            float d = amax / 127.0f;
+            float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+            cache_d[s * nb + b] = d;
+            for (int i = 0; i < QK; ++i) {
+                float t = roundf(v[i] * id);
+                if (t > 127.0f) t = 127.0f;
+                if (t < -127.0f) t = -127.0f;
+                if (t != t) t = 0.0f;       /* 0 * inf: a zero value stays zero */
+                cache_q[s * D + b * QK + i] = (int8_t)(int)t;
+            }
+        }
+    }
+}
+
+void q8o_kv_dequantize(const int8_t *cache_q, const float *cache_d, int64_t capacity, int64_t D,
+                       const int32_t *slots, int64_t rows, float *out)
+{
+    int64_t nb = D / QK;
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t s = slots != NULL ? (int64_t)slots[r] : r;
+        if (s < 0 || s >= capacity)
+            continue;
+        for (int64_t k = 0; k < D; ++k)
+            out[r * D + k] = (float)cache_q[s * D + k] * cache_d[s * nb + k / QK];
+    }
+}
