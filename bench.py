@@ -329,6 +329,7 @@ def run_ours(args):
     tc5 = tcgen05_vs_default(q8, st) if (rank == 0 and world == 1 and not args.no_producers) else None
     pre = prefill(q8, st) if (rank == 0 and world == 1 and not args.no_producers) else None
     cfgs = configs_table(q8, st) if (rank == 0 and world == 1 and not args.no_producers) else None
+    kv = kv_codec(q8, shape) if (rank == 0 and world == 1 and not args.no_producers) else None
     peak, peak_kind = _peaks()
     if rank == 0:
         cpu = cpu_baseline(shape, args.M) if (world == 1 and not args.no_cpu) else None
@@ -354,6 +355,7 @@ def run_ours(args):
             "tcgen05_vs_default": tc5,
             "prefill": pre,
             "configs": cfgs,
+            "kv_codec": kv,
             "cpu_baseline": cpu,
             "cpu_baseline_all_cores": cpu_all,
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
@@ -687,6 +689,67 @@ def producers(q8, shape, launches=20):
         out["swiglu_epilogue"] = {"M": 1, "F": F, "K": K, "us_gemv_with_epilogue": round(us_epi, 3),
                                   "us_gemv_then_swiglu": round(us_two, 3)}
         del Wgu
+    torch.cuda.empty_cache()
+    return out
+
+
+def kv_codec(q8, shape, launches=20):
+    """The int8 KV cache codec (cache write with a slot map, and the read
+    back), at the model's K/V row width D = kv_heads * head_dim: a bulk case
+    of 65536 rows (a 4096-token prefill of all 16 layers' K and V: 128 MB of
+    fp32 rows, more than L2) with plain launches, and one decode token's
+    rows of all layers (2 * layers rows) chained with PDL in a graph.
+    Algorithmic bytes: fp32 rows + int8 quants + fp32 scales + int32 slots."""
+    import torch
+
+    import q8_synth
+    peak, kind = _peaks()
+    D = shape.kv_dim
+    dev = "cuda"
+    out = {"D": D}
+    for label, rows, cap in (("bulk", 65536, 65536), ("decode", 2 * shape.layers, 4 * 4096 * 2 * shape.layers)):
+        x = q8_synth.normal_torch((rows, D), 1.0, q8_synth.derive_seed("kvb", rows), dev)
+        cq = torch.zeros((cap, D), dtype=torch.int8, device=dev)
+        cd = torch.zeros((cap, D // 32), dtype=torch.float32, device=dev)
+        slots = torch.randperm(cap, device=dev)[:rows].to(torch.int32)
+        back = torch.empty_like(x)
+
+        def timed(fn, pdl):
+            fn(0)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(launches):
+                    fn(q8.FLAG_PDL if pdl else 0)
+            g.replay()
+            torch.cuda.synchronize()
+            cur = torch.cuda.current_stream()
+            best = None
+            for _ in range(3):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(cur)
+                g.replay()
+                b.record(cur)
+                b.synchronize()
+                best = a.elapsed_time(b) if best is None else min(best, a.elapsed_time(b))
+            del g
+            return best * 1e3 / launches
+
+        nbytes = rows * D * 4 + rows * D + rows * (D // 32) * 4 + rows * 4
+        us_w = timed(lambda f: q8.q8_kv_quantize(x, cq, cd, slots=slots, flags=f), label == "decode")
+        us_r = timed(lambda f: q8.q8_kv_dequantize(cq, cd, back, slots=slots, flags=f), label == "decode")
+        ent = {"rows": rows, "capacity": cap, "bytes": nbytes,
+               "write_us": round(us_w, 3), "read_us": round(us_r, 3),
+               "write_GB/s": round(nbytes / (us_w * 1e-6) / 1e9, 1),
+               "read_GB/s": round(nbytes / (us_r * 1e-6) / 1e9, 1)}
+        if label == "bulk":
+            ent.update({"peak": peak, "peak_kind": kind,
+                        "write_frac": round(nbytes / (us_w * 1e-6) / 1e9 / peak, 4),
+                        "read_frac": round(nbytes / (us_r * 1e-6) / 1e9 / peak, 4)})
+        out[label] = ent
+        del x, cq, cd, slots, back
     torch.cuda.empty_cache()
     return out
 

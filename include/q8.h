@@ -393,6 +393,51 @@ Q8_API int q8_fused_quant_gemm_prefill(const void *W, int64_t N, int64_t K, cons
                                        float *y, void *A_blocks_out, void *workspace,
                                        size_t workspace_bytes, unsigned flags, void *stream);
 
+/*
+ * q8_kv_quantize / q8_kv_dequantize -- the int8 KV cache codec ("Ferro"
+ * README, "Exactness, scheduling and operations (LM serving)", item "KV
+ * cache": K/V rows stored as int8 with one fp32 scale per 32 values, the
+ * q8_0 scheme of llama.cpp applied to the cache; written by the cache-write
+ * step, dequantized where attention reads the cache).
+ *
+ * Codebook: for each 32-value block, d = amax / 127 in fp32 and q_i =
+ * roundf(x_i * (1/d)) with 1/d from the fp32 d -- the quants are exactly
+ * those q8_quantize_act gives the same block -- but the scale is kept as the
+ * fp32 d itself (not rounded to binary16).  Dequantization: x'_i = q_i * d,
+ * one single-precision multiply (round to nearest even).
+ *
+ * Cache layout (caller-owned device memory, q8_kv_cache_bytes(capacity, D)
+ * bytes in two planes): quants int8 [capacity][D], row s of slot s; scales
+ * fp32 [capacity][D/32], scale b of slot s covers quants 32b..32b+31 of
+ * that slot.  36 bytes per 32 values.
+ *
+ *   x          [rows][D] fp32 K or V rows (e.g. one token's row of all KV
+ *              heads of a layer), 16-byte aligned.
+ *   rows       1 <= rows <= 2^31 - 1.
+ *   D          positive multiple of 32, at most Q8_MAX_KV_D.
+ *   slots      device int32 [rows], 4-byte aligned: the cache slot of each
+ *              row (a paged cache's slot map), or NULL for slot = row.  A slot
+ *              outside [0, capacity) is skipped: nothing is written for that
+ *              row (q8_kv_dequantize writes zeros for it), and
+ *              q8_device_error then reports (-Q8_ESHAPE) << 8 | 8.
+ *   capacity   slots in the cache, 1 <= capacity <= 2^31 - 1.
+ *   cache_q, cache_d  the planes, 4-byte aligned.  Rows given the same slot
+ *              in one call race (any one of them may win, block by block).
+ *   out        [rows][D] fp32 (q8_kv_dequantize), 16-byte aligned: row r is
+ *              the dequantized slot slots[r].
+ *   flags      0 or Q8_FLAG_PDL.
+ * The written quants and scales, and the dequantized values, are bit-exact
+ * with the rule above for finite inputs.
+ */
+#define Q8_MAX_KV_D (1 << 24)
+Q8_API size_t q8_kv_cache_bytes(int64_t capacity, int64_t D);
+Q8_API int q8_kv_quantize(const float *x, int64_t rows, int64_t D, const int32_t *slots,
+                          int64_t capacity, int8_t *cache_q, float *cache_d, unsigned flags,
+                          void *stream);
+Q8_API int q8_kv_dequantize(const int8_t *cache_q, const float *cache_d, int64_t capacity,
+                            int64_t D, const int32_t *slots, int64_t rows, float *out,
+                            unsigned flags, void *stream);
+
 /* ---- test hooks (not on the hot path) ----------------------------------- */
 
 /* Inverse of q8_repack_weights: packed (16-byte aligned) -> [N][K/32] blocks
@@ -406,12 +451,15 @@ Q8_API int q8_block_dots(const void *W, int64_t N, int64_t K, const void *A_bloc
                   int M, int32_t *isum, void *stream);
 
 /* Read and clear the device-side error word of the current device (waits for
- * the device).  *code = 0 when no kernel reported a failed wait; otherwise
- * (-Q8_ETIMEOUT) << 8 ORed with where it happened: 1 a GEMV's copy stream,
- * 2 a GEMV's consumers, 4 a GEMV's drain of copies in flight; 16 the prefill
- * GEMM's worker warps, 32 its drain, 64 its MMA issuer, 128 its copy issuer.
- * A kernel whose wait gave up (2 s) stops its work and returns; its outputs
- * are undefined.  Returns a status. */
+ * the device).  *code = 0 when no kernel reported a failure; otherwise a
+ * status byte shifted left by 8 ORed with what happened where: 1 a GEMV's
+ * copy stream, 2 a GEMV's consumers, 4 a GEMV's drain of copies in flight;
+ * 16 the prefill GEMM's worker warps, 32 its drain, 64 its MMA issuer, 128
+ * its copy issuer -- each a bounded device wait (2 s) that gave up, status
+ * -Q8_ETIMEOUT; 8 a KV codec row whose slot lay outside the cache (that row
+ * skipped), status -Q8_ESHAPE when it is the only bit.  A kernel whose wait
+ * gave up stops its work and returns; its outputs are undefined.  Returns a
+ * status. */
 Q8_API int q8_device_error(unsigned *code);
 
 /* Properties the library uses: SM count and compute capability of the

@@ -30,6 +30,8 @@ FLAG_TCGEN05 = 2
 PREFILL_TILE_ROWS = 128
 PREFILL_SEGMENT = 16
 MAX_PREFILL_K = 65536
+MAX_KV_D = 1 << 24
+KV_BLOCK_BYTES = 36
 
 STATUS = {0: "Q8_OK", -1: "Q8_EINVAL", -2: "Q8_ESHAPE", -3: "Q8_EALIGN", -4: "Q8_EDEVICE",
           -5: "Q8_ECUDA", -6: "Q8_EWORKSPACE", -7: "Q8_ETIMEOUT", -8: "Q8_ESCRATCH"}
@@ -56,6 +58,9 @@ SIGNATURES = {
     "q8_prefill_workspace_bytes": (_sz, [_i64, _int]),
     "q8_gemm_prefill": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _vp, _sz, _u, _vp]),
     "q8_fused_quant_gemm_prefill": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _vp, _vp, _sz, _u, _vp]),
+    "q8_kv_cache_bytes": (_sz, [_i64, _i64]),
+    "q8_kv_quantize": (_int, [_vp, _i64, _i64, _vp, _i64, _vp, _vp, _u, _vp]),
+    "q8_kv_dequantize": (_int, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _u, _vp]),
     "q8_unpack_weights": (_int, [_vp, _i64, _i64, _vp, _vp]),
     "q8_block_dots": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _vp]),
     "q8_device_error": (_int, [ctypes.POINTER(ctypes.c_uint)]),
@@ -253,6 +258,42 @@ def interleave_gate_up(gate: torch.Tensor, up: torch.Tensor) -> torch.Tensor:
     if G < 32 or F % G:
         raise ValueError("F = %d has no SwiGLU epilogue layout (group %d)" % (F, G))
     return torch.stack([gate.reshape(F // G, G, K), up.reshape(F // G, G, K)], dim=1).reshape(2 * F, K)
+
+
+# ---- int8 KV cache codec ---------------------------------------------------------
+
+def q8_kv_cache_bytes(capacity: int, D: int) -> int:
+    return int(lib().q8_kv_cache_bytes(capacity, D))
+
+
+def q8_kv_quantize(x: torch.Tensor, cache_q: torch.Tensor, cache_d: torch.Tensor,
+                   slots: torch.Tensor | None = None, flags: int = 0, stream=None):
+    """Write K/V rows x [rows][D] into cache slots (slots: int32 [rows], or
+    None for slot = row) as int8 quants cache_q [capacity][D] and fp32 scales
+    cache_d [capacity][D/32] (see q8.h)."""
+    rows, D = x.shape
+    capacity = cache_q.shape[0]
+    if cache_q.shape != (capacity, D) or cache_d.shape != (capacity, D // QK):
+        raise ValueError("cache planes must be [capacity][D] int8 and [capacity][D/32] fp32")
+    _check("q8_kv_quantize", lib().q8_kv_quantize(
+        _dev(x, torch.float32, "x"), rows, D, _opt(slots, torch.int32, "slots"), capacity,
+        _dev(cache_q, torch.int8, "cache_q"), _dev(cache_d, torch.float32, "cache_d"),
+        flags, _stream(stream)))
+    return cache_q, cache_d
+
+
+def q8_kv_dequantize(cache_q: torch.Tensor, cache_d: torch.Tensor, out: torch.Tensor,
+                     slots: torch.Tensor | None = None, flags: int = 0, stream=None):
+    """out [rows][D] fp32 = the dequantized cache slots slots[r] (slot r when
+    slots is None)."""
+    capacity, D = cache_q.shape
+    rows = out.shape[0]
+    if cache_d.shape != (capacity, D // QK) or out.shape != (rows, D):
+        raise ValueError("shapes: cache_q [capacity][D], cache_d [capacity][D/32], out [rows][D]")
+    _check("q8_kv_dequantize", lib().q8_kv_dequantize(
+        _dev(cache_q, torch.int8, "cache_q"), _dev(cache_d, torch.float32, "cache_d"), capacity, D,
+        _opt(slots, torch.int32, "slots"), rows, _dev(out, torch.float32, "out"), flags, _stream(stream)))
+    return out
 
 
 # ---- test hooks ----------------------------------------------------------------

@@ -20,7 +20,7 @@ LIB = os.path.join(HERE, "libq8.so")
 
 SOURCES = ["q8_abi.cu", "q8_aux.cu", "q8_gemv.cu", "q8_gemv_r16.cu", "q8_gemv_r32.cu",
            "q8_gemv_r64.cu", "q8_gemv_r128.cu", "q8_noalloc.cu", "q8_producers.cu",
-           "q8_prefill.cu"]
+           "q8_prefill.cu", "q8_kv.cu"]
 HEADERS = ["q8_device.cuh", "q8_internal.h", "q8_gemv_impl.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

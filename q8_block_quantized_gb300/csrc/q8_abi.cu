@@ -304,6 +304,39 @@ int q8_fused_quant_gemm_swiglu(const void* W, int64_t F, int64_t K, const float*
 }
 
 
+size_t q8_kv_cache_bytes(int64_t capacity, int64_t D) {
+  if (capacity <= 0 || capacity > INT32_MAX || !k_ok(D) || D > Q8_MAX_KV_D) return 0;
+  return (size_t)capacity * (size_t)(D / QK) * (QK + 4);
+}
+
+int q8_kv_quantize(const float* x, int64_t rows, int64_t D, const int32_t* slots, int64_t capacity,
+                   int8_t* cache_q, float* cache_d, unsigned flags, void* stream) {
+  if (x == nullptr || cache_q == nullptr || cache_d == nullptr || (flags & ~Q8_FLAG_PDL) != 0) return Q8_EINVAL;
+  if (rows <= 0 || rows > INT32_MAX || capacity <= 0 || capacity > INT32_MAX || !k_ok(D) || D > Q8_MAX_KV_D)
+    return Q8_ESHAPE;
+  if (!aligned(x, 16) || !aligned(cache_q, 4) || !aligned(cache_d, 4) || (slots != nullptr && !aligned(slots, 4)))
+    return Q8_EALIGN;
+  DeviceInfo d;
+  int st = device_ok(&d);
+  if (st != Q8_OK) return st;
+  return cuda_status(launch_kv_quantize(x, rows, D, slots, capacity, cache_q, cache_d, d.sm_count,
+                                        (flags & Q8_FLAG_PDL) != 0, static_cast<cudaStream_t>(stream)));
+}
+
+int q8_kv_dequantize(const int8_t* cache_q, const float* cache_d, int64_t capacity, int64_t D, const int32_t* slots,
+                     int64_t rows, float* out, unsigned flags, void* stream) {
+  if (cache_q == nullptr || cache_d == nullptr || out == nullptr || (flags & ~Q8_FLAG_PDL) != 0) return Q8_EINVAL;
+  if (rows <= 0 || rows > INT32_MAX || capacity <= 0 || capacity > INT32_MAX || !k_ok(D) || D > Q8_MAX_KV_D)
+    return Q8_ESHAPE;
+  if (!aligned(out, 16) || !aligned(cache_q, 4) || !aligned(cache_d, 4) || (slots != nullptr && !aligned(slots, 4)))
+    return Q8_EALIGN;
+  DeviceInfo d;
+  int st = device_ok(&d);
+  if (st != Q8_OK) return st;
+  return cuda_status(launch_kv_dequantize(cache_q, cache_d, capacity, D, slots, rows, out, d.sm_count,
+                                          (flags & Q8_FLAG_PDL) != 0, static_cast<cudaStream_t>(stream)));
+}
+
 int q8_block_dots(const void* W, int64_t N, int64_t K, const void* A_blocks, int M, int32_t* isum,
                   void* stream) {
   if (W == nullptr || A_blocks == nullptr || isum == nullptr) return Q8_EINVAL;
@@ -325,7 +358,9 @@ int q8_device_error(unsigned* code) {
   if (cudaDeviceSynchronize() != cudaSuccess) return Q8_ECUDA;
   unsigned v = 0;
   if (read_and_clear_gemv_error(&v) != cudaSuccess) return Q8_ECUDA;
-  *code = v ? ((unsigned)(-Q8_ETIMEOUT) << 8) | v : 0u;
+  // a failed wait outranks a skipped KV row in the status byte; the bits say which
+  const int status = (v & ~ERR_KV_SLOT) != 0 ? Q8_ETIMEOUT : Q8_ESHAPE;
+  *code = v ? ((unsigned)(-status) << 8) | v : 0u;
   return Q8_OK;
 }
 

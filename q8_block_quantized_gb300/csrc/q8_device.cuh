@@ -161,8 +161,10 @@ __device__ __forceinline__ uint32_t pack4_s8(int a, int b, int c, int d) {
 // w[q]; every lane of the group gets the stored scale in d[q].  Each
 // shuffle level is taken for all B blocks together so their dependency
 // chains overlap.  All 32 lanes of the warp must call it (full-mask
-// shuffles; a lane with nothing to quantize passes zeros).
-template <int B>
+// shuffles; a lane with nothing to quantize passes zeros).  With
+// STORED16 = false, d[q] is the fp32 scale amax / 127 itself (the int8 KV
+// cache keeps it unrounded); the quants are the same either way.
+template <int B, bool STORED16 = true>
 __device__ __forceinline__ void quantize_group8(const float4 (&v)[B], uint32_t (&w)[B], float (&d)[B]) {
   float am[B];
 #pragma unroll
@@ -180,7 +182,7 @@ __device__ __forceinline__ void quantize_group8(const float4 (&v)[B], uint32_t (
   for (int q = 0; q < B; ++q) {
     const float dq = div127_rn(am[q]);
     const float id = rcp_rn(dq);
-    d[q] = __half2float(__float2half_rn(dq));
+    d[q] = STORED16 ? __half2float(__float2half_rn(dq)) : dq;
     w[q] = pack4_s8(q8_of(__fmul_rn(v[q].x, id)), q8_of(__fmul_rn(v[q].y, id)),
                     q8_of(__fmul_rn(v[q].z, id)), q8_of(__fmul_rn(v[q].w, id)));
   }

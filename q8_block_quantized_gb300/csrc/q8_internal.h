@@ -62,6 +62,16 @@ cudaError_t launch_pack_act(const uint8_t* src, int64_t M, int64_t K, uint8_t* d
 cudaError_t launch_prefill(const DeviceInfo& dev, const uint8_t* W, int64_t N, int64_t K, const uint8_t* A_packed,
                            int64_t M, float* y, bool pdl, cudaStream_t s);
 
+// Int8 KV cache codec (q8_kv.cu).  A row whose slot lies outside [0,
+// capacity) is skipped (the dequantized row is written as zeros) and sets
+// ERR_KV_SLOT in the device error word.
+constexpr unsigned ERR_KV_SLOT = 8u;
+cudaError_t launch_kv_quantize(const float* x, int64_t rows, int64_t D, const int32_t* slots, int64_t capacity,
+                               int8_t* cq, float* cd, int sm_count, bool pdl, cudaStream_t s);
+cudaError_t launch_kv_dequantize(const int8_t* cq, const float* cd, int64_t capacity, int64_t D,
+                                 const int32_t* slots, int64_t rows, float* out, int sm_count, bool pdl,
+                                 cudaStream_t s);
+
 // Fused producers (q8_producers.cu).
 cudaError_t launch_rmsnorm_quantize(const float* x, const float* delta, const float* gamma, float eps,
                                     int64_t M, int64_t K, float* h_out, uint8_t* out, bool pdl,

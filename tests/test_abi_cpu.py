@@ -142,6 +142,25 @@ def test_host_argument_checks_reject_before_any_device_work(lib):
     assert s(fake, 0, 64, fake, 0, None) == -2
     assert s(eight, 1, 64, fake, 0, None) == -3
     assert s(fake, 1, 64, odd, 0, None) == -3
+    kq = lib.q8_kv_quantize
+    assert kq(None, 1, 64, None, 4, fake, fake, 0, None) == -1                  # null x
+    assert kq(fake, 1, 64, None, 4, None, fake, 0, None) == -1                  # null quant plane
+    assert kq(fake, 1, 64, None, 4, fake, None, 0, None) == -1                  # null scale plane
+    assert kq(fake, 1, 64, None, 4, fake, fake, 2, None) == -1                  # unknown flag
+    assert kq(fake, 1, 48, None, 4, fake, fake, 0, None) == -2                  # D % 32
+    assert kq(fake, 0, 64, None, 4, fake, fake, 0, None) == -2                  # rows = 0
+    assert kq(fake, 1, 64, None, 0, fake, fake, 0, None) == -2                  # capacity = 0
+    assert kq(fake, 1, (1 << 24) + 32, None, 4, fake, fake, 0, None) == -2      # D > Q8_MAX_KV_D
+    assert kq(eight, 1, 64, None, 4, fake, fake, 0, None) == -3                 # x 8-aligned only
+    assert kq(fake, 1, 64, odd, 4, fake, fake, 0, None) == -3                   # slots odd
+    assert kq(fake, 1, 64, None, 4, ctypes.c_void_p(0x10002), fake, 0, None) == -3
+    kd = lib.q8_kv_dequantize
+    assert kd(fake, fake, 4, 64, None, 1, None, 0, None) == -1                  # null out
+    assert kd(fake, fake, 4, 64, None, 1, eight, 0, None) == -3                 # out 8-aligned only
+    assert kd(fake, fake, 4, 40, None, 1, fake, 0, None) == -2
+    assert kd(fake, odd, 4, 64, None, 1, fake, 0, None) == -3                   # scales odd
+    assert lib.q8_kv_cache_bytes(4096, 512) == 4096 * 16 * 36
+    assert lib.q8_kv_cache_bytes(0, 512) == 0 and lib.q8_kv_cache_bytes(4, 40) == 0
 
 
 def test_no_device_means_an_error_not_a_fallback(lib):
