@@ -20,8 +20,9 @@ LIB = os.path.join(HERE, "libq8.so")
 
 SOURCES = ["q8_abi.cu", "q8_aux.cu", "q8_gemv.cu", "q8_gemv_r16.cu", "q8_gemv_r32.cu",
            "q8_gemv_r64.cu", "q8_gemv_r128.cu", "q8_noalloc.cu", "q8_producers.cu",
-           "q8_prefill.cu", "q8_kv.cu"]
-HEADERS = ["q8_device.cuh", "q8_internal.h", "q8_gemv_impl.cuh"]
+           "q8_prefill.cu", "q8_kv.cu", "q8_gemv_vt.cu", "q8_gemv_vt_m4.cu", "q8_gemv_vt_m8.cu",
+           "q8_gemv_vt_m16.cu", "q8_gemv_vt_m32.cu"]
+HEADERS = ["q8_device.cuh", "q8_internal.h", "q8_gemv_impl.cuh", "q8_gemv_vt.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

@@ -86,7 +86,7 @@ int swiglu_gemm(const void* W, int64_t F, int64_t K, const void* A_blocks, const
   int st = device_ok(&d);
   if (st != Q8_OK) return st;
   GemvPlan p;
-  if (!plan_gemv(d, 2 * F, K, M, x != nullptr, false, &p) || p.S != 1) return Q8_ESHAPE;
+  if (!plan_gemv(d, 2 * F, K, M, x != nullptr, false, &p, false) || p.S != 1) return Q8_ESHAPE;
   (void)workspace;
   (void)workspace_bytes;  // no split along K: no workspace is used
   return cuda_status(launch_gemv(p, static_cast<const uint8_t*>(W), static_cast<const uint8_t*>(A_blocks), x,

@@ -94,7 +94,17 @@ int budget_of(int R, int MT, bool u5) {
 
 cudaError_t device_error_word(int dev, unsigned** out) { return error_word(dev, out); }
 
-bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, bool tcgen05, GemvPlan* out) {
+// Row counts from which a launch takes the virtual-tile kernel (4 to 32 rows
+// per pass); fewer rows take the one-tile-per-unit kernel below.
+#ifndef Q8_VT_MIN_M
+#define Q8_VT_MIN_M 9
+#endif
+
+bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, bool tcgen05, GemvPlan* out,
+               bool allow_vt) {
+  // (shapes the virtual-tile plan cannot take, e.g. K beyond what its splits
+  // cover, fall back to the kernel below: the bits are the same)
+  if (allow_vt && !tcgen05 && M >= Q8_VT_MIN_M && plan_vt(dev, N, K, M, fused, out)) return true;
   GemvPlan q;
   q.N = N;
   q.K = K;
@@ -172,6 +182,10 @@ bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, b
 cudaError_t launch_gemv(const GemvPlan& p, const uint8_t* W, const uint8_t* A, const float* x,
                         uint8_t* A_out, float* y, void* workspace, bool pdl, cudaStream_t s,
                         uint8_t* h_blocks) {
+  if (p.vt) {
+    if (h_blocks != nullptr) return cudaErrorInvalidValue;  // the SwiGLU epilogue is planned without vt
+    return launch_vt(p, W, A, x, A_out, y, workspace, pdl, s);
+  }
   const bool fused = (x != nullptr);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

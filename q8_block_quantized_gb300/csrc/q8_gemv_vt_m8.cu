@@ -1,0 +1,9 @@
+// q8_gemv_vt_m8.cu -- instantiations of the virtual-tile GEMV for passes of
+// up to 8 activation rows.
+#include "q8_gemv_vt.cuh"
+
+namespace q8 {
+namespace vt {
+Q8_VT_INSTANTIATE(8)
+}  // namespace vt
+}  // namespace q8

@@ -26,6 +26,11 @@ struct GemvPlan {
   bool u5 = false;   // block dots on the tcgen05 tensor cores (128-row tiles, 16 rows per pass)
   size_t smem = 0;   // dynamic shared memory per CTA
   size_t ws_bytes = 0;
+  // 4-32 rows per pass: the virtual-tile kernel (q8_gemv_vt.cuh): units of
+  // TV virtual tiles of 128 rows x RU chunks, UB staged blocks per unit,
+  // partials [S][rows][Np] when split along K
+  bool vt = false;
+  int TV = 0, UB = 0, Np = 0;
 };
 
 struct DeviceInfo {
@@ -35,7 +40,13 @@ struct DeviceInfo {
 };
 
 cudaError_t current_device_info(DeviceInfo* out);
-bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, bool tcgen05, GemvPlan* p);
+// allow_vt = false keeps every row count on the one-tile-per-unit kernel
+// (the SwiGLU epilogue exists only there).
+bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, bool tcgen05, GemvPlan* p,
+               bool allow_vt = true);
+bool plan_vt(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, GemvPlan* p);
+cudaError_t launch_vt(const GemvPlan& p, const uint8_t* W, const uint8_t* A, const float* x, uint8_t* A_out,
+                      float* y, void* workspace, bool pdl, cudaStream_t s);
 
 // Kernel launchers (q8_aux.cu / q8_gemv.cu).  Each returns the CUDA error of
 // the launch.  `pdl` launches with programmatic stream serialization.
