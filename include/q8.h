@@ -462,6 +462,16 @@ Q8_API int q8_block_dots(const void *W, int64_t N, int64_t K, const void *A_bloc
  * status. */
 Q8_API int q8_device_error(unsigned *code);
 
+/* Test hook: the time limit, in ns, of the decode GEMV kernels' waits on
+ * their copy ring (the weight stream and, with 9 or more rows, the
+ * activation staging), for every launch enqueued after this call; 0
+ * restores the default of 2 s.  A kernel whose wait gives up reports it in
+ * q8_device_error, stops, lets the copies it issued land (with the full 2 s
+ * bound, whatever the limit), and returns; its outputs are undefined.  Lets
+ * a test make the failure path run without any fault.  Process-wide; not
+ * for use while other threads launch GEMVs.  Returns Q8_OK. */
+Q8_API int q8_set_wait_limit_ns(uint64_t ns);
+
 /* Properties the library uses: SM count and compute capability of the
  * current device. */
 Q8_API int q8_device_info(int *sm_count, int *cc_major, int *cc_minor);

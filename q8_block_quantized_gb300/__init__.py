@@ -65,6 +65,7 @@ SIGNATURES = {
     "q8_block_dots": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _vp]),
     "q8_device_error": (_int, [ctypes.POINTER(ctypes.c_uint)]),
     "q8_device_info": (_int, [ctypes.POINTER(_int), ctypes.POINTER(_int), ctypes.POINTER(_int)]),
+    "q8_set_wait_limit_ns": (_int, [ctypes.c_uint64]),
 }
 
 _lib = None
@@ -317,6 +318,11 @@ def q8_device_error() -> int:
     code = ctypes.c_uint(0)
     _check("q8_device_error", lib().q8_device_error(ctypes.byref(code)))
     return code.value
+
+
+def q8_set_wait_limit_ns(ns: int) -> None:
+    """Test hook: limit of the GEMV ring waits for later launches (0 = 2 s)."""
+    _check("q8_set_wait_limit_ns", lib().q8_set_wait_limit_ns(int(ns)))
 
 
 def q8_device_info():

@@ -364,6 +364,11 @@ int q8_device_error(unsigned* code) {
   return Q8_OK;
 }
 
+int q8_set_wait_limit_ns(uint64_t ns) {
+  set_gemv_wait_limit_ns(ns);
+  return Q8_OK;
+}
+
 int q8_device_info(int* sm_count, int* cc_major, int* cc_minor) {
   DeviceInfo d;
   if (current_device_info(&d) != cudaSuccess) return Q8_ECUDA;

@@ -331,8 +331,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait on an mbarrier phase: false after `limit_ns` without progress.
+// A try_wait may suspend the thread for a time the hardware chooses, so a
+// limit below a millisecond (only set by tests) polls with test_wait instead
+// and is then honoured to the clock's resolution.
+constexpr uint64_t SHORT_WAIT_NS = 1000000ull;
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns < SHORT_WAIT_NS) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+      if (mbar_test_wait(bar, parity)) return true;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {

@@ -3,6 +3,7 @@
 // in q8_gemv_r*.cu).
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "q8_gemv_impl.cuh"
@@ -93,6 +94,12 @@ int budget_of(int R, int MT, bool u5) {
 }  // namespace
 
 cudaError_t device_error_word(int dev, unsigned** out) { return error_word(dev, out); }
+
+namespace {
+std::atomic<uint64_t> g_wait_limit{WAIT_LIMIT_NS};
+}  // namespace
+void set_gemv_wait_limit_ns(uint64_t ns) { g_wait_limit.store(ns == 0 ? WAIT_LIMIT_NS : ns); }
+uint64_t gemv_wait_limit_ns() { return g_wait_limit.load(); }
 
 // Row counts from which a launch takes the virtual-tile kernel (4 to 32 rows
 // per pass); fewer rows take the one-tile-per-unit kernel below.
@@ -205,6 +212,7 @@ cudaError_t launch_gemv(const GemvPlan& p, const uint8_t* W, const uint8_t* A, c
     args.ws_part = p.S > 1 ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(workspace) + TICKET_BYTES)
                            : nullptr;
     args.err = err;
+    args.wait_ns = gemv_wait_limit_ns();
     args.N = p.N;
     args.NB = (int)p.NB;
     args.nch = p.nch;

@@ -131,7 +131,10 @@ struct UCfg {
   static constexpr int A_BYTES = ON ? 2 * CHUNK_BLOCKS * SLICE_A : 0;
   static constexpr int B_BYTES = ON ? 2 * CHUNK_BLOCKS * SLICE_B : 0;
   static constexpr int TMEM_COLS = CHUNK_BLOCKS * MT;  // block j's dots in columns [MT j, MT j + MT)
-  static constexpr int MISC_INTS = ON ? 8 : 4;         // + the MMA mbarrier and the TMEM base
+  // flags, then (tcgen05) the MMA mbarrier and the TMEM base, then the two
+  // consumer abort flags
+  static constexpr int CAB = ON ? 8 : 4;
+  static constexpr int MISC_INTS = CAB + 2;
 };
 // dynamic shared memory a CTA may use on sm_103 (227 KB)
 constexpr int SMEM_LIMIT = 232448;
@@ -198,6 +201,7 @@ struct GemvArgs {
   float* ws_part;        // [S][M][N] partials (S > 1)
   unsigned* ws_cnt;      // [T] tickets (S > 1)
   unsigned* err;         // device error word
+  uint64_t wait_ns;      // limit of the ring's producer and consumer waits (WAIT_LIMIT_NS unless a test shortens it)
   int64_t N;
   int NB, nch, T, M, RU, S, units;
   int act_smem;          // bytes of the activation staging area of this launch (<= ACT_BUDGET, 16 | x)
@@ -230,7 +234,7 @@ __device__ __forceinline__ void produce(const GemvArgs& a, uint8_t* stage_buf, u
         cluster_arrive_one();
         cluster_done = true;
       }
-      if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, WAIT_LIMIT_NS)) {
+      if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, a.wait_ns)) {
         atomicOr(a.err, ERR_PRODUCER_WAIT);
         misc[0] = 1;
         stop = true;
@@ -637,6 +641,8 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
   constexpr bool TC = MT >= TC_MIN_MT;  // tensor-core path
   constexpr int HALVES = MCfg<MT>::HALVES;
   constexpr bool EXCHANGE = (P > 1) || TC || (HALVES > 1);
+  // the abort decision is taken after the per-round exchange barrier
+  static_assert(EXCHANGE || UCfg<R, MT, V>::ON, "every instantiation meets at a barrier each round");
   constexpr int RS = red_stride<MT>();
   constexpr int BAR_CONSUMERS = 1;  // named barrier of the consumer warps
   constexpr bool UM = UCfg<R, MT, V>::ON;  // tcgen05 path
@@ -650,8 +656,18 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
   uint64_t* full = reinterpret_cast<uint64_t*>(act_base + a.act_smem + red_bytes<R, MT, V>());
   uint64_t* empty = full + STAGES;
   volatile int* misc = reinterpret_cast<volatile int*>(empty + STAGES);
-  // misc[0]: abort flag, misc[1]: "this CTA combines the tile", misc[2]: rounds issued;
-  // tcgen05 path: misc[4..5] the MMA mbarrier, misc[6] the tensor-memory base
+  // misc[0]: abort flag (set by the producer or a consumer; stops the
+  // producer, starts the drain), misc[1]: "this CTA combines the tile",
+  // misc[2]: rounds issued; tcgen05 path: misc[4..5] the MMA mbarrier, misc[6]
+  // the tensor-memory base; misc[CAB], misc[CAB + 1]: the consumers' abort
+  // flags, by parity of the round barriers.  A consumer whose wait gave up
+  // sets the flag of the next round barrier before arriving there, and every
+  // consumer reads that flag after passing it: between two barriers no one
+  // writes the flag the others are reading, so all consumers leave at the same
+  // barrier (misc[0], which the producer may set at any moment, is never read
+  // for that decision).
+  volatile int* cab = misc + UCfg<R, MT, V>::CAB;
+  int bc = 0;  // round barriers passed (the same in every consumer)
   uint64_t* mma_bar = reinterpret_cast<uint64_t*>(const_cast<int*>(misc) + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(misc) + 6);
 
@@ -664,6 +680,8 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
     misc[0] = 0;
     misc[1] = 0;
     misc[2] = 0;
+    cab[0] = 0;
+    cab[1] = 0;
     if constexpr (UM) mbar_init(mma_bar, 1);
     fence_mbar_init();
   }
@@ -764,10 +782,11 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
     for (int rho = 0; rho < nrounds; ++rho) {
       // the abort decision must be the same for every consumer (they meet
       // at the exchange barrier below), so it is read after that barrier
-      const bool got = mbar_wait_bounded(&full[stage], phase, WAIT_LIMIT_NS);
+      const bool got = mbar_wait_bounded(&full[stage], phase, a.wait_ns);
       if (!got) {
         atomicOr(a.err, ERR_CONSUMER_WAIT);
         misc[0] = 1;
+        cab[bc & 1] = 1;  // read by every consumer after the next round barrier
       }
       float mv[MC];  // this thread's merged columns of the round
       if constexpr (UM) {
@@ -792,7 +811,8 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
         }
         fence_proxy_async_smem();
         named_bar_sync(BAR_CONSUMERS, NT);
-        const bool go = misc[0] == 0;  // read after the barrier: the same in every consumer
+        const bool go = cab[bc & 1] == 0;  // the same in every consumer
+        ++bc;
         if (go && threadIdx.x == 0) {
           tc_fence_after_sync();
           constexpr uint32_t IDESC = umma_idesc_f16(128, MT);
@@ -808,6 +828,7 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
           if (!done) {
             atomicOr(a.err, ERR_CONSUMER_WAIT);
             misc[0] = 1;
+            cab[bc & 1] = 1;
           }
           done = __all_sync(0xffffffffu, done);  // tcgen05.ld is warp-collective
           if (done) mphase ^= 1u;
@@ -848,16 +869,23 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
         }
 #pragma unroll
         for (int cc = 0; cc < MC; ++cc) mv[cc] = tadd(half_sum[0][cc], half_sum[1][cc]);
+        // a stage is released (and counted) only when its round was received:
+        // after a failed wait no stage with a copy in flight is reused, and
+        // the drain below waits for each of them
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);
-        ++consumed;
+        if (got) {
+          if (lane == 0) mbar_arrive(&empty[stage]);
+          ++consumed;
+        }
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
         tc_fence_before_sync();
         named_bar_sync(BAR_CONSUMERS, NT);  // operands and tensor memory free for the next round
-        if (misc[0]) {
+        const bool ab = cab[bc & 1] != 0;
+        ++bc;
+        if (!go || ab) {
           ok = false;
           break;
         }
@@ -908,9 +936,12 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
             for (int m = 0; m < MT; ++m) rb[((hb * P + p) * R + i) * RS + m] = v[m];
           }
         }
+        // a stage is released (and counted) only when its round was received
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);
-        ++consumed;
+        if (got) {
+          if (lane == 0) mbar_arrive(&empty[stage]);
+          ++consumed;
+        }
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
@@ -920,7 +951,9 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
           // written in round k was last read in round k-2, before the barrier
           // of round k-1 that every writer has passed
           named_bar_sync(BAR_CONSUMERS, NT);
-          if (misc[0]) {
+          const bool ab = cab[bc & 1] != 0;
+          ++bc;
+          if (ab) {
             ok = false;
             break;
           }
@@ -928,7 +961,7 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
   #pragma unroll
           for (int c = 0; c < MC; ++c) mv[c] = tree_of<P, HALVES>(rb + i * RS + mcg * MC + c, R * RS, P * R * RS);
         } else {
-          if (!got || misc[0]) {
+          if (!got) {  // (unreachable: every instantiation exchanges, see the static_assert)
             ok = false;
             break;
           }
@@ -1059,11 +1092,13 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
     }
   }
 
-  // After a failed wait: let rounds that were issued but not consumed land
-  // before the CTA's shared memory goes away (bounded as well).
+  // After a failed wait: let rounds that were issued but not received by
+  // warp 0 land before the CTA's shared memory goes away.  Those stages were
+  // never released, so each has at most one copy in flight; the drain keeps
+  // the full bound whatever limit the ring's waits had.
   if (threadIdx.x == 0 && misc[0]) {
     for (int k = consumed; k < misc[2]; ++k) {
-      if (!mbar_wait_bounded(&full[k % STAGES], (uint32_t)((k / STAGES) & 1), WAIT_LIMIT_NS / 4)) {
+      if (!mbar_wait_bounded(&full[k % STAGES], (uint32_t)((k / STAGES) & 1), WAIT_LIMIT_NS)) {
         atomicOr(a.err, ERR_DRAIN_WAIT);
         break;
       }
@@ -1076,7 +1111,7 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
     tc_fence_before_sync();
     named_bar_sync(BAR_CONSUMERS, NT);
     if (warp == 0) {
-      if (lane == 0 && misc[0]) (void)mbar_wait_bounded(mma_bar, mphase, WAIT_LIMIT_NS / 4);
+      if (lane == 0 && misc[0]) (void)mbar_wait_bounded(mma_bar, mphase, WAIT_LIMIT_NS);
       __syncwarp();
       tmem_dealloc(tmem, UCfg<R, MT, V>::TMEM_COLS);
     }

@@ -162,6 +162,7 @@ cudaError_t launch_vt(const GemvPlan& p, const uint8_t* W, const uint8_t* A, con
     a.ws_cnt = p.S > 1 ? reinterpret_cast<unsigned*>(workspace) : nullptr;
     a.ws_part = p.S > 1 ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(workspace) + TICKET_BYTES) : nullptr;
     a.err = err;
+    a.wait_ns = gemv_wait_limit_ns();
     a.N = p.N;
     a.NB = (int)p.NB;
     a.nch = p.nch;

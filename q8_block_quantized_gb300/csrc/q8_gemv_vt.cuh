@@ -115,6 +115,7 @@ struct Args {
   float* ws_part;        // [S][M][Np] partials (S > 1)
   unsigned* ws_cnt;      // [TV] tickets (S > 1)
   unsigned* err;         // device error word
+  uint64_t wait_ns;      // limit of the ring's and the staging's waits (WAIT_LIMIT_NS unless a test shortens it)
   int64_t N;
   int NB, nch, T, R, G, TV, M, RU, S, units, UB, Np;
   int raw_bytes;         // shared memory for the staging's raw copies (raw_bytes<MT>(UB))
@@ -159,7 +160,7 @@ __device__ __forceinline__ void produce(const Args& a, uint8_t* stage_buf, uint6
     const int c0 = s * a.RU;
     const int nr = min(a.RU, a.nch - c0);
     for (int rho = 0; rho < nr; ++rho) {
-      if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, WAIT_LIMIT_NS)) {
+      if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, a.wait_ns)) {
         atomicOr(a.err, ERR_PRODUCER_WAIT);
         misc[0] = 1;
         stop = true;
@@ -319,7 +320,7 @@ __device__ __forceinline__ void stage_act(const Args& a, uint8_t* aq, float* ad,
     }
     bool got = false;
     if (misc[0] == 0) {
-      got = mbar_wait_bounded(rr.bar, rr.phase, WAIT_LIMIT_NS);
+      got = mbar_wait_bounded(rr.bar, rr.phase, a.wait_ns);
       if (!got) {
         atomicOr(a.err, ERR_CONSUMER_WAIT);
         misc[0] = 1;
@@ -579,7 +580,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_vt_kernel(const Args a) {
       // reused and the drain below can wait for each of them
       bool got = false;
       if (misc[0] == 0) {
-        got = mbar_wait_bounded(&full[stage], phase, WAIT_LIMIT_NS);
+        got = mbar_wait_bounded(&full[stage], phase, a.wait_ns);
         if (!got) {
           atomicOr(a.err, ERR_CONSUMER_WAIT);
           misc[0] = 1;
@@ -769,14 +770,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_vt_kernel(const Args a) {
     }
   }
 
-  // After a failed wait: let rounds that were issued but not received by
-  // warp 0 land before the CTA's shared memory goes away (bounded as well).
-  // Those stages were never released, so each has at most one copy in flight.
+  // After a failed wait: let copies that were issued but not received by
+  // warp 0 land before the CTA's shared memory goes away.  Those stages were
+  // never released, so each has at most one copy in flight; the drain keeps
+  // the full bound whatever limit the other waits had.
   if (threadIdx.x == 0 && misc[0]) {
     if (rr.issued > rr.waited)  // the last piece's copies (at most one piece in flight)
-      if (!mbar_wait_bounded(abar, (uint32_t)(rr.waited & 1), WAIT_LIMIT_NS / 4)) atomicOr(a.err, ERR_DRAIN_WAIT);
+      if (!mbar_wait_bounded(abar, (uint32_t)(rr.waited & 1), WAIT_LIMIT_NS)) atomicOr(a.err, ERR_DRAIN_WAIT);
     for (int k = consumed; k < misc[2]; ++k) {
-      if (!mbar_wait_bounded(&full[k % STAGES], (uint32_t)((k / STAGES) & 1), WAIT_LIMIT_NS / 4)) {
+      if (!mbar_wait_bounded(&full[k % STAGES], (uint32_t)((k / STAGES) & 1), WAIT_LIMIT_NS)) {
         atomicOr(a.err, ERR_DRAIN_WAIT);
         break;
       }

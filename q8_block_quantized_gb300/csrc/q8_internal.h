@@ -63,6 +63,10 @@ cudaError_t launch_gemv(const GemvPlan& p, const uint8_t* W, const uint8_t* A, c
                         uint8_t* A_out, float* y, void* workspace, bool pdl, cudaStream_t s,
                         uint8_t* h_blocks = nullptr);
 cudaError_t read_and_clear_gemv_error(unsigned* code);
+// Limit of the GEMV kernels' ring waits for launches from now on (a test
+// hook: 0 restores the default of 2 s).
+void set_gemv_wait_limit_ns(uint64_t ns);
+uint64_t gemv_wait_limit_ns();
 // The device word the kernels set bits in when a bounded wait gives up.
 cudaError_t device_error_word(int dev, unsigned** out);
 
