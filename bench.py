@@ -324,6 +324,25 @@ def run_ours(args):
     e2e_value = aggregate_gbs(bytes_step, world, ms_e2e)
     del graph2, st2
 
+    # the same e2e step through the ABI without graph capture: every call is
+    # planned and launched by the host, as a caller without graphs sees it
+    def eager_steps(n):
+        for _ in range(n):
+            st.x_all.copy_(x_host, non_blocking=True)
+            st.step()
+            y_host[0].copy_(st.y_all, non_blocking=True)
+    eager_steps(3)
+    barrier()
+    n_eager = max(1, min(args.steps, 300))
+    h0 = time.perf_counter()
+    e0.record(stream)
+    eager_steps(n_eager)
+    e1.record(stream)
+    h1 = time.perf_counter()
+    barrier()
+    ms_eager = max_over_ranks(e0.elapsed_time(e1) / n_eager, world, device="cuda")
+    host_us_per_call = (h1 - h0) * 1e6 / n_eager / max(1, st.launches_per_step())
+
     roof = roofline(st, q8) if rank == 0 else None
     prod = producers(q8, shape) if (rank == 0 and not args.no_producers) else None
     tc5 = tcgen05_vs_default(q8, st) if (rank == 0 and world == 1 and not args.no_producers) else None
@@ -361,7 +380,12 @@ def run_ours(args):
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT,
                     "h2d_bytes_per_step": st.x_all.numel() * 4,
                     "d2h_bytes_per_step": st.y_all.numel() * 4,
-                    "ms_per_step": round(ms_e2e, 5)},
+                    "ms_per_step": round(ms_e2e, 5),
+                    "eager": {"value": round(aggregate_gbs(bytes_step, world, ms_eager), 2), "unit": UNIT,
+                              "ms_per_step": round(ms_eager, 5), "steps": n_eager,
+                              "host_us_per_launch": round(host_us_per_call, 3),
+                              "note": "same copies, every call launched by the host through the C ABI "
+                                      "(no graph; stream-ordered, PDL chained)"}},
             "gpu_launches": st.launches_per_step() * args.steps,
             "clocks": clocks,
         }
@@ -487,11 +511,14 @@ def roofline(st, q8, reps=3):
                         for t, k, b, nn, _ in rows}}
 
 
-def configs_table(q8, st, rounds=30, reps=20, seed=0):
+def configs_table(q8, st, rounds=30, reps=20, seed=0, with_3b=True):
     """The workloads of the metric beside the headline step, each as its own
     CUDA graph on the same weights (the pages' method: configurations
     interleaved in a seeded random order, the median over rounds):
       - the full stack at M = 1, 4, 8, 16 (config 4): GB/s and tok/s;
+      - one decoder layer's projections at M = 1 (config 2), 16 chained
+        calls of layer 0 per graph: us per layer;
+      - the Llama-3.2-3B-shaped stack at M = 1, 16, 32, 64 (config 5);
       - one 2048 x 2048 GEMV at M = 1 (config 1), 40 chained calls per graph,
         hot (one W, resident in L2) and cold (40 copies of W rotated,
         179 MB > L2): us per call;
@@ -526,6 +553,15 @@ def configs_table(q8, st, rounds=30, reps=20, seed=0):
                                           shared_weights=st.weights)
         keep.append(s2)
         cases["stack M=%d" % M] = (s2.capture(), 1, s2.bytes_per_step(), M)
+    # one decoder layer's projections at M = 1 (qkv, o, gate/up, down), 16
+    # chained copies of layer 0 per graph
+    lay = Q8Stack(st.shape, M=1, mode="fused", layers=1, shared_weights=st.weights, include_head=False)
+    keep.append(lay)
+
+    def layer_run():
+        for _ in range(16):
+            lay.step()
+    cases["layer M=1"] = (capture(layer_run), 16, lay.bytes_per_step(), 1)
 
     def gemv_case(W, N, K, M, calls=1, copies=1):
         # `calls` chained calls per graph, rotating over `copies` copies of W
@@ -553,6 +589,15 @@ def configs_table(q8, st, rounds=30, reps=20, seed=0):
         g, n, by = gemv_case(Wh, head.N, head.K, M, calls=4)
         cases["lm_head M=%d" % M] = (g, n, by, M)
 
+    # the Llama-3.2-3B-shaped stack (28 layers + head) at M = 1, 16, 32, 64
+    if with_3b:
+        st3 = Q8Stack(q8_synth.LLAMA_3B, M=1, mode="fused")
+        keep.append(st3)
+        for M in (1, 16, 32, 64):
+            s3 = st3 if M == 1 else Q8Stack(q8_synth.LLAMA_3B, M=M, mode="fused", shared_weights=st3.weights)
+            keep.append(s3)
+            cases["3b stack M=%d" % M] = (s3.capture(), 1, s3.bytes_per_step(), M)
+
     names = list(cases)
     samples = {k: [] for k in names}
     cur = torch.cuda.current_stream()
@@ -577,8 +622,9 @@ def configs_table(q8, st, rounds=30, reps=20, seed=0):
         ms = float(np.median(samples[k]))
         by, M = cases[k][2], cases[k][3]
         ent = {"case": k, "M": M, "us_median": round(ms * 1e3, 3), "GB/s": round(by / (ms * 1e-3) / 1e9, 1)}
-        if k.startswith("stack"):
+        if "stack" in k:
             ent["tok_s"] = round(M / (ms * 1e-3), 1)
+        ent["frac_of_measured_peak"] = round(by / (ms * 1e-3) / 1e9 / _peaks()[0], 4)
         out["results"].append(ent)
     del cases, keep
     torch.cuda.empty_cache()

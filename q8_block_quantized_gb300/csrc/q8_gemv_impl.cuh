@@ -51,6 +51,8 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "q8_device.cuh"
 #include "q8_internal.h"
 
@@ -1120,15 +1122,24 @@ __global__ void __launch_bounds__(MCfg<MT>::THREADS, MCfg<MT>::MIN_CTAS) gemv_ke
 
 // Every libq8 kernel asks for the largest shared-memory carveout (the same
 // for all, so an SM switching between kernels needs no reconfiguration).
+// The attributes are set once per instantiation and device (a bit per
+// device, set after success), not on every launch.
+constexpr int ATTR_MAX_DEVICES = 64;
 template <int R, int MT, bool FUSED, int V>
 cudaError_t set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<R, MT, FUSED, V>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)gemv_smem_bytes<R, MT, V>());
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gemv_kernel<R, MT, FUSED, V>,
-                              cudaFuncAttributePreferredSharedMemoryCarveout,
-                              (int)cudaSharedmemCarveoutMaxShared);
+  const uint64_t bit = (dev >= 0 && dev < ATTR_MAX_DEVICES) ? (uint64_t)1 << dev : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(gemv_kernel<R, MT, FUSED, V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)gemv_smem_bytes<R, MT, V>());
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(gemv_kernel<R, MT, FUSED, V>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+  return e;
 }
 
 template <int R, int MT, bool FUSED, int V>
@@ -1159,13 +1170,20 @@ cudaError_t launch_gemv_t(const GemvArgs& args, int grid, int cluster, bool pdl,
   return cudaLaunchKernelEx(&cfg, gemv_kernel<R, MT, FUSED, V>, args);
 }
 
+// CTAs of this instantiation that fit on an SM, queried once per device.
 template <int R, int MT, bool FUSED, int V>
 int occupancy_t() {
+  static std::atomic<int> cached[ATTR_MAX_DEVICES];  // 0: not queried yet (static storage: zero)
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= ATTR_MAX_DEVICES) return 0;
+  const int c = cached[dev].load(std::memory_order_acquire);
+  if (c != 0) return c > 0 ? c : 0;
   if (set_attributes<R, MT, FUSED, V>() != cudaSuccess) return 0;
   int occ = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemv_kernel<R, MT, FUSED, V>, MCfg<MT>::THREADS,
                                                     gemv_smem_bytes<R, MT, V>()) != cudaSuccess)
     return 0;
+  cached[dev].store(occ > 0 ? occ : -1, std::memory_order_release);
   return occ;
 }
 

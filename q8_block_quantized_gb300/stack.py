@@ -53,6 +53,7 @@ class Q8Stack:
     tcgen05: bool = False                # Q8_FLAG_TCGEN05 on every GEMV call
     device: str = "cuda"
     shared_weights: dict | None = None   # reuse another stack's packed weights
+    include_head: bool = True            # False: the layers' projections only
     calls: list = field(default_factory=list)
 
     def __post_init__(self):
@@ -63,7 +64,7 @@ class Q8Stack:
         projs = self.shape.layer_projs()
         head = self.shape.head()
         dev = torch.device(self.device)
-        entries = [(li, p) for li in range(L) for p in projs] + [(L, head)]
+        entries = [(li, p) for li in range(L) for p in projs] + ([(L, head)] if self.include_head else [])
         # one flat fp32 input buffer and one flat output buffer per step
         self.x_all = torch.empty(self.M * sum(p.K for _, p in entries), dtype=torch.float32,
                                  device=dev)
