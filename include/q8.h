@@ -331,9 +331,12 @@ Q8_API int q8_fused_quant_gemm_swiglu(const void *W, int64_t F, int64_t K, const
  * calls that may run at the same time on the GPU (other streams, other host
  * threads) race on it and must be serialized by the caller.  Each split call
  * first clears the array's ticket area with an asynchronous memset on
- * `stream`.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.
+ * `stream`; on those shapes Q8_FLAG_PDL therefore overlaps the kernel with
+ * the memset, not with the caller's previous kernel.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress, with
+ * that device current) and keeps it; make that first call before any stream
+ * capture, and do not use the library across a cudaDeviceReset of that
+ * device (the address belongs to the context that looked it up).
  *
  * flags is 0 or Q8_FLAG_PDL (the tcgen05 option is not offered here).
  * Arguments, alignment and errors otherwise as q8_gemm.

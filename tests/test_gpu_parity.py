@@ -181,16 +181,55 @@ def test_gemm_within_tolerance(q8, N, K, M):
     assert np.array_equal(Af.cpu().numpy(), Ab)
 
 
-def test_gemm_exact_integer_sum_with_unit_scales(q8):
+def _unit_blocks(rng, rows, K):
+    """Integer values in [-127, 127] with a 127 in every block: every scale is
+    exactly 1 and the quants are the values themselves."""
+    v = rng.integers(-127, 128, size=(rows, K)).astype(np.float32)
+    v[:, ::32] = 127.0
+    return v
+
+
+# Each decode path computes its own block dots: the DP4A path (1-4 rows),
+# the fp16 mma.sync tile kernel (5-8 rows), the virtual-tile kernel (9-64
+# rows, in passes of up to 32) and, with Q8_FLAG_TCGEN05, tcgen05 MMAs (16-row
+# passes on 128-row tiles).  With unit scales and activation row m zero
+# except block b(m), y[m][n] is that row's exact int32 dot for block b(m):
+# every path's dot is compared bit for bit with the oracle's, at every block
+# position of a chunk and on every tile height.
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 12, 16, 32, 64])
+@pytest.mark.parametrize("N", [40, 300, 2048, 16384])
+def test_decode_block_dots_exact_on_every_path(q8, M, N):
+    K = 512  # two chunks of 8 blocks
+    NB = K // 32
+    rng = np.random.default_rng(N * 100 + M)
+    w = _unit_blocks(rng, N, K)
+    x = _unit_blocks(rng, M, K)
+    sel = np.arange(M) % NB
+    for m in range(M):
+        keep = np.zeros(K, dtype=bool)
+        keep[sel[m] * 32:(sel[m] + 1) * 32] = True
+        x[m, ~keep] = 0.0  # zero blocks: scale 0, quants 0, terms exactly 0
+    Wb, Ab = oracle.quantize(w), oracle.quantize(x)
+    isum = oracle.block_dots(Wb, Ab, K)  # [M][N][NB]
+    expect = isum[np.arange(M), :, sel].astype(np.float32)  # [M][N]
+    W = _gpu_pack(q8, torch.from_numpy(w))
+    A = torch.from_numpy(Ab).to(DEV)
+    y = _run_gemm(q8, W, N, K, A, M)
+    assert np.array_equal(y.cpu().numpy(), expect)
+    yf, _ = _run_fused(q8, W, N, K, torch.from_numpy(x).to(DEV), M)
+    assert np.array_equal(yf.cpu().numpy(), expect)
+    if M >= 9 and N % 128 == 0 and q8.q8_packed_tile_rows(N) == 128:
+        yt = _run_gemm(q8, W, N, K, A, M, flags=q8.FLAG_TCGEN05)
+        assert np.array_equal(yt.cpu().numpy(), expect)
+
+
+@pytest.mark.parametrize("M", [4, 8, 16, 64])
+def test_gemm_exact_integer_sum_with_unit_scales(q8, M):
     # every block has amax = 127, so every scale is exactly 1 and
     # y = sum_b isum_b exactly (partial sums stay below 2^24 here)
-    N, K, M = 260, 2048, 4
-    rng = np.random.default_rng(8)
-    def unit_blocks(rows):
-        v = rng.integers(-127, 128, size=(rows, K)).astype(np.float32)
-        v[:, ::32] = 127.0
-        return v
-    w, x = unit_blocks(N), unit_blocks(M)
+    N, K = 260, 2048
+    rng = np.random.default_rng(8 + M)
+    w, x = _unit_blocks(rng, N, K), _unit_blocks(rng, M, K)
     Wb, Ab = oracle.quantize(w), oracle.quantize(x)
     isum = oracle.block_dots(Wb, Ab, K).astype(np.int64).sum(axis=2)
     assert np.abs(isum).max() < 2**24
@@ -199,6 +238,42 @@ def test_gemm_exact_integer_sum_with_unit_scales(q8):
     assert np.array_equal(y.cpu().numpy().astype(np.int64), isum)
     yf, _ = _run_fused(q8, W, N, K, torch.from_numpy(x).to(DEV), M)
     assert np.array_equal(yf.cpu().numpy().astype(np.int64), isum)
+
+
+@pytest.mark.parametrize("M", [1, 3, 8, 16, 40])
+def test_gemm_zero_and_subnormal_scale_blocks(q8, M):
+    # blocks whose binary16 scale is 0 or subnormal (amax below 127 * 2^-14),
+    # in W and in the activations, among ordinary ones: products of two
+    # subnormal binary16 scales are still exact normal fp32 values
+    N, K = 300, 1024
+    rng = np.random.default_rng(20 + M)
+    w = (rng.standard_normal((N, K)) * q8_synth.WEIGHT_STD).astype(np.float32)
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    nb = K // 32
+    for arr, rows in ((w, N), (x, M)):
+        kind = rng.integers(0, 4, size=(rows, nb))  # 0 zero, 1 subnormal, 2 tiny subnormal, 3 ordinary
+        for r in range(rows):
+            for b in range(nb):
+                blk = arr[r, b * 32:(b + 1) * 32]
+                if kind[r, b] == 0:
+                    blk[:] = 0.0
+                elif kind[r, b] == 1:
+                    blk *= np.float32(1e-4) / np.abs(blk).max()
+                elif kind[r, b] == 2:
+                    blk *= np.float32(3e-7) / np.abs(blk).max()
+    Wb, Ab = oracle.quantize(w), oracle.quantize(x)
+    d16, _ = oracle.split_blocks(Wb, K)
+    assert ((d16 & 0x7C00) == 0).any() and ((d16 != 0) & ((d16 & 0x7C00) == 0)).any()
+    y_ref, S_ref = oracle.gemm(Wb, Ab, K)
+    W = _gpu_pack(q8, torch.from_numpy(w))
+    y = _run_gemm(q8, W, N, K, torch.from_numpy(Ab).to(DEV), M)
+    _assert_within_tol(y, y_ref, S_ref)
+    yf, Af = _run_fused(q8, W, N, K, torch.from_numpy(x).to(DEV), M, want_A=True)
+    assert np.array_equal(Af.cpu().numpy(), Ab)
+    assert torch.equal(yf, y)
+    # the row decoded alone has the same bits
+    y1 = _run_gemm(q8, W, N, K, torch.from_numpy(Ab[-1:].copy()).to(DEV), 1)
+    assert torch.equal(y1[0], y[-1])
 
 
 # ---------------------------------------------------------------------------

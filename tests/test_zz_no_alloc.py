@@ -9,6 +9,9 @@ result against q8_gemm with a caller-allocated workspace: within the parity
 tolerance used everywhere (|dy| <= 1e-5 * sum|terms| + 1e-6, sum|terms| from
 the oracle) and, because both run the same reduction order, bit for bit.
 
+Shapes of more than 32 rows run as several launches that reuse the scratch
+one after the other; Q8_FLAG_PDL is covered too.
+
 This file is collected last so a run that stops at the first failure has
 already run every other test; it passes alone in a fresh process too.
 """
@@ -39,34 +42,44 @@ def _case(q8, N, K, M, seed):
     x = q8_synth.activations(M, K, q8_synth.derive_seed("na-x", M, K, seed))
     Wb = oracle.quantize(w.numpy())
     Ab = oracle.quantize(x.numpy())
-    _, S = oracle.gemm(Wb, Ab, K)
+    y_or, S = oracle.gemm(Wb, Ab, K)
     W = q8.pack_weights_f32(w.cuda())
     A = torch.from_numpy(Ab).cuda()
-    return W, A, S
+    return W, A, y_or, S
 
 
-def _noalloc_raw(q8, W, N, K, A, M, y):
+def _noalloc_raw(q8, W, N, K, A, M, y, flags=0):
     # straight through the C ABI with raw pointers
     st = q8.lib().q8_gemm_noalloc(ctypes.c_void_p(W.data_ptr()), N, K,
                                   ctypes.c_void_p(A.data_ptr()), M,
-                                  ctypes.c_void_p(y.data_ptr()), 0,
+                                  ctypes.c_void_p(y.data_ptr()), flags,
                                   ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert st == 0, q8.lib().q8_strerror(st).decode()
 
 
-@pytest.mark.parametrize("N,K,M", [(256, 8192, 16), (300, 4096, 16), (512, 2048, 1), (2048, 2048, 3)])
-def test_noalloc_matches_gemm_twice(q8, N, K, M):
+# (N, K, M, whether the shape splits along K and so uses the scratch)
+SHAPES = [(256, 8192, 16, True), (300, 4096, 16, True), (300, 4096, 40, True),
+          (512, 2048, 1, False), (2048, 2048, 3, False)]
+
+
+@pytest.mark.parametrize("N,K,M,split", SHAPES)
+@pytest.mark.parametrize("flags", [0, 1])  # plain, and Q8_FLAG_PDL
+def test_noalloc_matches_gemm_twice(q8, N, K, M, split, flags):
+    assert (q8.q8_workspace_bytes(N, K, M) > 0) == split
+    assert q8.q8_workspace_bytes(N, K, M) <= q8.NOALLOC_SCRATCH_BYTES
     results = []
     for call in range(2):  # two calls in a row reuse the same built-in scratch
-        W, A, S = _case(q8, N, K, M, seed=call)
+        W, A, y_or, S = _case(q8, N, K, M, seed=call)
         ws = q8.new_workspace(N, K, M)
         y_ref = torch.full((M, N), float("nan"), device="cuda")
         q8.q8_gemm(W, N, K, A, M, y_ref, workspace=ws)
         y = torch.full((M, N), float("nan"), device="cuda")
-        _noalloc_raw(q8, W, N, K, A, M, y)
+        _noalloc_raw(q8, W, N, K, A, M, y, flags)
         torch.cuda.synchronize()
-        err = (y.double() - y_ref.double()).abs().cpu().numpy()
-        assert (err <= 1e-5 * S + 1e-6).all(), (N, K, M, call, err.max())
+        # the oracle's fp64 product, within the parity tolerance
+        err = (y.double().cpu().numpy() - y_or)
+        assert (np.abs(err) <= 1e-5 * S + 1e-6).all(), (N, K, M, call, np.abs(err).max())
+        # and bit for bit the call with a caller-allocated workspace
         assert torch.equal(y, y_ref)
         results.append(y)
     assert not torch.equal(results[0], results[1])  # different inputs, fresh results
