@@ -18,15 +18,11 @@ namespace q8 {
 namespace {
 
 constexpr int KV_THREADS = 256;
-constexpr int KV_BATCH = 2;  // blocks per lane group with their loads in flight together
+constexpr int KV_BATCH = 4;  // blocks per lane group with their loads in flight together
 
-// Rows whose slot lies outside the cache are skipped and reported here.
-__device__ __forceinline__ bool slot_of(const int32_t* slots, int64_t r, int64_t capacity, int64_t* s) {
-  const int64_t v = slots != nullptr ? (int64_t)__ldcg(slots + r) : r;
-  *s = v;
-  return v >= 0 && v < capacity;
-}
-
+// Write: the rows' loads do not depend on their slots, so a batch issues the
+// slot loads and the row loads together; a row whose slot lies outside the
+// cache is skipped and reported.
 __global__ void __launch_bounds__(KV_THREADS) kv_quantize_kernel(const float* __restrict__ x, int64_t rows,
                                                                 int nb, const int32_t* __restrict__ slots,
                                                                 int64_t capacity, int8_t* __restrict__ cq,
@@ -38,36 +34,51 @@ __global__ void __launch_bounds__(KV_THREADS) kv_quantize_kernel(const float* __
   const int64_t total = rows * nb;
   const int64_t groups = (int64_t)gridDim.x * (KV_THREADS / 8);
   const int64_t g0 = (int64_t)blockIdx.x * (KV_THREADS / 8) + (threadIdx.x >> 3);
+  // this lane group's blocks are g0, g0 + groups, ...: their (row, block)
+  // advance by (groups / nb, groups % nb) with a carry (no division per block)
+  const int64_t qg = groups / nb, rg = groups - (groups / nb) * nb;
+  int64_t r_cur = g0 / nb, b_cur = g0 - (g0 / nb) * nb;
   // trip counts are uniform across the warp: the shuffles see full warps
   for (int64_t base = 0; base < total; base += groups * KV_BATCH) {
     float4 v[KV_BATCH];
-    int64_t blk[KV_BATCH], s[KV_BATCH];
-    bool on[KV_BATCH];
+    int64_t blk[KV_BATCH], r[KV_BATCH], bb[KV_BATCH], s[KV_BATCH];
+    bool in[KV_BATCH];
 #pragma unroll
     for (int q = 0; q < KV_BATCH; ++q) {
       blk[q] = base + q * groups + g0;
-      on[q] = false;
-      v[q] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      if (blk[q] < total) {
-        const int64_t r = blk[q] / nb;
-        on[q] = slot_of(slots, r, capacity, &s[q]);
-        if (!on[q] && sub == 0 && blk[q] - r * nb == 0) atomicOr(err, ERR_KV_SLOT);
-        if (on[q]) v[q] = __ldcs(reinterpret_cast<const float4*>(x + blk[q] * QK) + sub);
+      in[q] = blk[q] < total;
+      r[q] = r_cur;
+      bb[q] = b_cur;
+      r_cur += qg;
+      b_cur += rg;
+      if (b_cur >= nb) {
+        b_cur -= nb;
+        ++r_cur;
       }
+      s[q] = in[q] ? (slots != nullptr ? (int64_t)__ldcg(slots + r[q]) : r[q]) : -1;
+      v[q] = in[q] ? __ldcs(reinterpret_cast<const float4*>(x + blk[q] * QK) + sub)
+                   : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
     uint32_t w[KV_BATCH];
     float d[KV_BATCH];
     quantize_group8<KV_BATCH, false>(v, w, d);
 #pragma unroll
     for (int q = 0; q < KV_BATCH; ++q) {
-      if (!on[q]) continue;
-      const int64_t r = blk[q] / nb, b = blk[q] - r * nb;
+      if (!in[q]) continue;
+      const int64_t b = bb[q];
+      if (s[q] < 0 || s[q] >= capacity) {
+        if (sub == 0 && b == 0) atomicOr(err, ERR_KV_SLOT);
+        continue;
+      }
       reinterpret_cast<uint32_t*>(cq + s[q] * D + b * QK)[sub] = w[q];
       if (sub == 0) cd[s[q] * nb + b] = d[q];
     }
   }
 }
 
+// Read back: a batch loads its slots first, then every block's quants and
+// scale, then stores; a row whose slot lies outside the cache reads as zeros
+// and is reported.
 __global__ void __launch_bounds__(KV_THREADS) kv_dequantize_kernel(const int8_t* __restrict__ cq,
                                                                   const float* __restrict__ cd,
                                                                   int64_t capacity, int nb,
@@ -80,21 +91,45 @@ __global__ void __launch_bounds__(KV_THREADS) kv_dequantize_kernel(const int8_t*
   const int64_t D = (int64_t)nb * QK;
   const int64_t total = rows * nb;
   const int64_t groups = (int64_t)gridDim.x * (KV_THREADS / 8);
-  for (int64_t g = (int64_t)blockIdx.x * (KV_THREADS / 8) + (threadIdx.x >> 3); g < total; g += groups) {
-    const int64_t r = g / nb, b = g - r * nb;
-    int64_t s;
-    float4 o = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if (slot_of(slots, r, capacity, &s)) {
-      const uint32_t w = __ldcs(reinterpret_cast<const unsigned int*>(cq + s * D + b * QK) + sub);
-      const float d = __ldcs(cd + s * nb + b);
-      o.x = __fmul_rn((float)(int)(int8_t)(w & 0xffu), d);
-      o.y = __fmul_rn((float)(int)(int8_t)((w >> 8) & 0xffu), d);
-      o.z = __fmul_rn((float)(int)(int8_t)((w >> 16) & 0xffu), d);
-      o.w = __fmul_rn((float)(int)(int8_t)(w >> 24), d);
-    } else if (sub == 0 && b == 0) {
-      atomicOr(err, ERR_KV_SLOT);
+  const int64_t g0 = (int64_t)blockIdx.x * (KV_THREADS / 8) + (threadIdx.x >> 3);
+  const int64_t qg = groups / nb, rg = groups - (groups / nb) * nb;
+  int64_t r_cur = g0 / nb, b_cur = g0 - (g0 / nb) * nb;
+  for (int64_t base = 0; base < total; base += groups * KV_BATCH) {
+    int64_t blk[KV_BATCH], b[KV_BATCH], s[KV_BATCH];
+    bool in[KV_BATCH], ok[KV_BATCH];
+#pragma unroll
+    for (int q = 0; q < KV_BATCH; ++q) {
+      blk[q] = base + q * groups + g0;
+      in[q] = blk[q] < total;
+      const int64_t r = r_cur;
+      b[q] = b_cur;
+      r_cur += qg;
+      b_cur += rg;
+      if (b_cur >= nb) {
+        b_cur -= nb;
+        ++r_cur;
+      }
+      s[q] = in[q] ? (slots != nullptr ? (int64_t)__ldcg(slots + r) : r) : -1;
     }
-    __stcs(reinterpret_cast<float4*>(out + g * QK) + sub, o);
+    uint32_t w[KV_BATCH];
+    float d[KV_BATCH];
+#pragma unroll
+    for (int q = 0; q < KV_BATCH; ++q) {
+      ok[q] = in[q] && s[q] >= 0 && s[q] < capacity;
+      w[q] = ok[q] ? __ldcs(reinterpret_cast<const unsigned int*>(cq + s[q] * D + b[q] * QK) + sub) : 0u;
+      d[q] = ok[q] ? __ldcs(cd + s[q] * nb + b[q]) : 0.0f;
+    }
+#pragma unroll
+    for (int q = 0; q < KV_BATCH; ++q) {
+      if (!in[q]) continue;
+      if (!ok[q] && sub == 0 && b[q] == 0) atomicOr(err, ERR_KV_SLOT);
+      float4 o;
+      o.x = __fmul_rn((float)(int)(int8_t)(w[q] & 0xffu), d[q]);
+      o.y = __fmul_rn((float)(int)(int8_t)((w[q] >> 8) & 0xffu), d[q]);
+      o.z = __fmul_rn((float)(int)(int8_t)((w[q] >> 16) & 0xffu), d[q]);
+      o.w = __fmul_rn((float)(int)(int8_t)(w[q] >> 24), d[q]);
+      __stcs(reinterpret_cast<float4*>(out + blk[q] * QK) + sub, o);
+    }
   }
 }
 
