@@ -965,6 +965,19 @@ def run_prefill_only(args):
     torch.cuda.synchronize()
 
 
+def run_kv_only(args):
+    """The int8 KV codec legs alone (for profiling): one JSON line."""
+    import torch
+
+    import __graft_entry__
+    import q8_synth
+    __graft_entry__.build()
+    import q8_block_quantized_gb300 as q8
+    shape = q8_synth.LLAMA_1B if args.model == "1b" else q8_synth.LLAMA_3B
+    print(json.dumps(kv_codec(q8, shape)))
+    torch.cuda.synchronize()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -983,8 +996,12 @@ def main():
     ap.add_argument("--prefill-only", type=int, default=0, metavar="ROWS",
                     help="only time the prefill tile GEMM over the stack at ROWS tokens (one JSON line; "
                          "not the benchmark line)")
+    ap.add_argument("--kv-only", action="store_true",
+                    help="only time the int8 KV codec (one JSON line; not the benchmark line)")
     args = ap.parse_args()
-    if args.prefill_only:
+    if args.kv_only:
+        run_kv_only(args)
+    elif args.prefill_only:
         run_prefill_only(args)
     elif args.impl == "reference":
         run_reference(args)
