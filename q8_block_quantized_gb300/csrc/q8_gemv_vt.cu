@@ -11,6 +11,59 @@
 namespace q8 {
 namespace vt {
 
+// ---- the staged image of the activations (fused calls with many rows) --------
+// Quantizes x [M][K] once, exactly as q8_quantize_act does, and writes the
+// staged layout of the virtual-tile kernel for each launch of 32 rows and
+// each K range of UB blocks.  Launch p (rows 32p..) owns pass_stride bytes at
+// img + p * pass_stride; its image s (act_bytes(UB) bytes for its MP staged
+// rows, at s * act_bytes(UB) within) holds the fp16 quants of its row m,
+// block bl at m * rsb + bl * 64 and the fp32 scale at MP * rsb + (bl * MP +
+// m) * 4.  Every launch has MP_full staged rows except the last (MP_last).
+// Optionally also writes the blocks themselves (A_out).  Eight lanes per
+// block; the trip counts are uniform across the CTA.
+constexpr int IMG_THREADS = 256;
+constexpr int IMG_B = 2;  // blocks per lane group in flight
+__global__ void __launch_bounds__(IMG_THREADS) vt_image_kernel(const float* __restrict__ x, int M, int NB, int UB,
+                                                               int MP_full, int MP_last, uint8_t* __restrict__ img,
+                                                               int64_t pass_stride, uint8_t* __restrict__ A_out) {
+  pdl_launch_dependents();
+  pdl_wait();
+  constexpr int B = IMG_B;
+  const int sub = threadIdx.x & 7;
+  const int rsb = act_rsb(UB);
+  const int last_pass = (M - 1) >> 5;
+  const int64_t total = (int64_t)M * NB;
+  const int64_t groups = (int64_t)gridDim.x * (IMG_THREADS / 8);
+  const int64_t g0 = (int64_t)blockIdx.x * (IMG_THREADS / 8) + (threadIdx.x >> 3);
+  for (int64_t base = 0; base < total; base += groups * B) {
+    float4 v[B];
+    int64_t blk[B];
+#pragma unroll
+    for (int q = 0; q < B; ++q) {
+      blk[q] = base + q * groups + g0;
+      v[q] = blk[q] < total ? __ldcg(reinterpret_cast<const float4*>(x + blk[q] * QK) + sub)
+                            : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    uint32_t w[B];
+    float d[B];
+    quantize_group8<B>(v, w, d);
+#pragma unroll
+    for (int q = 0; q < B; ++q) {
+      if (blk[q] >= total) continue;
+      const int m = (int)(blk[q] / NB), b = (int)(blk[q] - (int64_t)m * NB);
+      const int pass = m >> 5, ml = m & 31;
+      const int MP = pass == last_pass ? MP_last : MP_full;
+      const int s = b / UB, bl = b - s * UB;
+      uint8_t* im = img + pass * pass_stride + (int64_t)s * ((int64_t)MP * rsb + (int64_t)UB * MP * 4);
+      uint32_t lo, hi;
+      i8x4_to_h2x2(w[q], lo, hi);
+      *reinterpret_cast<uint2*>(im + (size_t)ml * rsb + bl * 64 + sub * 8) = make_uint2(lo, hi);
+      if (sub == 0) reinterpret_cast<float*>(im + (size_t)MP * rsb)[bl * MP + ml] = d[q];
+      if (A_out != nullptr) store_block_lane(A_out + blk[q] * BLOCK_BYTES, sub, w[q], d[q]);
+    }
+  }
+}
+
 
 namespace {
 
@@ -56,18 +109,28 @@ cudaError_t ensure_attributes(int dev, int MT, bool fused) {
 }
 
 // A fused call with at least this many rows per pass quantizes x once (the
-// quantize kernel, into A_blocks_out or the workspace) and runs the GEMV on
-// the blocks: every CTA quantizing all of its K range costs more than the
-// extra launch once the rows are many.
+// image kernel, into the workspace and A_blocks_out) and runs the GEMV on the
+// staged images: every CTA quantizing and converting all of its K range costs
+// more than the extra launch once the rows are many.
 constexpr int QUANT_FIRST_MT = 16;
 
 // Workspace of a plan: the tickets (always reserved: one workspace serves
 // every call, and a split call needs them zero), the partials when split
-// along K, then the quantized activations of a quantize-first fused call.
+// along K, then the staged images of a quantize-first fused call.
 size_t act_offset(const GemvPlan& q, int Mp) {
   const size_t part = TICKET_BYTES + (q.S > 1 ? (size_t)q.S * Mp * q.Np * 4 : 0);
   return (part + 15) & ~(size_t)15;
 }
+
+// Staged rows of an instantiation and the bytes of one staged image.
+int mp_of(int MT) { return MT < 8 ? 8 : MT; }
+size_t image_bytes(int MT, int UB) {
+  const int MP = mp_of(MT);
+  return (size_t)MP * act_rsb(UB) + (size_t)UB * MP * 4;
+}
+// Images of a call: every launch of 32 rows owns S images of the plan's
+// largest instantiation.
+size_t pass_stride(const GemvPlan& q) { return (size_t)q.S * image_bytes(q.MT, q.UB); }
 
 int64_t pow2_floor(int64_t v) {
   int64_t p = 1;
@@ -121,7 +184,7 @@ bool plan_vt(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, Gem
   q.Np = (int)((N + 3) / 4 * 4);
   q.cluster = 1;
   q.ws_bytes = q.S > 1 ? TICKET_BYTES + (size_t)q.S * Mp * q.Np * 4 : 0;
-  if (fused && q.MT >= QUANT_FIRST_MT) q.ws_bytes = act_offset(q, Mp) + (size_t)M * q.NB * BLOCK_BYTES;
+  if (fused && q.MT >= QUANT_FIRST_MT) q.ws_bytes = act_offset(q, Mp) + (size_t)((M + 31) / 32) * pass_stride(q);
   *out = q;
   return true;
 }
@@ -135,13 +198,31 @@ cudaError_t launch_vt(const GemvPlan& p, const uint8_t* W, const uint8_t* A, con
   if (e != cudaSuccess) return e;
   unsigned* err = nullptr;
   if ((e = device_error_word(dev, &err)) != cudaSuccess) return e;
+  const uint8_t* img = nullptr;
   if (fused && p.MT >= QUANT_FIRST_MT) {
-    // quantize once (bit-exact with the in-kernel quantization), then the
-    // GEMV on the blocks as a programmatic dependent of the quantize kernel
-    uint8_t* blocks = A_out != nullptr ? A_out
-                                       : reinterpret_cast<uint8_t*>(workspace) + act_offset(p, p.M > 32 ? 32 : p.M);
-    if ((e = launch_quantize(x, p.M, p.K, blocks, pdl, s)) != cudaSuccess) return e;
-    A = blocks;
+    // quantize once into the staged images (bit-exact with the in-kernel
+    // quantization), then the GEMV on them as a programmatic dependent
+    uint8_t* im = reinterpret_cast<uint8_t*>(workspace) + act_offset(p, p.M > 32 ? 32 : p.M);
+    const int last = p.M - (p.M - 1) / 32 * 32;  // rows of the last launch
+    const int mt_last = mt_of(last) < p.MT ? mt_of(last) : p.MT;
+    const int64_t nblocks = (int64_t)p.M * p.NB;
+    const int64_t per_cta = (int64_t)(IMG_THREADS / 8) * IMG_B;
+    int64_t grid = (nblocks + per_cta - 1) / per_cta;
+    if (grid > 8 * 1024) grid = 8 * 1024;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(IMG_THREADS);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, vt_image_kernel, x, p.M, (int)p.NB, p.UB, mp_of(p.MT), mp_of(mt_last), im,
+                           (int64_t)pass_stride(p), A_out);
+    if (e != cudaSuccess) return e;
+    img = im;
+    A = nullptr;
     x = nullptr;
     A_out = nullptr;
     fused = false;
@@ -177,6 +258,7 @@ cudaError_t launch_vt(const GemvPlan& p, const uint8_t* W, const uint8_t* A, con
     a.UB = p.UB;
     a.Np = p.Np;
     a.raw_bytes = raw_of(MT, p.UB);
+    a.img = img ? img + (size_t)(m0 / 32) * pass_stride(p) : nullptr;
     switch (MT) {
       case 4: e = launch_m<4>(a, fused, p.grid, pdl, s); break;
       case 8: e = launch_m<8>(a, fused, p.grid, pdl, s); break;

@@ -119,6 +119,10 @@ struct Args {
   int64_t N;
   int NB, nch, T, R, G, TV, M, RU, S, units, UB, Np;
   int raw_bytes;         // shared memory for the staging's raw copies (raw_bytes<MT>(UB))
+  // optional: the staged activations of every K range, prepared by the image
+  // kernel ([S] images of act_bytes<MT>(UB) bytes, 16-byte aligned); the
+  // staging is then one bulk copy per unit
+  const uint8_t* img;
 };
 
 __device__ __forceinline__ uint2 lds64(const void* p) { return *reinterpret_cast<const uint2*>(p); }
@@ -235,6 +239,27 @@ template <int MT, bool FUSED>
 __device__ __forceinline__ void stage_act(const Args& a, uint8_t* aq, float* ad, int rsb, uint8_t* raw, int b0,
                                           int nblk, RawRing& rr, volatile int* misc) {
   constexpr int BAR_CONSUMERS = 1;
+  if (a.img != nullptr) {
+    // the K range's staged image, prepared once for every CTA: one bulk copy
+    named_bar_sync(BAR_CONSUMERS, NT);  // the staged blocks are free
+    const uint32_t bytes = (uint32_t)act_bytes<MT>(a.UB);
+    if (threadIdx.x == 0 && misc[0] == 0) {
+      mbar_arrive_expect_tx(rr.bar, bytes);
+      bulk_g2s_nohint(aq, a.img + (size_t)(b0 / a.UB) * bytes, bytes, rr.bar);
+      ++rr.issued;
+    }
+    if (misc[0] == 0) {
+      const bool got = mbar_wait_bounded(rr.bar, rr.phase, a.wait_ns);
+      if (!got) {
+        atomicOr(a.err, ERR_CONSUMER_WAIT);
+        misc[0] = 1;
+      } else if (threadIdx.x == 0) {
+        ++rr.waited;
+      }
+    }
+    rr.phase ^= 1u;
+    return;  // every consumer waited for the copy itself
+  }
   constexpr int BPP = NT / 8;  // blocks per pass
   constexpr int BATCH = FUSED ? 4 : 8;
   const int64_t K = (int64_t)a.NB * QK;
