@@ -343,23 +343,52 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The same two waits acquiring at cluster scope: for phases completed by
+// arrivals of other CTAs of the cluster (mbar_arrive_remote).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait on an mbarrier phase: false after `limit_ns` without progress.
 // A try_wait may suspend the thread for a time the hardware chooses, so a
 // limit below a millisecond (only set by tests) polls with test_wait instead
-// and is then honoured to the clock's resolution.
+// and is then honoured to the clock's resolution.  CLUSTER: acquire at
+// cluster scope, always polling (phases completed by other CTAs' arrivals
+// are waited for without suspending the thread).
 constexpr uint64_t SHORT_WAIT_NS = 1000000ull;
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
-  if (limit_ns < SHORT_WAIT_NS) {
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-      if (mbar_test_wait(bar, parity)) return true;
-      if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
+template <bool CLUSTER>
+__device__ __forceinline__ bool mbar_probe(uint64_t* bar, uint32_t parity, bool poll) {
+  if constexpr (CLUSTER) {
+    return poll ? mbar_test_wait_cluster(bar, parity) : mbar_try_wait_cluster(bar, parity);
+  } else {
+    return poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity);
   }
-  if (mbar_try_wait(bar, parity)) return true;
+}
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const bool poll = CLUSTER || limit_ns < SHORT_WAIT_NS;
+  if (mbar_probe<CLUSTER>(bar, parity, poll)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_probe<CLUSTER>(bar, parity, poll)) return true;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
@@ -484,6 +513,20 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
 __device__ __forceinline__ void st_cluster_u16(uint32_t addr, unsigned short v) {
   asm volatile("st.shared::cluster.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+// Arrival on the mbarrier at `remote` (a shared::cluster address, e.g. from
+// mapa_shared), releasing at cluster scope what happened before it.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
 
 // Programmatic dependent launch: no-ops when the grid was launched normally.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

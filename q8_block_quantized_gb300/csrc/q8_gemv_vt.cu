@@ -108,6 +108,27 @@ cudaError_t ensure_attributes(int dev, int MT, bool fused) {
   return e;
 }
 
+// Clusters of `cl` CTAs that can be resident at once, per device,
+// instantiation and cluster size (queried once).
+int g_max_clusters[MAX_DEVICES][4][2][9];
+bool g_max_clusters_known[MAX_DEVICES][4][2][9] = {};
+int max_clusters(int dev, int MT, bool fused, int cl) {
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  const int mi = mi_of(MT), fi = fused ? 1 : 0;
+  if (!g_max_clusters_known[dev][mi][fi][cl]) {
+    int n;
+    switch (MT) {
+      case 4: n = max_clusters_m<4>(fused, cl); break;
+      case 8: n = max_clusters_m<8>(fused, cl); break;
+      case 16: n = max_clusters_m<16>(fused, cl); break;
+      default: n = max_clusters_m<32>(fused, cl); break;
+    }
+    g_max_clusters[dev][mi][fi][cl] = n;
+    g_max_clusters_known[dev][mi][fi][cl] = true;
+  }
+  return g_max_clusters[dev][mi][fi][cl];
+}
+
 // A fused call with at least this many rows per pass quantizes x once (the
 // image kernel, into the workspace and A_blocks_out) and runs the GEMV on the
 // staged images: every CTA quantizing and converting all of its K range costs
@@ -116,9 +137,10 @@ constexpr int QUANT_FIRST_MT = 16;
 
 // Workspace of a plan: the tickets (always reserved: one workspace serves
 // every call, and a split call needs them zero), the partials when split
-// along K, then the staged images of a quantize-first fused call.
+// along K without a cluster, then the staged images of a quantize-first
+// fused call.
 size_t act_offset(const GemvPlan& q, int Mp) {
-  const size_t part = TICKET_BYTES + (q.S > 1 ? (size_t)q.S * Mp * q.Np * 4 : 0);
+  const size_t part = TICKET_BYTES + (q.S > 1 && q.cluster == 1 ? (size_t)q.S * Mp * q.Np * 4 : 0);
   return (part + 15) & ~(size_t)15;
 }
 
@@ -183,7 +205,19 @@ bool plan_vt(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, Gem
   q.grid = (int)(units < dev.sm_count ? units : dev.sm_count);
   q.Np = (int)((N + 3) / 4 * 4);
   q.cluster = 1;
-  q.ws_bytes = q.S > 1 ? TICKET_BYTES + (size_t)q.S * Mp * q.Np * 4 : 0;
+  // split along K: the S CTAs of a virtual tile form a cluster and combine
+  // through distributed shared memory, when every virtual tile's cluster
+  // can be resident at once (a CTA of a cluster waits for its peers before
+  // it moves on, so a second wave would wait for the first)
+  if (S > 1 && S <= MAX_CLUSTER) {
+    const bool kfused = fused && q.MT < QUANT_FIRST_MT;  // the instantiation launched
+    if (ensure_attributes(dev.device, q.MT, kfused) != cudaSuccess) return false;
+    if (TV <= max_clusters(dev.device, q.MT, kfused, (int)S)) {
+      q.cluster = (int)S;
+      q.grid = (int)(TV * S);
+    }
+  }
+  q.ws_bytes = q.S > 1 ? act_offset(q, Mp) : 0;
   if (fused && q.MT >= QUANT_FIRST_MT) q.ws_bytes = act_offset(q, Mp) + (size_t)((M + 31) / 32) * pass_stride(q);
   *out = q;
   return true;
@@ -259,6 +293,7 @@ cudaError_t launch_vt(const GemvPlan& p, const uint8_t* W, const uint8_t* A, con
     a.Np = p.Np;
     a.raw_bytes = raw_of(MT, p.UB);
     a.img = img ? img + (size_t)(m0 / 32) * pass_stride(p) : nullptr;
+    a.cl = p.cluster;
     switch (MT) {
       case 4: e = launch_m<4>(a, fused, p.grid, pdl, s); break;
       case 8: e = launch_m<8>(a, fused, p.grid, pdl, s); break;

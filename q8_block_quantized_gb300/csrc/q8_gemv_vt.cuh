@@ -58,9 +58,10 @@ constexpr int STAGES = 3;
 constexpr int STAGE_BYTES = VR * CHUNK_BLOCKS * BLOCK_BYTES;  // 34,816
 constexpr int SLOT_UNIT = CHUNK_BLOCKS * BLOCK_BYTES;         // 272 bytes per row of a chunk
 constexpr int SMEM_LIMIT = 232448;                            // dynamic shared memory of one CTA
-constexpr int MISC_BYTES = (2 * STAGES + 1) * 8 + 24;         // mbarriers + flags
+constexpr int MISC_BYTES = (2 * STAGES + 3) * 8 + 24;         // mbarriers + flags
 constexpr int ACT_BUDGET = SMEM_LIMIT - STAGES * STAGE_BYTES - MISC_BYTES;
 constexpr int MAX_SPLITS = 64;
+constexpr int MAX_CLUSTER = 8;                                 // portable cluster size
 constexpr int SPLIT_LV = 7;                                   // counter levels for S <= 127
 constexpr int MAX_TILES_SPLIT = 4096;                         // tickets in the workspace prefix
 constexpr size_t TICKET_BYTES = (size_t)MAX_TILES_SPLIT * 4;
@@ -123,7 +124,26 @@ struct Args {
   // kernel ([S] images of act_bytes<MT>(UB) bytes, 16-byte aligned); the
   // staging is then one bulk copy per unit
   const uint8_t* img;
+  // CTAs of a cluster (1: none).  With cl = S > 1 each cluster owns whole
+  // virtual tiles, its CTA of rank s the K split s, and the splits combine
+  // through distributed shared memory instead of the workspace.
+  int cl;
 };
+
+// Units of this CTA: first, first + step, ... below end.  Plain launches
+// take units blockIdx.x, blockIdx.x + gridDim.x, ...; in a cluster the CTA
+// of rank s takes split s of virtual tiles cid, cid + ncl, ... (cid: its
+// cluster, ncl: the clusters of the grid; clusters are consecutive CTAs).
+struct UnitRange {
+  int first, step, end;
+};
+__device__ __forceinline__ UnitRange unit_range(const Args& a) {
+  if (a.cl > 1) {
+    const int rank = (int)blockIdx.x % a.cl, cid = (int)blockIdx.x / a.cl;
+    return {rank * a.TV + cid, (int)gridDim.x / a.cl, (rank + 1) * a.TV};
+  }
+  return {(int)blockIdx.x, (int)gridDim.x, a.units};
+}
 
 __device__ __forceinline__ uint2 lds64(const void* p) { return *reinterpret_cast<const uint2*>(p); }
 
@@ -151,6 +171,9 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
 }
 
 // ---- producer: one lane streams the rounds of every unit of this CTA -------
+// In a cluster the producer lane also completes the cluster barrier that
+// the kernel opens (mbarriers initialised everywhere): it waits once its
+// first STAGES rounds are issued, so streaming does not wait for the cluster.
 __device__ __forceinline__ void produce(const Args& a, uint8_t* stage_buf, uint64_t* full, uint64_t* empty,
                                         volatile int* misc) {
   const uint64_t pol = l2_policy_evict_first();
@@ -158,12 +181,18 @@ __device__ __forceinline__ void produce(const Args& a, uint8_t* stage_buf, uint6
   uint32_t phase = 0;
   int issued = 0;
   bool stop = false;
+  bool cluster_done = a.cl == 1;
   const int slot = a.R * SLOT_UNIT;
-  for (int u = blockIdx.x; u < a.units && !stop; u += gridDim.x) {
+  const UnitRange ur = unit_range(a);
+  for (int u = ur.first; u < ur.end && !stop; u += ur.step) {
     const int s = u / a.TV, tv = u - s * a.TV;
     const int c0 = s * a.RU;
     const int nr = min(a.RU, a.nch - c0);
     for (int rho = 0; rho < nr; ++rho) {
+      if (!cluster_done && issued == STAGES) {
+        asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+        cluster_done = true;
+      }
       if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, a.wait_ns)) {
         atomicOr(a.err, ERR_PRODUCER_WAIT);
         misc[0] = 1;
@@ -205,6 +234,7 @@ __device__ __forceinline__ void produce(const Args& a, uint8_t* stage_buf, uint6
       }
     }
   }
+  if (!cluster_done) asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
 
 // ---- activation staging ------------------------------------------------------
@@ -532,8 +562,13 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_vt_kernel(const Args a) {
   uint64_t* full = reinterpret_cast<uint64_t*>(raw + a.raw_bytes);
   uint64_t* empty = full + STAGES;
   uint64_t* abar = empty + STAGES;
-  volatile int* misc = reinterpret_cast<volatile int*>(abar + 1);
+  uint64_t* pready = abar + 1;  // cluster: the partials of every CTA of the cluster are in place
+  uint64_t* pdone = abar + 2;   // cluster: every CTA of the cluster has read this CTA's partials
+  volatile int* misc = reinterpret_cast<volatile int*>(abar + 3);
   // misc[0]: abort flag, misc[1]: "this CTA combines the tile", misc[2]: rounds issued
+  // In a cluster, a unit's partials [M][VR] sit in the raw area: the CTA
+  // stages its one K range before its first unit and never again.
+  float* pbuf = reinterpret_cast<float*>(raw);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -542,6 +577,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_vt_kernel(const Args a) {
       mbar_init(&empty[s], NCW);
     }
     mbar_init(abar, 1);
+    if (a.cl > 1) {
+      mbar_init(pready, a.cl);
+      mbar_init(pdone, a.cl);
+    }
     misc[0] = 0;
     misc[1] = 0;
     misc[2] = 0;
@@ -549,10 +588,28 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_vt_kernel(const Args a) {
   }
   __syncthreads();
   pdl_launch_dependents();
+  // In a cluster every thread arrives on the cluster barrier now (the
+  // mbarriers above are initialised) and waits before its first access to
+  // another CTA: the consumers before their first remote arrival, the
+  // producer lane inside produce(); lanes 1-31 of the producer warp wait and
+  // exit.
+  const bool clu = a.cl > 1;
   if (warp == NCW) {
+    if (clu) {
+      __syncwarp();
+      cluster_arrive_aligned();
+      if (lane != 0) {
+        asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+        return;
+      }
+    }
     if (lane == 0) produce(a, stage_buf, full, empty, misc);
     return;
   }
+  if (clu) cluster_arrive_aligned();
+  bool cl_synced = !clu;
+  int ncomb = 0;  // cluster combines done (phase parity of pready and pdone)
+  const int crank = clu ? (int)blockIdx.x % a.cl : 0;
   RawRing rr{abar, 0u, 0, 0};
 
   const int g = lane >> 2, tig = lane & 3;
@@ -566,7 +623,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_vt_kernel(const Args a) {
   bool waited = false;
   int staged_s = -1;
 
-  for (int u = blockIdx.x; u < a.units; u += gridDim.x) {
+  const UnitRange ur = unit_range(a);
+  for (int u = ur.first; u < ur.end; u += ur.step) {
     const int s = u / a.TV, tv = u - s * a.TV;
     const int c0 = s * a.RU;
     const int nr = min(a.RU, a.nch - c0);
@@ -690,6 +748,104 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_vt_kernel(const Args a) {
       continue;
     }
 
+    if (clu) {
+      // split along K inside the cluster: every CTA puts its unit value into
+      // its own shared memory, and CTA rank k combines the k-th share of the
+      // tile's outputs from the partials of all ranks (distributed shared
+      // memory), in split order as below
+      // (one thread waits on each mbarrier and a CTA barrier passes the
+      // phase on; the arrivals on the cl CTAs are issued by cl lanes at once)
+      if (ncomb > 0) {  // the previous unit's partials are read by every CTA
+        if (threadIdx.x == 0 && misc[0] == 0 &&
+            !mbar_wait_bounded<true>(pdone, (uint32_t)((ncomb - 1) & 1), a.wait_ns)) {
+          atomicOr(a.err, ERR_CONSUMER_WAIT);
+          misc[0] = 1;
+        }
+        named_bar_sync(BAR_CONSUMERS, NT);
+      }
+      if (!cl_synced) {  // every CTA's mbarriers are initialised
+        cluster_wait_aligned();
+        cl_synced = true;
+      }
+      if (ok && live && misc[0] == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NTL; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int m = 8 * nt + 2 * tig + (e & 1);
+            const int row = g + (e >> 1) * 8;
+            if (m < a.M) pbuf[m * VR + row0v + row] = pv[nt][e];
+          }
+      }
+      named_bar_sync(BAR_CONSUMERS, NT);
+      if ((int)threadIdx.x < a.cl) mbar_arrive_remote(mapa_shared(smem_u32(pready), threadIdx.x));
+      if (threadIdx.x == 0 && misc[0] == 0 && !mbar_wait_bounded<true>(pready, (uint32_t)(ncomb & 1), a.wait_ns)) {
+        atomicOr(a.err, ERR_CONSUMER_WAIT);
+        misc[0] = 1;
+      }
+      named_bar_sync(BAR_CONSUMERS, NT);  // every partial of the cluster is visible
+      {
+        const int64_t nbase = (int64_t)tv * VR;
+        const int nrows = (int)min((int64_t)VR, a.N - nbase);
+        const int quads = a.M * (VR / 4);
+        const int share = (quads + a.cl - 1) / a.cl;
+        const int qa = crank * share, qb = min(quads, qa + share);
+        const uint32_t pb0 = smem_u32(pbuf);
+        for (int qd = qa + (int)threadIdx.x; qd < qb; qd += NT) {
+          const int m = qd / (VR / 4), n4 = (qd - m * (VR / 4)) * 4;
+          const uint32_t off = pb0 + (uint32_t)(m * VR + n4) * 4u;
+          float4 pk[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            pk[k] = k < a.cl ? ld_cluster_f4(mapa_shared(off, (uint32_t)k)) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          float sl[SPLIT_LV][4];
+#pragma unroll
+          for (int l = 0; l < SPLIT_LV; ++l)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sl[l][e] = 0.0f;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            if (k < a.cl) {
+              float vv[4] = {pk[k].x, pk[k].y, pk[k].z, pk[k].w};
+              bool placed = false;
+#pragma unroll
+              for (int l = 0; l < SPLIT_LV; ++l) {
+                if (!placed) {
+                  if ((k >> l) & 1) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) vv[e] = tadd(sl[l][e], vv[e]);
+                  } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sl[l][e] = vv[e];
+                    placed = true;
+                  }
+                }
+              }
+            }
+          }
+          float out[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          bool h = false;
+#pragma unroll
+          for (int l = 0; l < SPLIT_LV; ++l) {
+            if ((a.cl >> l) & 1) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) out[e] = h ? tadd(sl[l][e], out[e]) : sl[l][e];
+              h = true;
+            }
+          }
+          if (misc[0] == 0) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if (n4 + e < nrows) a.y[(int64_t)m * a.N + nbase + n4 + e] = out[e];
+          }
+        }
+      }
+      named_bar_sync(BAR_CONSUMERS, NT);  // this CTA's reads of the partials are done
+      if ((int)threadIdx.x < a.cl) mbar_arrive_remote(mapa_shared(smem_u32(pdone), threadIdx.x));
+      ++ncomb;
+      continue;
+    }
+
     // split along K: publish the unit value, take a ticket, the last one combines
     if (ok && live && misc[0] == 0) {
 #pragma unroll
@@ -795,6 +951,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemv_vt_kernel(const Args a) {
     }
   }
 
+  if (clu) {
+    if (!cl_synced) cluster_wait_aligned();
+    // no other CTA of the cluster reads this one's shared memory any more
+    // (the full bound, whatever the other waits had)
+    if (threadIdx.x == 0 && ncomb > 0 &&
+        !mbar_wait_bounded<true>(pdone, (uint32_t)((ncomb - 1) & 1), WAIT_LIMIT_NS))
+      atomicOr(a.err, ERR_DRAIN_WAIT);
+  }
   // After a failed wait: let copies that were issued but not received by
   // warp 0 land before the CTA's shared memory goes away.  Those stages were
   // never released, so each has at most one copy in flight; the drain keeps
@@ -816,6 +980,8 @@ template <int MT>
 cudaError_t launch_m(const Args& a, bool fused, int grid, bool pdl, cudaStream_t s);
 template <int MT>
 cudaError_t attributes_m(bool fused);
+template <int MT>
+int max_clusters_m(bool fused, int cl);
 
 template <int MT, bool FUSED>
 cudaError_t set_attributes() {
@@ -833,12 +999,46 @@ cudaError_t launch_t(const Args& args, int grid, bool pdl, cudaStream_t s) {
   cfg.blockDim = dim3(THREADS);
   cfg.dynamicSmemBytes = smem_bytes();
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (args.cl > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = args.cl;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, gemv_vt_kernel<MT, FUSED>, args);
+}
+
+// Clusters of `cl` CTAs of this kernel that can be resident at once (0 when
+// none can).
+template <int MT, bool FUSED>
+int max_clusters_t(int cl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(cl);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem_bytes();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemv_vt_kernel<MT, FUSED>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 // Per-row-count translation units instantiate the launch and the attribute
@@ -851,6 +1051,10 @@ cudaError_t launch_t(const Args& args, int grid, bool pdl, cudaStream_t s) {
   template <>                                                                                           \
   cudaError_t attributes_m<MT>(bool fused) {                                                            \
     return fused ? set_attributes<MT, true>() : set_attributes<MT, false>();                            \
+  }                                                                                                     \
+  template <>                                                                                           \
+  int max_clusters_m<MT>(bool fused, int cl) {                                                          \
+    return fused ? max_clusters_t<MT, true>(cl) : max_clusters_t<MT, false>(cl);                        \
   }
 
 }  // namespace vt

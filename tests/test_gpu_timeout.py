@@ -74,3 +74,36 @@ def test_shortened_wait_reports_timeout_and_next_call_is_correct(q8, big, M):
     q8.q8_fused_quant_gemm(W, N, K, x, M, y2, workspace=ws)
     assert q8.q8_device_error() == 0
     assert torch.equal(y2, y_ref)
+
+
+@pytest.mark.parametrize("M", [16, 40])
+def test_shortened_wait_on_k_split_shapes(q8, M):
+    # 16 virtual tiles of 128 rows, K split 8 ways: the splits of a tile run
+    # as one cluster and combine through distributed shared memory.  A
+    # failed wait must not stop a CTA from signalling the others, and no CTA
+    # may leave while another still reads its shared memory: the call ends,
+    # reports the timeout without a drain failure, and the next call is right.
+    N, K = 2048, 8192
+    W = q8.pack_weights_f32(q8_synth.weights(N, K, q8_synth.derive_seed("timeout-split", N, K), DEV))
+    x = q8_synth.activations(M, K, q8_synth.derive_seed("timeout-split-x", M), DEV)
+    ws = q8.new_workspace(N, K, M)
+    y_ref = torch.empty(M, N, device=DEV)
+    q8.q8_fused_quant_gemm(W, N, K, x, M, y_ref, workspace=ws)
+    assert q8.q8_device_error() == 0
+    y = torch.empty(M, N, device=DEV)
+    q8.q8_set_wait_limit_ns(1)
+    try:
+        q8.q8_fused_quant_gemm(W, N, K, x, M, y, workspace=ws)
+        code = q8.q8_device_error()
+    finally:
+        q8.q8_set_wait_limit_ns(0)
+    assert code >> 8 == ETIMEOUT_STATUS, hex(code)
+    roles = code & 0xFF
+    assert roles & (ROLE_PRODUCER | ROLE_CONSUMER), hex(code)
+    assert not roles & ~(ROLE_PRODUCER | ROLE_CONSUMER), hex(code)
+    if ws is not None:
+        ws.zero_()
+    y2 = torch.empty(M, N, device=DEV)
+    q8.q8_fused_quant_gemm(W, N, K, x, M, y2, workspace=ws)
+    assert q8.q8_device_error() == 0
+    assert torch.equal(y2, y_ref)
