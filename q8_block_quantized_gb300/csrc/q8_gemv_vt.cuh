@@ -481,10 +481,6 @@ __device__ __forceinline__ void block_terms(const uint8_t* cq, const uint8_t* sc
   const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
   float acc[NTL][4];
 #pragma unroll
-  for (int nt = 0; nt < NTL; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
-#pragma unroll
   for (int h = 0; h < 2; ++h) {
     uint32_t af[4];
     i8x4_to_h2x2(lds32(cq + ((2 * j + h) * r + rloc + g) * 16 + 4 * tig), af[0], af[2]);
@@ -492,7 +488,11 @@ __device__ __forceinline__ void block_terms(const uint8_t* cq, const uint8_t* sc
 #pragma unroll
     for (int nt = 0; nt < NTL; ++nt) {
       const uint2 b = lds64(aq + (size_t)(8 * nt + g) * rsb + blk * 64 + h * 32 + tig * 8);
-      mma_16816(acc[nt], af, b.x, b.y);
+      if (h == 0) {
+        mma_16816_c0(acc[nt], af, b.x, b.y);
+      } else {
+        mma_16816_acc(acc[nt], af, b.x, b.y);
+      }
     }
   }
   const float dw0 =
