@@ -115,8 +115,9 @@ Q8_API size_t q8_packed_bytes(int64_t N, int64_t K);
 Q8_API int q8_packed_tile_rows(int64_t N);
 
 /* Workspace bytes q8_gemm / q8_fused_quant_gemm need for this shape on the
- * current device (0 when the work is not split along K).  Returns 0 for
- * invalid shapes. */
+ * current device: partial sums when the work is split along K, and from 16
+ * rows per launch the activations staged once per call for every CTA; 0
+ * when neither applies.  Returns 0 for invalid shapes. */
 Q8_API size_t q8_workspace_bytes(int64_t N, int64_t K, int M);
 
 /*
@@ -319,13 +320,15 @@ Q8_API int q8_fused_quant_gemm_swiglu(const void *W, int64_t F, int64_t K, const
  * no counterpart; it is a packaging variant of q8_gemm and computes the same
  * bits.
  *
- * When the work is split along K, the partial sums go to a scratch array of
+ * What q8_gemm keeps in its workspace (partial sums of a split along K, the
+ * activations staged once per call) goes to a scratch array of
  * Q8_NOALLOC_SCRATCH_BYTES compiled into the library: it occupies that much
  * memory on every GPU that loads the library, until the process exits.
- * Neither this call nor the library allocates anything.  Shapes whose split
- * would need more scratch than that return Q8_ESCRATCH before anything is
- * enqueued (q8_workspace_bytes(N, K, M) tells the size; 0 means no scratch
- * is used and any size works).
+ * Neither this call nor the library allocates anything.  When the staged
+ * activations would not fit, the call stages them in every CTA instead (the
+ * same bits); shapes whose split alone needs more scratch return
+ * Q8_ESCRATCH before anything is enqueued (q8_workspace_bytes(N, K, M) is an
+ * upper bound of the size; 0 means no scratch is used and any size works).
  *
  * Every call shares the one array and it keeps the last call's contents:
  * calls that may run at the same time on the GPU (other streams, other host

@@ -108,10 +108,10 @@ uint64_t gemv_wait_limit_ns() { return g_wait_limit.load(); }
 #endif
 
 bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, bool tcgen05, GemvPlan* out,
-               bool allow_vt) {
+               bool allow_vt, bool allow_image) {
   // (shapes the virtual-tile plan cannot take, e.g. K beyond what its splits
   // cover, fall back to the kernel below: the bits are the same)
-  if (allow_vt && !tcgen05 && M >= Q8_VT_MIN_M && plan_vt(dev, N, K, M, fused, out)) return true;
+  if (allow_vt && !tcgen05 && M >= Q8_VT_MIN_M && plan_vt(dev, N, K, M, fused, allow_image, out)) return true;
   GemvPlan q;
   q.N = N;
   q.K = K;

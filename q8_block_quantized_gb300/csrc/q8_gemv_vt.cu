@@ -11,19 +11,22 @@
 namespace q8 {
 namespace vt {
 
-// ---- the staged image of the activations (fused calls with many rows) --------
-// Quantizes x [M][K] once, exactly as q8_quantize_act does, and writes the
-// staged layout of the virtual-tile kernel for each launch of 32 rows and
-// each K range of UB blocks.  Launch p (rows 32p..) owns pass_stride bytes at
+// ---- the staged image of the activations (calls with many rows) ---------------
+// Quantizes x [M][K] once, exactly as q8_quantize_act does (FROM_BLOCKS:
+// reads the blocks A [M][NB] instead), and writes the staged layout of the
+// virtual-tile kernel for each launch of 32 rows and each K range of UB
+// blocks.  Launch p (rows 32p..) owns pass_stride bytes at
 // img + p * pass_stride; its image s (act_bytes(UB) bytes for its MP staged
 // rows, at s * act_bytes(UB) within) holds the fp16 quants of its row m,
 // block bl at m * rsb + bl * 64 and the fp32 scale at MP * rsb + (bl * MP +
 // m) * 4.  Every launch has MP_full staged rows except the last (MP_last).
-// Optionally also writes the blocks themselves (A_out).  Eight lanes per
-// block; the trip counts are uniform across the CTA.
+// Optionally also writes the blocks themselves (A_out, quantizing only).
+// Eight lanes per block; the trip counts are uniform across the CTA.
 constexpr int IMG_THREADS = 256;
 constexpr int IMG_B = 2;  // blocks per lane group in flight
-__global__ void __launch_bounds__(IMG_THREADS) vt_image_kernel(const float* __restrict__ x, int M, int NB, int UB,
+template <bool FROM_BLOCKS>
+__global__ void __launch_bounds__(IMG_THREADS) vt_image_kernel(const float* __restrict__ x,
+                                                               const uint8_t* __restrict__ A, int M, int NB, int UB,
                                                                int MP_full, int MP_last, uint8_t* __restrict__ img,
                                                                int64_t pass_stride, uint8_t* __restrict__ A_out) {
   pdl_launch_dependents();
@@ -36,17 +39,32 @@ __global__ void __launch_bounds__(IMG_THREADS) vt_image_kernel(const float* __re
   const int64_t groups = (int64_t)gridDim.x * (IMG_THREADS / 8);
   const int64_t g0 = (int64_t)blockIdx.x * (IMG_THREADS / 8) + (threadIdx.x >> 3);
   for (int64_t base = 0; base < total; base += groups * B) {
-    float4 v[B];
     int64_t blk[B];
-#pragma unroll
-    for (int q = 0; q < B; ++q) {
-      blk[q] = base + q * groups + g0;
-      v[q] = blk[q] < total ? __ldcg(reinterpret_cast<const float4*>(x + blk[q] * QK) + sub)
-                            : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    }
     uint32_t w[B];
     float d[B];
-    quantize_group8<B>(v, w, d);
+    if constexpr (FROM_BLOCKS) {
+      // a block is 34 bytes (2-byte aligned): the binary16 scale, then 32 quants
+#pragma unroll
+      for (int q = 0; q < B; ++q) {
+        blk[q] = base + q * groups + g0;
+        w[q] = 0u;
+        d[q] = 0.0f;
+        if (blk[q] < total) {
+          const unsigned short* b16 = reinterpret_cast<const unsigned short*>(A + blk[q] * BLOCK_BYTES);
+          w[q] = (uint32_t)__ldcg(b16 + 1 + 2 * sub) | ((uint32_t)__ldcg(b16 + 2 + 2 * sub) << 16);
+          d[q] = __half2float(__ushort_as_half(__ldcg(b16)));
+        }
+      }
+    } else {
+      float4 v[B];
+#pragma unroll
+      for (int q = 0; q < B; ++q) {
+        blk[q] = base + q * groups + g0;
+        v[q] = blk[q] < total ? __ldcg(reinterpret_cast<const float4*>(x + blk[q] * QK) + sub)
+                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+      quantize_group8<B>(v, w, d);
+    }
 #pragma unroll
     for (int q = 0; q < B; ++q) {
       if (blk[q] >= total) continue;
@@ -59,7 +77,7 @@ __global__ void __launch_bounds__(IMG_THREADS) vt_image_kernel(const float* __re
       i8x4_to_h2x2(w[q], lo, hi);
       *reinterpret_cast<uint2*>(im + (size_t)ml * rsb + bl * 64 + sub * 8) = make_uint2(lo, hi);
       if (sub == 0) reinterpret_cast<float*>(im + (size_t)MP * rsb)[bl * MP + ml] = d[q];
-      if (A_out != nullptr) store_block_lane(A_out + blk[q] * BLOCK_BYTES, sub, w[q], d[q]);
+      if (!FROM_BLOCKS && A_out != nullptr) store_block_lane(A_out + blk[q] * BLOCK_BYTES, sub, w[q], d[q]);
     }
   }
 }
@@ -129,10 +147,11 @@ int max_clusters(int dev, int MT, bool fused, int cl) {
   return g_max_clusters[dev][mi][fi][cl];
 }
 
-// A fused call with at least this many rows per pass quantizes x once (the
-// image kernel, into the workspace and A_blocks_out) and runs the GEMV on the
-// staged images: every CTA quantizing and converting all of its K range costs
-// more than the extra launch once the rows are many.
+// A call with at least this many rows per pass stages its activations once
+// (the image kernel: quantizes x into the workspace and A_blocks_out, or
+// converts the blocks) and runs the GEMV on the staged images: every CTA
+// quantizing or converting all of its K range costs more than the extra
+// launch once the rows are many.
 constexpr int QUANT_FIRST_MT = 16;
 
 // Workspace of a plan: the tickets (always reserved: one workspace serves
@@ -164,7 +183,7 @@ int64_t pow2_floor(int64_t v) {
 }  // namespace vt
 
 // Plan of the virtual-tile kernel for M rows (passes of at most 32 rows).
-bool plan_vt(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, GemvPlan* out) {
+bool plan_vt(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, bool image, GemvPlan* out) {
   using namespace vt;
   if (dev.device < 0 || dev.device >= MAX_DEVICES) return false;
   GemvPlan q;
@@ -210,7 +229,7 @@ bool plan_vt(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, Gem
   // can be resident at once (a CTA of a cluster waits for its peers before
   // it moves on, so a second wave would wait for the first)
   if (S > 1 && S <= MAX_CLUSTER) {
-    const bool kfused = fused && q.MT < QUANT_FIRST_MT;  // the instantiation launched
+    const bool kfused = fused && !(image && q.MT >= QUANT_FIRST_MT);  // the instantiation launched
     if (ensure_attributes(dev.device, q.MT, kfused) != cudaSuccess) return false;
     if (TV <= max_clusters(dev.device, q.MT, kfused, (int)S)) {
       q.cluster = (int)S;
@@ -218,7 +237,8 @@ bool plan_vt(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, Gem
     }
   }
   q.ws_bytes = q.S > 1 ? act_offset(q, Mp) : 0;
-  if (fused && q.MT >= QUANT_FIRST_MT) q.ws_bytes = act_offset(q, Mp) + (size_t)((M + 31) / 32) * pass_stride(q);
+  q.img = image && q.MT >= QUANT_FIRST_MT;
+  if (q.img) q.ws_bytes = act_offset(q, Mp) + (size_t)((M + 31) / 32) * pass_stride(q);
   *out = q;
   return true;
 }
@@ -233,9 +253,9 @@ cudaError_t launch_vt(const GemvPlan& p, const uint8_t* W, const uint8_t* A, con
   unsigned* err = nullptr;
   if ((e = device_error_word(dev, &err)) != cudaSuccess) return e;
   const uint8_t* img = nullptr;
-  if (fused && p.MT >= QUANT_FIRST_MT) {
-    // quantize once into the staged images (bit-exact with the in-kernel
-    // quantization), then the GEMV on them as a programmatic dependent
+  if (p.img) {
+    // stage once into the images (bit-exact with the in-kernel staging),
+    // then the GEMV on them as a programmatic dependent
     uint8_t* im = reinterpret_cast<uint8_t*>(workspace) + act_offset(p, p.M > 32 ? 32 : p.M);
     const int last = p.M - (p.M - 1) / 32 * 32;  // rows of the last launch
     const int mt_last = mt_of(last) < p.MT ? mt_of(last) : p.MT;
@@ -252,8 +272,10 @@ cudaError_t launch_vt(const GemvPlan& p, const uint8_t* W, const uint8_t* A, con
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, vt_image_kernel, x, p.M, (int)p.NB, p.UB, mp_of(p.MT), mp_of(mt_last), im,
-                           (int64_t)pass_stride(p), A_out);
+    e = fused ? cudaLaunchKernelEx(&cfg, vt_image_kernel<false>, x, (const uint8_t*)nullptr, p.M, (int)p.NB,
+                                   p.UB, mp_of(p.MT), mp_of(mt_last), im, (int64_t)pass_stride(p), A_out)
+              : cudaLaunchKernelEx(&cfg, vt_image_kernel<true>, (const float*)nullptr, A, p.M, (int)p.NB, p.UB,
+                                   mp_of(p.MT), mp_of(mt_last), im, (int64_t)pass_stride(p), (uint8_t*)nullptr);
     if (e != cudaSuccess) return e;
     img = im;
     A = nullptr;

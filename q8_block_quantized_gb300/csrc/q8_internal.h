@@ -31,6 +31,7 @@ struct GemvPlan {
   // partials [S][rows][Np] when split along K
   bool vt = false;
   int TV = 0, UB = 0, Np = 0;
+  bool img = false;  // the activations are staged once per call into the workspace (16+ rows per pass)
 };
 
 struct DeviceInfo {
@@ -41,10 +42,11 @@ struct DeviceInfo {
 
 cudaError_t current_device_info(DeviceInfo* out);
 // allow_vt = false keeps every row count on the one-tile-per-unit kernel
-// (the SwiGLU epilogue exists only there).
+// (the SwiGLU epilogue exists only there); allow_image = false plans the
+// virtual-tile kernel without the staged activation images (less workspace).
 bool plan_gemv(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, bool tcgen05, GemvPlan* p,
-               bool allow_vt = true);
-bool plan_vt(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, GemvPlan* p);
+               bool allow_vt = true, bool allow_image = true);
+bool plan_vt(const DeviceInfo& dev, int64_t N, int64_t K, int M, bool fused, bool image, GemvPlan* p);
 cudaError_t launch_vt(const GemvPlan& p, const uint8_t* W, const uint8_t* A, const float* x, uint8_t* A_out,
                       float* y, void* workspace, bool pdl, cudaStream_t s);
 

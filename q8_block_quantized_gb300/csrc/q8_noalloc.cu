@@ -72,6 +72,9 @@ extern "C" int q8_gemm_noalloc(const void* W, int64_t N, int64_t K, const void* 
   if (d.device < 0 || d.device >= MAX_DEVICES) return Q8_EDEVICE;
   GemvPlan p;
   if (!plan_gemv(d, N, K, M, false, false, &p)) return Q8_ESHAPE;
+  // without the staged activation images if those do not fit (the bits are the same)
+  if (p.ws_bytes > NOALLOC_BYTES && p.img && !plan_gemv(d, N, K, M, false, false, &p, true, false))
+    return Q8_ESHAPE;
   if (p.ws_bytes > NOALLOC_BYTES) return Q8_ESCRATCH;  // this shape needs more scratch than built in
   void* ws = nullptr;
   if (p.ws_bytes > 0) {

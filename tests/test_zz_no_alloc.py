@@ -108,3 +108,23 @@ def test_noalloc_rejects_shapes_beyond_scratch(q8):
                                   ctypes.c_void_p(y.data_ptr()), 0, None)
     assert st == -8
     assert "scratch" in q8.lib().q8_strerror(st).decode()
+
+
+def test_noalloc_stages_in_every_cta_when_the_images_do_not_fit(q8):
+    # 64 rows (two launches of 32) at K = 32768: the activations staged once
+    # per call would need more than the built-in scratch, the split's partial
+    # sums alone fit -- the call stages its activations in every CTA instead
+    # and computes the same bits as q8_gemm with a full workspace
+    N, K, M = 256, 32768, 64
+    assert q8.q8_workspace_bytes(N, K, M) > q8.NOALLOC_SCRATCH_BYTES
+    W, A, y_or, S = _case(q8, N, K, M, seed=7)
+    ws = q8.new_workspace(N, K, M)
+    y_ref = torch.full((M, N), float("nan"), device="cuda")
+    q8.q8_gemm(W, N, K, A, M, y_ref, workspace=ws)
+    y = torch.full((M, N), float("nan"), device="cuda")
+    _noalloc_raw(q8, W, N, K, A, M, y)
+    torch.cuda.synchronize()
+    err = (y.double().cpu().numpy() - y_or)
+    assert (np.abs(err) <= 1e-5 * S + 1e-6).all(), np.abs(err).max()
+    assert torch.equal(y, y_ref)
+    assert q8.q8_device_error() == 0
