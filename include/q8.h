@@ -231,8 +231,8 @@ Q8_API int q8_repack_weights(const void *src_blocks, int64_t N, int64_t K, void 
  *   K         positive multiple of 32.
  *   A_blocks  [M][K/32] activation blocks (q8_quantize_act), 2-byte aligned.
  *   M         activation rows, 1 <= M <= Q8_MAX_M.  Decode batches (up to
- *             16 rows) run in one launch; more rows (prefill) run as passes
- *             of 16 rows, each streaming W again, with the same per-row
+ *             32 rows) run in one launch; more rows run as launches of 32
+ *             rows, each streaming W again, with the same per-row
  *             arithmetic, so a prefill row is bitwise the row decoded alone
  *             (Ferro README, "Exactness contract": a row's result does not
  *             depend on the other rows of the launch).  For many rows,
