@@ -34,6 +34,9 @@ METRIC = "Q8_0 decode GEMV effective HBM GB/s (% of GB300 peak) and tok/s, M=1â€
 UNIT = "GB/s"
 DTYPE = "i8*i8->i32, f32 scale+sum"
 FALLBACK_HBM_GBS = 6800.0
+# GB300's nominal HBM3e bandwidth (the data-sheet figure, ~8 TB/s): reported
+# beside the measured copy peak, which is the roofline's denominator
+NOMINAL_HBM_GBS = 7900.0
 
 
 def _peaks():
@@ -369,6 +372,8 @@ def run_ours(args):
             "tok_s": round(args.M * world / (ms_max * 1e-3), 1),
             "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
             "hbm_peak_gbs": peak, "hbm_peak_kind": peak_kind,
+            "pct_of_nominal_hbm_peak": round(100.0 * value / world / NOMINAL_HBM_GBS, 2),
+            "nominal_hbm_gbs": NOMINAL_HBM_GBS,
             "roofline": roof,
             "producers": prod,
             "tcgen05_vs_default": tc5,
