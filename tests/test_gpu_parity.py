@@ -470,3 +470,31 @@ def test_extreme_shapes_sampled_against_oracle(q8, N, K, M):
     del w, W
     torch.cuda.empty_cache()
     assert q8.q8_device_error() == 0
+
+
+# A single virtual tile (N <= 128) split along K into S = K / 256 units: the
+# S CTAs of the tile form one thread-block cluster (S <= 8) and combine
+# their values through distributed shared memory; S = 12 takes the
+# workspace and tickets.  Every row equals the row decoded alone (the
+# one-row kernel, its own split and merge) bit for bit, and the oracle's
+# product within tolerance; fused and unfused calls, and one launch of 32
+# rows plus one of 8 (M = 40).
+@pytest.mark.parametrize("S", [2, 3, 5, 7, 8, 12])
+@pytest.mark.parametrize("M", [9, 16, 40])
+def test_k_split_combine_every_split_count(q8, S, M):
+    N, K = 100, 256 * S
+    w, x = _case(N, K, M, 31 + S)
+    W = _gpu_pack(q8, w)
+    Wb = oracle.quantize(w.numpy())
+    Ab = oracle.quantize(x.numpy())
+    A = torch.from_numpy(Ab).to(DEV)
+    y = _run_gemm(q8, W, N, K, A, M)
+    yf, _ = _run_fused(q8, W, N, K, x.to(DEV), M)
+    torch.cuda.synchronize()
+    assert torch.equal(y, yf)
+    y_ref, S_ref = oracle.gemm(Wb, Ab, K)
+    _assert_within_tol(y, y_ref, S_ref)
+    for m in (0, M // 2, M - 1):
+        solo = _run_gemm(q8, W, N, K, A[m:m + 1].contiguous(), 1)
+        assert torch.equal(y[m:m + 1], solo), m
+    assert q8.q8_device_error() == 0
