@@ -22,7 +22,7 @@ SOURCES = ["q8_abi.cu", "q8_aux.cu", "q8_gemv.cu", "q8_gemv_r16.cu", "q8_gemv_r3
            "q8_gemv_r64.cu", "q8_gemv_r128.cu", "q8_noalloc.cu", "q8_producers.cu",
            "q8_prefill.cu", "q8_kv.cu", "q8_gemv_vt.cu", "q8_gemv_vt_m4.cu", "q8_gemv_vt_m8.cu",
            "q8_gemv_vt_m16.cu", "q8_gemv_vt_m32.cu"]
-HEADERS = ["q8_device.cuh", "q8_internal.h", "q8_gemv_impl.cuh", "q8_gemv_vt.cuh"]
+HEADERS = ["q8_device.cuh", "q8_internal.h", "q8_gemv_impl.cuh", "q8_gemv_vt.cuh", "q8_f32x2.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",

@@ -45,6 +45,7 @@
 #include <cuda_runtime.h>
 
 #include "q8_device.cuh"
+#include "q8_f32x2.cuh"
 #include "q8_internal.h"
 
 namespace q8 {
@@ -146,29 +147,6 @@ __device__ __forceinline__ UnitRange unit_range(const Args& a) {
 }
 
 __device__ __forceinline__ uint2 lds64(const void* p) { return *reinterpret_cast<const uint2*>(p); }
-
-// Two fp32 values in one 64-bit register pair, and their element-wise IEEE
-// multiply and add (f32x2: each element rounded to nearest even, exactly as
-// the scalar operation) -- half the instructions for the block terms and
-// their tree.
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
 
 // ---- producer: one lane streams the rounds of every unit of this CTA -------
 // In a cluster the producer lane also completes the cluster barrier that
