@@ -363,8 +363,14 @@ Q8_API int q8_gemm_noalloc(const void *W, int64_t N, int64_t K, const void *A_bl
  * s_b = fp32(d_w[n][b] * d_a[m][b]) (both binary16 scales widened to fp32),
  *   sigma = +0; sigma = fma(isum_b, s_b, sigma) for the blocks b of one
  *           segment of Q8_PREFILL_SEGMENT consecutive blocks, in order;
- *   Y = +0; Y = Y + sigma for the segments, in order; y[m][n] = Y.
- * (IEEE single precision, round to nearest even, fma rounded once.)  This
+ *   of the nseg segments the first ceil(nseg/2) form the low half, the
+ *   rest the high half:
+ *   Y_lo = +0; Y_lo = Y_lo + sigma for the low half's segments, in order;
+ *   Y_hi = +0; Y_hi = Y_hi + sigma for the high half's segments, in order;
+ *   y[m][n] = Y_lo + Y_hi.
+ * (IEEE single precision, round to nearest even, fma rounded once.)  The
+ * two halves let a launch with few output tiles split every tile along K
+ * over two CTAs without changing any bit.  This
  * is not the decode order of q8_gemm, so a prefill row is not bitwise the
  * decoded row; both are within the library's tolerance of the exact sum:
  * here |y - exact| <= (17 + ceil(K/512)) * 2^-24 * S with S the sum of the

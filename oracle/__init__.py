@@ -177,8 +177,9 @@ def gemm(W, A, K: int):
 
 def gemm_prefill_order(W, A, K: int, seg: int = 16) -> np.ndarray:
     """float32 [M][N]: the prefill product in its fixed single-precision
-    order (fma through segments of `seg` blocks, segment sums added in
-    order); see q8o_gemm_prefill_order."""
+    order (fma through segments of `seg` blocks; the segment sums of the
+    first ceil(nseg/2) segments and of the rest each added in order; then the
+    two halves added); see q8o_gemm_prefill_order."""
     lib = _load()
     W, A = _u8(W), _u8(A)
     nb = K // QK

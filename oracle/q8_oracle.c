@@ -227,22 +227,28 @@ void q8o_gemm(const uint8_t *W, int64_t N, int64_t K,
  * The prefill product's single-precision summation order.  [Ferro],
  * "Exactness contract": prefill rows take the tile GEMM, and a row's result
  * depends neither on how many rows share the launch nor on how the prompt
- * is sliced.  The page fixes no order; the reading taken is the plainest
- * one a tile GEMM can keep per row: for each output, the blocks in order,
- * cut into segments of `seg` consecutive blocks (the last may be shorter);
+ * is sliced.  The page fixes no order; the reading taken is a plain one a
+ * tile GEMM can keep per row and split along K into two halves: for each
+ * output, the blocks in order, cut into nseg segments of `seg` consecutive
+ * blocks (the last may be shorter), the first h = ceil(nseg / 2) segments
+ * forming the low half and the rest the high half;
  *   s_b   = d_w * d_a in fp32 (exact: two 11-bit significands),
  *   sigma = fma(isum_b, s_b, sigma) through a segment, from +0,
- *   Y     = Y + sigma through the segments, from +0.
- * y[m][n] = Y (float).  Every step is one IEEE single-precision operation
- * rounded to nearest even; fmaf rounds once.
+ *   Y_lo  = Y_lo + sigma through the low half's segments, from +0,
+ *   Y_hi  = Y_hi + sigma through the high half's segments, from +0,
+ *   y     = Y_lo + Y_hi.
+ * Every step is one IEEE single-precision operation rounded to nearest
+ * even; fmaf rounds once.
  * ------------------------------------------------------------------------- */
 void q8o_gemm_prefill_order(const uint8_t *W, int64_t N, int64_t K,
                             const uint8_t *A, int64_t M, int64_t seg, float *y)
 {
     int64_t nb = K / QK;
+    int64_t nseg = (nb + seg - 1) / seg;
+    int64_t h = (nseg + 1) / 2;
     for (int64_t m = 0; m < M; ++m)
         for (int64_t n = 0; n < N; ++n) {
-            float Y = 0.0f, sigma = 0.0f;
+            float Y_lo = 0.0f, Y_hi = 0.0f, sigma = 0.0f;
             for (int64_t b = 0; b < nb; ++b) {
                 const uint8_t *wb = W + (n * nb + b) * BLOCK_BYTES;
                 const uint8_t *ab = A + (m * nb + b) * BLOCK_BYTES;
@@ -252,11 +258,14 @@ void q8o_gemm_prefill_order(const uint8_t *W, int64_t N, int64_t K,
                 float s_b = scale_of(wb) * scale_of(ab);
                 sigma = fmaf((float)isum, s_b, sigma);
                 if ((b + 1) % seg == 0 || b == nb - 1) {
-                    Y = Y + sigma;
+                    if (b / seg < h)
+                        Y_lo = Y_lo + sigma;
+                    else
+                        Y_hi = Y_hi + sigma;
                     sigma = 0.0f;
                 }
             }
-            y[m * N + n] = Y;
+            y[m * N + n] = Y_lo + Y_hi;
         }
 }
 

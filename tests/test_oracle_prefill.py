@@ -4,11 +4,13 @@ The prefill tile GEMM keeps, per output, one fixed single-precision order
 ("Ferro" README, "Exactness contract": prefill rows take the tile GEMM and a
 row's result does not depend on how many rows share the launch or how the
 prompt is sliced).  The reading: blocks in order, in segments of 16; inside
-a segment sigma = fma(isum_b, d_w d_a, sigma) from +0; Y = Y + sigma over
-the segments from +0.  Pinned here by values derived by hand (which fail
-for another segment length, a plain running sum, a tree, or a separately
-rounded product), by single-rounding results computed exactly in fp64, and
-by the error bound against the fp64 product.
+a segment sigma = fma(isum_b, d_w d_a, sigma) from +0; the segment sums of
+the first ceil(nseg/2) segments (low half) and of the rest (high half) each
+added in order from +0; y = Y_lo + Y_hi.  Pinned here by values derived by
+hand (which fail for another segment length, a plain running sum, one
+sequential sum over all segments, or a separately rounded product), by
+single-rounding results computed exactly in fp64, and by the error bound
+against the fp64 product.
 """
 import math
 
@@ -53,6 +55,31 @@ def test_segment_structure_by_hand():
     assert oracle.gemm_prefill_order(W, A, 32 * nb, seg=nb)[0, 0] == np.float32(2.0 ** 24)
     y64, _ = oracle.gemm(W, A, 32 * nb)
     assert y64[0, 0] == 2.0 ** 24 + 32
+
+
+def test_halves_by_hand():
+    # four segments of 16 blocks: segment 0 sums to 2^24 (block 0 as above,
+    # its other blocks zero), segments 1, 2, 3 to 1 each.  Low half = the
+    # first two segments: Y_lo = 2^24 + 1, a tie that rounds to 2^24; high
+    # half Y_hi = 1 + 1 = 2; y = 2^24 + 2 (exact).  One sequential sum over
+    # the four segments gives 2^24 (every + 1 is a tie back to 2^24); the
+    # exact sum is 2^24 + 3.
+    nb = 64
+    w = [_block(32.0, [64, 64, 64, 64])] + [_block(0.0, []) for _ in range(nb - 1)]
+    a = [_block(32.0, [64, 64, 64, 64])] + [_block(0.0, []) for _ in range(nb - 1)]
+    for j in (16, 32, 48):
+        w[j] = _block(1.0, [1])
+        a[j] = _block(1.0, [1])
+    W, A = _rows([w]), _rows([a])
+    assert oracle.gemm_prefill_order(W, A, 32 * nb)[0, 0] == np.float32(2.0 ** 24 + 2)
+    # one segment of all 64 blocks: a running fma sum, 2^24
+    assert oracle.gemm_prefill_order(W, A, 32 * nb, seg=nb)[0, 0] == np.float32(2.0 ** 24)
+    y64, _ = oracle.gemm(W, A, 32 * nb)
+    assert y64[0, 0] == 2.0 ** 24 + 3
+    # three segments (K = 48 blocks): low half = two segments, high half the
+    # third alone: Y_lo = 2^24 (tie), Y_hi = 1, y = 2^24 + 1 -> tie -> 2^24
+    W3, A3 = _rows([w[:48]]), _rows([a[:48]])
+    assert oracle.gemm_prefill_order(W3, A3, 32 * 48)[0, 0] == np.float32(2.0 ** 24)
 
 
 def _fused_case():
