@@ -389,9 +389,12 @@ Q8_API int q8_gemm_noalloc(const void *W, int64_t N, int64_t K, const void *A_bl
  *   A_blocks_out  (fused call only, may be NULL) receives the [M][K/32]
  *              blocks of x, 2-byte aligned.
  *   workspace  16-byte aligned, at least q8_prefill_workspace_bytes(K, M)
- *              bytes, not overlapping the other buffers: it receives the
- *              activation blocks packed in 128-row tiles (and, in the fused
- *              call without A_blocks_out, the blocks of x).  Scratch only.
+ *              bytes, not overlapping the other buffers: it receives 4096
+ *              bytes of flags for tiles split along K (cleared by the call
+ *              itself), the activation blocks packed in 128-row tiles and,
+ *              in the fused call without A_blocks_out, the blocks of x.
+ *              Scratch only; calls that may run at the same time must not
+ *              share one.
  *   flags      0 or Q8_FLAG_PDL (the first launch is a programmatic
  *              dependent of the previous work on the stream; the call waits
  *              for that work before it reads anything).

@@ -111,7 +111,8 @@ int prefill_gemm(const void* W, int64_t N, int64_t K, const void* A_blocks, cons
       (A_out != nullptr && !aligned(A_out, 2)))
     return Q8_EALIGN;
   const size_t pk = prefill_packed_bytes(K, M);
-  const size_t need = (x != nullptr && A_out == nullptr) ? 2 * pk : pk;
+  // workspace: the split flags, the packed activations, the blocks of x
+  const size_t need = PREFILL_FLAG_BYTES + ((x != nullptr && A_out == nullptr) ? 2 * pk : pk);
   if (workspace == nullptr || workspace_bytes < need) return Q8_EWORKSPACE;
   if (!aligned(workspace, 16)) return Q8_EALIGN;
   DeviceInfo d;
@@ -119,7 +120,8 @@ int prefill_gemm(const void* W, int64_t N, int64_t K, const void* A_blocks, cons
   if (st != Q8_OK) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   bool pdl = (flags & Q8_FLAG_PDL) != 0;
-  uint8_t* packed = static_cast<uint8_t*>(workspace);
+  unsigned* split_flags = static_cast<unsigned*>(workspace);
+  uint8_t* packed = static_cast<uint8_t*>(workspace) + PREFILL_FLAG_BYTES;
   const uint8_t* blocks = static_cast<const uint8_t*>(A_blocks);
   cudaError_t e;
   if (x != nullptr) {
@@ -128,8 +130,9 @@ int prefill_gemm(const void* W, int64_t N, int64_t K, const void* A_blocks, cons
     blocks = out;
     pdl = true;  // the next launches depend on this library's own launch
   }
-  if ((e = launch_pack_act(blocks, M, K, packed, pdl, s)) != cudaSuccess) return Q8_ECUDA;
-  return cuda_status(launch_prefill(d, static_cast<const uint8_t*>(W), N, K, packed, M, y, true, s));
+  const int nflags = prefill_splits(d, N, K, M) ? (int)(PREFILL_FLAG_BYTES / 4) : 0;
+  if ((e = launch_pack_act(blocks, M, K, packed, pdl, s, split_flags, nflags)) != cudaSuccess) return Q8_ECUDA;
+  return cuda_status(launch_prefill(d, static_cast<const uint8_t*>(W), N, K, packed, M, y, split_flags, true, s));
 }
 
 }  // namespace
@@ -164,7 +167,7 @@ int q8_packed_tile_rows(int64_t N) { return N > 0 ? layout_tile_rows(N) : 0; }
 
 size_t q8_prefill_workspace_bytes(int64_t K, int M) {
   if (!k_ok(K) || K > Q8_MAX_PREFILL_K || M < 1) return 0;
-  return 2 * prefill_packed_bytes(K, M);
+  return PREFILL_FLAG_BYTES + 2 * prefill_packed_bytes(K, M);
 }
 
 int q8_gemm_prefill(const void* W, int64_t N, int64_t K, const void* A_blocks, int M, float* y, void* workspace,

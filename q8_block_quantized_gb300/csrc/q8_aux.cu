@@ -36,9 +36,14 @@ __global__ void __launch_bounds__(QUANT_THREADS) quantize_kernel(const float* __
 // inverse == false copies rows -> packed, inverse == true packed -> rows.
 // R is the tile height: q8_packed_tile_rows(N) for weights, 128 for the
 // activations of the prefill GEMM.
-__global__ void repack_kernel(uint8_t* rows, int64_t N, int64_t nb, int R, uint8_t* packed, bool inverse) {
+// zero, nzero: words to clear first (the prefill GEMM's split flags; none
+// for the weights)
+__global__ void repack_kernel(uint8_t* rows, int64_t N, int64_t nb, int R, uint8_t* packed, bool inverse,
+                              unsigned* zero, int nzero) {
   pdl_launch_dependents();
   pdl_wait();  // (a no-op unless launched as a programmatic dependent)
+  if (blockIdx.x == 0)
+    for (int k = threadIdx.x; k < nzero; k += blockDim.x) zero[k] = 0u;
   const int64_t T = (N + R - 1) / R;
   const int64_t total = T * nb * R;
   for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
@@ -138,11 +143,12 @@ cudaError_t launch_repack(const uint8_t* src, int64_t N, int64_t K, uint8_t* dst
   const int64_t nb = K / QK;
   const int R = layout_tile_rows(N);
   const int64_t total = ((N + R - 1) / R) * nb * R;
-  repack_kernel<<<grid_for(total, 256), 256, 0, s>>>(const_cast<uint8_t*>(src), N, nb, R, dst, false);
+  repack_kernel<<<grid_for(total, 256), 256, 0, s>>>(const_cast<uint8_t*>(src), N, nb, R, dst, false, nullptr, 0);
   return cudaGetLastError();
 }
 
-cudaError_t launch_pack_act(const uint8_t* src, int64_t M, int64_t K, uint8_t* dst, bool pdl, cudaStream_t s) {
+cudaError_t launch_pack_act(const uint8_t* src, int64_t M, int64_t K, uint8_t* dst, bool pdl, cudaStream_t s,
+                            unsigned* zero, int nzero) {
   const int64_t nb = K / QK;
   const int R = MAX_TILE_ROWS;
   const int64_t total = ((M + R - 1) / R) * nb * R;
@@ -155,7 +161,7 @@ cudaError_t launch_pack_act(const uint8_t* src, int64_t M, int64_t K, uint8_t* d
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, repack_kernel, const_cast<uint8_t*>(src), M, nb, R, dst, false);
+  return cudaLaunchKernelEx(&cfg, repack_kernel, const_cast<uint8_t*>(src), M, nb, R, dst, false, zero, nzero);
 }
 
 cudaError_t launch_unpack(const uint8_t* packed, int64_t N, int64_t K, uint8_t* dst,
@@ -163,7 +169,7 @@ cudaError_t launch_unpack(const uint8_t* packed, int64_t N, int64_t K, uint8_t* 
   const int64_t nb = K / QK;
   const int R = layout_tile_rows(N);
   const int64_t total = ((N + R - 1) / R) * nb * R;
-  repack_kernel<<<grid_for(total, 256), 256, 0, s>>>(dst, N, nb, R, const_cast<uint8_t*>(packed), true);
+  repack_kernel<<<grid_for(total, 256), 256, 0, s>>>(dst, N, nb, R, const_cast<uint8_t*>(packed), true, nullptr, 0);
   return cudaGetLastError();
 }
 

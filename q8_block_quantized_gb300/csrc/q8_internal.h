@@ -75,9 +75,15 @@ cudaError_t device_error_word(int dev, unsigned** out);
 // Prefill tile GEMM (q8_prefill.cu): activation blocks [M][K/32] are packed
 // into 128-row tiles (the weights' packed layout with R = 128), then every
 // 128 x 128 output tile is one CTA's work.
-cudaError_t launch_pack_act(const uint8_t* src, int64_t M, int64_t K, uint8_t* dst, bool pdl, cudaStream_t s);
+// (zero, nzero: words cleared before the packing, for the prefill GEMM's split flags)
+cudaError_t launch_pack_act(const uint8_t* src, int64_t M, int64_t K, uint8_t* dst, bool pdl, cudaStream_t s,
+                            unsigned* zero = nullptr, int nzero = 0);
+// flags: PREFILL_FLAG_BYTES of split flags, cleared by the pack launch before it
+constexpr size_t PREFILL_FLAG_BYTES = 4096;
 cudaError_t launch_prefill(const DeviceInfo& dev, const uint8_t* W, int64_t N, int64_t K, const uint8_t* A_packed,
-                           int64_t M, float* y, bool pdl, cudaStream_t s);
+                           int64_t M, float* y, unsigned* flags, bool pdl, cudaStream_t s);
+// whether launch_prefill splits this shape along K (its pack launch clears the flags first)
+bool prefill_splits(const DeviceInfo& dev, int64_t N, int64_t K, int64_t M);
 
 // Int8 KV cache codec (q8_kv.cu).  A row whose slot lies outside [0,
 // capacity) is skipped (the dequantized row is written as zeros) and sets

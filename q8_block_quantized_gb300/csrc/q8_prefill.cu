@@ -79,6 +79,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 constexpr int PF_TN = Q8_PREFILL_TILE_ROWS;  // weight rows per tile: MMA M, tensor-memory lanes
 constexpr int PF_TM = Q8_PREFILL_TILE_ROWS;  // activation rows per tile: MMA N
@@ -101,7 +109,8 @@ constexpr int PF_NBUF = 2;              // accumulators and operand buffers in f
 // fp32 activation scales of a block: written at its conversion, read at its
 // fold a block later; a warp can be at most three blocks ahead of another
 constexpr int PF_DA_BUFS = 4;
-constexpr uint32_t PF_Y_COL = PF_NBUF * PF_TM;  // the segment sums Y
+constexpr uint32_t PF_Y_COL = PF_NBUF * PF_TM;  // the running sum Y of the current half
+constexpr uint32_t PF_YLO_COL = PF_Y_COL + PF_TM;  // the low half's sum, kept for the end
 constexpr uint32_t PF_TMEM_COLS = 512;
 constexpr size_t PF_OFF_OPS = (size_t)PF_STAGES * PF_STAGE;
 constexpr size_t PF_OFF_DA = PF_OFF_OPS + (size_t)PF_NBUF * PF_OPS;
@@ -110,7 +119,14 @@ constexpr size_t PF_SMEM = PF_OFF_BAR + (2 * PF_STAGES + 2 * PF_NBUF) * sizeof(u
 static_assert(PF_OFF_OPS % 1024 == 0, "operand buffers aligned");
 static_assert(PF_SMEM <= 232448, "shared memory per CTA");
 static_assert(PF_TN == 128 && PF_TM == 128, "one MMA shape: M = N = 128");
-static_assert(PF_Y_COL + PF_TM <= PF_TMEM_COLS, "tensor-memory columns");
+static_assert(PF_YLO_COL + PF_TM <= PF_TMEM_COLS, "tensor-memory columns");
+// A launch with few output tiles splits each along K into its low and high
+// half (two CTAs): the high half's CTA stores its sums into y and raises one
+// flag per worker warp; the low half's CTA adds them to its own.  The flags
+// (PF_FLAG_BYTES at the start of the workspace) are cleared by the pack
+// kernel that precedes every GEMM launch.
+constexpr int PF_FLAG_TILES = 128;  // split tiles at most (8 flags of 4 bytes each)
+static_assert(PF_FLAG_TILES * 8 * 4 <= PREFILL_FLAG_BYTES, "split flags fit the workspace's flag area");
 
 enum : unsigned { ERR_PF_WORKER = 16u, ERR_PF_DRAIN = 32u, ERR_PF_ISSUER = 64u, ERR_PF_PRODUCER = 128u };
 
@@ -118,12 +134,25 @@ struct PrefillArgs {
   const uint8_t* W;  // packed weights, tiles of RW rows
   const uint8_t* A;  // packed activations, tiles of 128 rows
   float* y;          // [M][N]
+  unsigned* flags;   // split: [tile][8 worker warps], zero at the start
   int64_t N;
   int M, NB, nch;
   int tm, tiles;     // output tiles along M, in all (< 2^31, checked on the host)
   int RW;
+  int split;         // 1, or 2: item = (tile, half), one item per CTA
+  int h;             // segments of the low half: ceil(nseg / 2)
   unsigned* err;
 };
+
+// The chunks of item T (tile T / split, half T % split): all of K, or the
+// low half's segments (2 chunks each) or the rest.
+__device__ __forceinline__ void pf_item(const PrefillArgs& a, int T, int& tile, int& part, int& c0, int& c1) {
+  tile = T / a.split;
+  part = T - tile * a.split;
+  const int cm = a.h * (Q8_PREFILL_SEGMENT / CHUNK_BLOCKS);
+  c0 = (a.split == 2 && part == 1) ? cm : 0;
+  c1 = (a.split == 2 && part == 0) ? cm : a.nch;
+}
 
 // The 16 fp16 values of quants q (one row, 16 consecutive k) at dst and
 // dst + 128: two core matrices along K of the no-swizzle K-major layout
@@ -187,9 +216,11 @@ __device__ __noinline__ void pf_issue(const PrefillArgs& a, uint8_t* smem, uint6
 __device__ __forceinline__ void pf_producer(const PrefillArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                             volatile int* misc) {
   uint32_t k = 0;
-  for (int T = blockIdx.x; T < a.tiles; T += gridDim.x) {
-    const int nt = T / a.tm, mt = T - nt * a.tm;
-    for (int c = 0; c < a.nch; ++c, ++k) {
+  for (int T = blockIdx.x; T < a.tiles * a.split; T += gridDim.x) {
+    int tile, part, c0, c1;
+    pf_item(a, T, tile, part, c0, c1);
+    const int nt = tile / a.tm, mt = tile - nt * a.tm;
+    for (int c = c0; c < c1; ++c, ++k) {
       const int stage = (int)(k & 1u);
       if (misc[0] != 0 || !mbar_wait_bounded(&empty[stage], ((k >> 1) & 1u) ^ 1u, WAIT_LIMIT_NS)) {
         if (misc[0] == 0) atomicOr(a.err, ERR_PF_PRODUCER);
@@ -212,8 +243,10 @@ __device__ __forceinline__ void pf_issuer(const PrefillArgs& a, uint8_t* smem, u
   uint32_t b = 0;           // blocks issued (only its low bits are used)
   uint32_t mma_issued = 0;  // bit p: parity of accumulator p's MMAs so far; bit 2 + p: any
   bool stop = false;
-  for (int T = blockIdx.x; T < a.tiles && !stop; T += gridDim.x) {
-    for (int c = 0; c < a.nch && !stop; ++c) {
+  for (int T = blockIdx.x; T < a.tiles * a.split && !stop; T += gridDim.x) {
+    int tile, part, c0, c1;
+    pf_item(a, T, tile, part, c0, c1);
+    for (int c = c0; c < c1 && !stop; ++c) {
       const int kb = chunk_blocks(c, a.NB);
       for (int j = 0; j < kb; ++j, ++b) {
         const int pb = (int)(b & 1u);
@@ -243,6 +276,55 @@ __device__ __forceinline__ void pf_issuer(const PrefillArgs& a, uint8_t* smem, u
           !mbar_wait_bounded(&mma_bar[p], ((mma_issued >> p) & 1u) ^ 1u, WAIT_LIMIT_NS))
         atomicOr(a.err, ERR_PF_DRAIN);
   }
+}
+
+// The outputs of one closing half (one warp; its thread holds weight row n
+// and 64 consecutive activation rows of the tile: yp = &y[m0][n], stepped by
+// N; mleft of them exist).  v = this half's sums (tensor memory at yc):
+//   add_lo:  y = Y_lo (tensor memory at yl) + v;
+//   combine: y = v + the other CTA's high-half sums, read from y once its
+//            warp's flag is up (false if it does not come);
+//   publish: y = v, then the flag;  otherwise y = v.
+__device__ __noinline__ bool pf_outputs(uint32_t yc, uint32_t yl, float* yp, int64_t N, int mleft, bool add_lo,
+                                        bool combine, bool publish, unsigned* flag) {
+  const int lane = threadIdx.x & 31;
+  if (combine) {
+    bool ready = true;
+    if (lane == 0) {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_u32(flag) == 0u) {
+        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+          ready = false;
+          break;
+        }
+      }
+    }
+    if (__shfl_sync(0xffffffffu, ready ? 1 : 0, 0) == 0) return false;
+  }
+#pragma unroll 1
+  for (int q = 0; q < 8; ++q) {
+    uint32_t v[8], lv[8];
+    tmem_ld8(yc + q * 8, v);
+    if (add_lo) tmem_ld8(yl + q * 8, lv);
+    tmem_ld_wait();
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float o = __uint_as_float(v[k]);
+      if (add_lo) o = __fadd_rn(__uint_as_float(lv[k]), o);  // Y_lo + Y_hi
+      const bool in = q * 8 + k < mleft;
+      if (combine && in) o = __fadd_rn(o, __ldcg(yp));  // Y_lo + Y_hi, Y_hi from the other CTA
+      if (in) *yp = o;
+      yp += N;
+    }
+  }
+  if (publish) {
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence();
+      st_release_u32(flag, 1u);
+    }
+  }
+  return true;
 }
 
 __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const PrefillArgs a) {
@@ -295,8 +377,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const PrefillArg
     uint32_t kseq = 0;  // chunks
     bool dead = false;
 
-    for (int T = blockIdx.x; T < a.tiles && !dead; T += gridDim.x) {
-      const int nt = T / a.tm, mt = T - (T / a.tm) * a.tm;
+    for (int T = blockIdx.x; T < a.tiles * a.split && !dead; T += gridDim.x) {
+      int tile, part, c0, c1;
+      pf_item(a, T, tile, part, c0, c1);
+      const int nt = tile / a.tm, mt = tile - (tile / a.tm) * a.tm;
       const int ra = tile_rows(mt, a.M, PF_TM);
       const int64_t tw = (int64_t)nt * G + g;
       const int rw = tw * a.RW < a.N ? tile_rows(tw, a.N, a.RW) : 0;
@@ -339,11 +423,23 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const PrefillArg
         }
         const bool last = b == a.NB - 1;
         if (!last && (b + 1) % PF_SEG != 0) return true;
-        // end of a segment: Y = Y + sigma (from +0), Y in tensor memory
+        const int segi = b / PF_SEG;
+        const bool lo_end = !last && segi == a.h - 1;  // the low half closes; the high half follows
+        // A half closes with v = Y + sigma:
+        //   whole K here, low half: v is kept in tensor memory (Y_lo), the high half starts from +0;
+        //   whole K here, last block: y = Y_lo + v (y = v when K has one segment);
+        //   split tile, low half: y = v + the high half's sums, once that half's warp published them;
+        //   split tile, high half: y = v, then this warp's flag.
+        const bool keep_lo = a.split == 1 && lo_end;
+        const bool add_lo = a.split == 1 && last && segi >= a.h;
+        const bool combine = a.split == 2 && part == 0;
+        const bool publish = a.split == 2 && part == 1;
+        const bool fin = (lo_end || last) && !keep_lo;  // y is written below
         const uint32_t yc = tmem + lane_base + PF_Y_COL + (uint32_t)(hf * 64);
-        float* yp = a.y + ((int64_t)mt * PF_TM + hf * 64) * a.N + (int64_t)nt * PF_TN + row;
-        const int64_t N = a.N;
-        const int mleft = wv ? ra - hf * 64 : 0;  // columns of this thread inside the tile
+        const uint32_t yl = tmem + lane_base + PF_YLO_COL + (uint32_t)(hf * 64);
+        // pass 1: Y = Y + sigma (from +0 at a half's first segment) into tensor
+        // memory -- the running sum, or the low half's sum (Y_lo)
+        const uint32_t dst = keep_lo ? yl : yc;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t yv[16];
@@ -360,24 +456,20 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const PrefillArg
             f2_unpack(f2_add(f2_pack(__uint_as_float(yv[2 * e]), __uint_as_float(yv[2 * e + 1])), sig[q * 8 + e]),
                       lo, hi);
             sig[q * 8 + e] = 0ull;
-            if (last) {  // y[mt*128 + m][n] through a pointer stepped by N
-              if (q * 16 + 2 * e < mleft) *yp = lo;
-              yp += N;
-              if (q * 16 + 2 * e + 1 < mleft) *yp = hi;
-              yp += N;
-            } else {
-              yv[2 * e] = __float_as_uint(lo);
-              yv[2 * e + 1] = __float_as_uint(hi);
-            }
+            yv[2 * e] = __float_as_uint(lo);
+            yv[2 * e + 1] = __float_as_uint(hi);
           }
-          if (!last) tmem_st16(yc + q * 16, yv);
+          tmem_st16(dst + q * 16, yv);
         }
-        if (!last) tmem_st_wait();
-        first_seg = false;
-        return true;
+        tmem_st_wait();
+        first_seg = keep_lo;  // the high half starts from +0
+        if (!fin) return true;
+        // pass 2: the outputs (out of line: once per tile and half)
+        return pf_outputs(yc, yl, a.y + ((int64_t)mt * PF_TM + hf * 64) * a.N + (int64_t)nt * PF_TN + row, a.N,
+                          wv ? ra - hf * 64 : 0, add_lo, combine, publish, a.flags + (size_t)tile * PF_NW + warp);
       };
 
-      for (int c = 0; c < a.nch && !dead; ++c, ++kseq) {
+      for (int c = c0; c < c1 && !dead; ++c, ++kseq) {
         const int stage = (int)(kseq & 1u);
         const bool got =
             __all_sync(0xffffffffu, misc[0] == 0 && mbar_wait_bounded(&full[stage], (kseq >> 1) & 1u, WAIT_LIMIT_NS));
@@ -445,8 +537,17 @@ bool g_pf_attr[64] = {};
 
 }  // namespace
 
+// Split along K when the output tiles fill at most half of the SMs and K has
+// at least two segments: every tile becomes two CTAs (all resident at once,
+// one CTA per SM), each with half of the segments.
+bool prefill_splits(const DeviceInfo& dev, int64_t N, int64_t K, int64_t M) {
+  const int64_t tiles = ((N + PF_TN - 1) / PF_TN) * ((M + PF_TM - 1) / PF_TM);
+  const int64_t nseg = (K / QK + PF_SEG - 1) / PF_SEG;
+  return nseg >= 2 && tiles <= PF_FLAG_TILES && 2 * tiles <= dev.sm_count;
+}
+
 cudaError_t launch_prefill(const DeviceInfo& dev, const uint8_t* W, int64_t N, int64_t K, const uint8_t* A_packed,
-                           int64_t M, float* y, bool pdl, cudaStream_t s) {
+                           int64_t M, float* y, unsigned* flags, bool pdl, cudaStream_t s) {
   cudaError_t e;
   {
     std::lock_guard<std::mutex> lk(g_pf_mu);
@@ -473,7 +574,12 @@ cudaError_t launch_prefill(const DeviceInfo& dev, const uint8_t* W, int64_t N, i
   a.tm = (int)tm;
   a.tiles = (int)(tn * tm);
   a.err = err;
-  const int64_t grid = a.tiles < dev.sm_count ? a.tiles : dev.sm_count;
+  a.flags = flags;
+  const int nseg = (a.NB + PF_SEG - 1) / PF_SEG;
+  a.h = (nseg + 1) / 2;
+  a.split = prefill_splits(dev, N, K, M) ? 2 : 1;
+  const int64_t items = (int64_t)a.tiles * a.split;
+  const int64_t grid = items < dev.sm_count ? items : dev.sm_count;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(PF_THREADS);

@@ -127,12 +127,12 @@ def test_host_argument_checks_reject_before_any_device_work(lib):
     assert pf(fake, 64, 64, odd, 1, y, fake, big, 0, None) == -3               # A misaligned
     assert pf(fake, 64, 64, fake, 1, y, eight, big, 0, None) == -3             # workspace 8-aligned
     assert pf(fake, 64, 64, fake, 3, y, None, big, 0, None) == -6              # no workspace
-    assert pf(fake, 64, 64, fake, 3, y, fake, 3 * 2 * 34 - 1, 0, None) == -6   # one byte short
+    assert pf(fake, 64, 64, fake, 3, y, fake, 4096 + 208 - 1, 0, None) == -6   # one byte short (flags + packed)
     fq = lib.q8_fused_quant_gemm_prefill
     assert fq(fake, 64, 64, None, 1, y, None, fake, big, 0, None) == -1        # null x
     assert fq(fake, 64, 64, fake, 1, y, odd, fake, big, 0, None) == -3         # A_blocks_out odd
-    assert fq(fake, 64, 64, fake, 3, y, None, fake, 2 * 208 - 1, 0, None) == -6  # x's blocks need room too
-    assert lib.q8_prefill_workspace_bytes(64, 3) == 2 * 208                    # 3*2*34 = 204 -> 208, twice
+    assert fq(fake, 64, 64, fake, 3, y, None, fake, 4096 + 2 * 208 - 1, 0, None) == -6  # x's blocks need room too
+    assert lib.q8_prefill_workspace_bytes(64, 3) == 4096 + 2 * 208             # split flags + 3*2*34 = 204 -> 208, twice
     assert lib.q8_prefill_workspace_bytes(65536 + 32, 3) == 0
     assert lib.q8_prefill_workspace_bytes(64, 0) == 0
     s = lib.q8_swiglu_quantize

@@ -109,8 +109,12 @@ def test_prefill_subnormal_and_zero_scales(q8):
     assert q8.q8_device_error() == 0
 
 
-def test_prefill_rows_do_not_depend_on_the_launch(q8):
-    N, K, M = 2048, 2048, 300
+# N = 2048: every launch below splits its tiles along K over two CTAs;
+# N = 4096: the full prompt (96 tiles) does not, its slices do -- the bits
+# are the same either way
+@pytest.mark.parametrize("N", [2048, 4096])
+def test_prefill_rows_do_not_depend_on_the_launch(q8, N):
+    K, M = 2048, 300
     _, _, _, W, A = _case(q8, N, K, M, "inv")
     y = _prefill(q8, W, N, K, A, M)
     # slices of the prompt (cut inside a 128-row tile), single rows, and a
@@ -133,7 +137,9 @@ def test_fused_prefill_equals_quantize_then_prefill(q8):
     q8.q8_fused_quant_gemm_prefill(W, N, K, x, M, yf, ws, flags=q8.FLAG_PDL)
     A_out = torch.zeros_like(A)
     yf2 = torch.full_like(y, float("nan"))
-    q8.q8_fused_quant_gemm_prefill(W, N, K, x, M, yf2, ws[: ws.numel() // 2], A_blocks_out=A_out)
+    # with A_blocks_out the blocks of x need no room in the workspace
+    pk = (M * (K // 32) * 34 + 15) // 16 * 16
+    q8.q8_fused_quant_gemm_prefill(W, N, K, x, M, yf2, ws[: ws.numel() - pk], A_blocks_out=A_out)
     torch.cuda.synchronize()
     assert torch.equal(yf.view(torch.int32), y.view(torch.int32))
     assert torch.equal(yf2.view(torch.int32), y.view(torch.int32))
@@ -189,8 +195,8 @@ def test_prefill_argument_errors(q8):
     ws = q8.new_prefill_workspace(K, M)
     lib = q8.lib()
     s = torch.cuda.current_stream().cuda_stream
-    # workspace one byte short of the packed activations
-    need = ws.numel() // 2
+    # workspace one byte short of the split flags (4096 bytes) and the packed activations
+    need = 4096 + (ws.numel() - 4096) // 2
     assert lib.q8_gemm_prefill(W.data_ptr(), N, K, A.data_ptr(), M, y.data_ptr(), ws.data_ptr(), need - 1, 0,
                                s) == -6
     assert lib.q8_gemm_prefill(W.data_ptr(), N, K, A.data_ptr(), M, y.data_ptr(), ws.data_ptr(), need, 0, s) == 0
