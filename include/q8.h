@@ -369,8 +369,11 @@ Q8_API int q8_gemm_noalloc(const void *W, int64_t N, int64_t K, const void *A_bl
  *   Y_hi = +0; Y_hi = Y_hi + sigma for the high half's segments, in order;
  *   y[m][n] = Y_lo + Y_hi.
  * (IEEE single precision, round to nearest even, fma rounded once.)  The
- * two halves let a launch with few output tiles split every tile along K
- * over two CTAs without changing any bit.  This
+ * two halves let a launch with few output tiles (at most half as many as
+ * the GPU has SMs) split every tile along K over two CTAs without changing
+ * any bit; the low half's CTA then waits, bounded, for the high half's, so
+ * if other work keeps the launch's CTAs from all being resident at once the
+ * call reports a timeout through q8_device_error instead of hanging.  This
  * is not the decode order of q8_gemm, so a prefill row is not bitwise the
  * decoded row; both are within the library's tolerance of the exact sum:
  * here |y - exact| <= (17 + ceil(K/512)) * 2^-24 * S with S the sum of the
