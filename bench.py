@@ -805,13 +805,13 @@ def kv_codec(q8, shape, launches=20):
     return out
 
 
-def prefill(q8, st, M=512, steps=3, tile_rows=(512, 2048), decode_passes=True, warmup=2):
+def prefill(q8, st, M=512, steps=3, tile_rows=(128, 512, 2048), decode_passes=True, warmup=2):
     """Prefill over the same projection stack, each case one CUDA graph:
     the prefill tile GEMM (q8_fused_quant_gemm_prefill: quantize, pack, one
     tile GEMM per projection; each 128-row weight tile reused across 128
     activation rows) at `tile_rows` tokens, and for comparison the decode
-    GEMV at M rows (q8_fused_quant_gemm: passes of 16 rows, W streamed once
-    per pass).  Time per step, tokens/s; for the tile GEMM also the int8
+    GEMV at M rows (q8_fused_quant_gemm: launches of 32 rows, W streamed once
+    per launch).  Time per step, tokens/s; for the tile GEMM also the int8
     multiply-accumulate rate (2 ops per MAC) and the fraction of the
     measured dense bf16 tensor peak (fp16 operands run at the same rate)."""
     import torch
